@@ -1,0 +1,446 @@
+"""Pins of the CPU oracle against facts fixed outside the oracle itself.
+
+Each test checks the oracle against a library routine (torch / numpy casts and
+matmuls), a closed form, an invariant of the mathematics, a brute-force or
+alternative formulation, or a value printed on the pages (tests/golden).
+A plausible slip in the oracle (a dropped term, a wrong sign or index, a
+transposed operand, a swapped nibble) fails at least one of them.
+"""
+
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+rng = np.random.default_rng(1234)
+
+
+def f32(x):
+    return float(np.float32(x))
+
+
+# ------------------------------------------------------------------ codecs
+
+def test_e4m3_decode_matches_torch_for_every_code():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float32).numpy()
+    for c in range(256):
+        got = oracle.e4m3_decode(c)
+        if np.isnan(ref[c]):
+            assert math.isnan(got), c
+        else:
+            assert got == ref[c], (c, got, ref[c])
+
+
+def test_e4m3_roundtrip_every_finite_code():
+    for c in range(256):
+        if c & 0x7F == 0x7F:
+            continue
+        assert oracle.e4m3_encode(oracle.e4m3_decode(c)) == c
+
+
+def test_e4m3_encode_matches_torch_rne_on_random_values():
+    x = np.concatenate([rng.standard_normal(4000) * s for s in (1e-3, 0.05, 1.0, 30.0, 200.0)])
+    x = np.clip(x, -448, 448).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(v) for v in x], np.uint8)
+    assert (got == ref).all()
+
+
+def test_e4m3_ties_go_to_even_and_saturate():
+    # the midpoint of two neighbouring magnitudes rounds to the even code
+    for c in range(0, 126):
+        lo, hi = oracle.e4m3_decode(c), oracle.e4m3_decode(c + 1)
+        mid = (lo + hi) / 2
+        assert np.float32(mid) == mid
+        want = c if c % 2 == 0 else c + 1
+        assert oracle.e4m3_encode(mid) == want, (c, mid)
+        assert oracle.e4m3_encode(-mid) == 0x80 | want
+    for v in (448.0, 460.0, 480.0, 1e6, 3.0e38):
+        assert oracle.e4m3_encode(v) == 0x7E
+        assert oracle.e4m3_encode(-v) == 0xFE
+    assert oracle.e4m3_decode(0x7E) == 448.0
+    assert oracle.e4m3_decode(0x01) == 2.0 ** -9
+    assert oracle.e4m3_decode(0x38) == 1.0
+
+
+def test_e2m1_codes_ties_and_saturation():
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    for c in range(16):
+        v = oracle.e2m1_decode(c)
+        assert abs(v) == mags[c & 7] and (v < 0) == (c >= 8 and c != 8)
+        if c != 8:  # -0 encodes back to -0 (its sign is cleared later by the quantiser)
+            assert oracle.e2m1_encode(v) == c
+    assert oracle.e2m1_encode(-0.0) == 8
+    ties = {0.25: 0, 0.75: 2, 1.25: 2, 1.75: 4, 2.5: 4, 3.5: 6, 5.0: 6}
+    for x, c in ties.items():
+        assert oracle.e2m1_encode(x) == c, x
+        assert oracle.e2m1_encode(-x) == (8 | c), x
+    for x in (6.0, 6.5, 7.0, 100.0):
+        assert oracle.e2m1_encode(x) == 7
+    # nearest value off the midpoints
+    for x in rng.uniform(0, 6, 2000).astype(np.float32):
+        c = oracle.e2m1_encode(float(x))
+        d = [abs(float(x) - m) for m in mags]
+        assert d[c] == min(d)
+
+
+def test_bf16_encode_matches_torch():
+    x = np.concatenate([rng.standard_normal(20000).astype(np.float32),
+                        # exact ties: bf16 values plus half an ulp
+                        (rng.standard_normal(2000).astype(np.float32).view(np.uint32) & 0xFFFF0000 | 0x8000).view(np.float32)])
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([oracle.bf16_encode(float(v)) for v in x], np.uint16)
+    assert (got == ref).all()
+    for b in rng.integers(0, 0x7F80, 200):
+        assert oracle.bf16_encode(oracle.bf16_decode(int(b))) == b
+
+
+def test_e8m0_decode():
+    for c in range(255):
+        assert oracle.e8m0_decode(c) == 2.0 ** (c - 127)
+    assert math.isnan(oracle.e8m0_decode(255))
+
+
+# ------------------------------------------------------------ quant rules
+
+def test_fp8_scale_rule():
+    assert oracle.fp8_scale(0.0) == 1.0
+    assert oracle.fp8_scale(448.0) == 1.0
+    for a in rng.uniform(1e-3, 1e3, 100).astype(np.float32):
+        assert oracle.fp8_scale(float(a)) == np.float32(a) / np.float32(448.0)
+
+
+def test_mx_exponent_is_the_smallest_non_clipping_power():
+    assert oracle.mx_exponent(0.0) == 0
+    assert oracle.mx_exponent(448.0) == 0
+    assert oracle.mx_exponent(f32(np.nextafter(np.float32(448), np.float32(1e9)))) == 1
+    assert oracle.mx_exponent(224.0) == -1
+    assert oracle.mx_exponent(3.0) == -7  # 448 / 128 = 3.5 >= 3 > 1.75
+    for a in np.exp(rng.uniform(-40, 40, 2000)).astype(np.float32):
+        e = oracle.mx_exponent(float(a))
+        assert 448.0 * 2.0 ** e >= a > 448.0 * 2.0 ** (e - 1)
+
+
+def test_nvfp4_group_max_maps_to_six_and_zero_group():
+    for trial in range(300):
+        v = (rng.standard_normal(16) * 10 ** rng.uniform(-1, 2)).astype(np.float32)
+        gi = None if trial % 2 else float(np.float32(1.0) / np.float32(rng.uniform(0.5, 2)))
+        nib, sf = oracle.nvfp4_group16(v, gi)
+        k = int(np.argmax(np.abs(v)))
+        assert nib[k] & 7 == 7, (v, nib, sf)          # |max| -> 6
+        assert (nib[k] >= 8) == (v[k] < 0)
+        # every element dequantises to within one E2M1 step of its value
+        s = oracle.e4m3_decode(sf) / (1.0 if gi is None else gi)
+        deq = np.array([oracle.e2m1_decode(n) for n in nib]) * s
+        assert np.all(np.abs(deq - v) <= 2.0 * s + 1e-6)
+    nib, sf = oracle.nvfp4_group16(np.zeros(16, np.float32), None)
+    assert sf == 0x01 and not nib.any()              # scale floored at 2^-9
+    v = np.zeros(16, np.float32)
+    v[0], v[1] = 12.0, -1e-4                          # tiny negative -> +0
+    nib, sf = oracle.nvfp4_group16(v, None)
+    assert nib[1] == 0 and nib[0] == 7
+
+
+def test_nvfp4_sign_clearing_matches_the_pages_word_trick():
+    # the qkv_index_fused_epilogue page (_nvfp4_quant32) clears the sign of
+    # zero-magnitude nibbles on packed words with w & (((w & m) + m) | m),
+    # m = 0x77777777; the oracle clears them one nibble at a time
+    m = 0x77777777
+    for _ in range(2000):
+        nibs = rng.integers(0, 16, 8)
+        w = 0
+        for j, n in enumerate(nibs):
+            w |= int(n) << (4 * j)
+        cleared = w & ((((w & m) + m) | m)) & 0xFFFFFFFF
+        want = 0
+        for j, n in enumerate(nibs):
+            n = 0 if (n & 7) == 0 else int(n)
+            want |= n << (4 * j)
+        assert cleared == want
+
+
+# ------------------------------------------------------- norm and rope
+
+def test_head_rmsnorm_unit_rms_with_zero_gamma_and_constant_rows():
+    g0 = np.zeros(128, np.uint16)  # bf16 0.0
+    for _ in range(20):
+        y = (rng.standard_normal(128) * 10 ** rng.uniform(-2, 2)).astype(np.float32)
+        z = oracle.head_rmsnorm(y, g0, 1e-6)
+        ms = float(np.mean(y.astype(np.float64) ** 2))
+        eps = float(np.float32(1e-6))  # eps is an f32 argument
+        assert abs(math.sqrt(np.mean(z ** 2)) - math.sqrt(ms / (ms + eps))) < 1e-12
+    gam = np.array([oracle.bf16_encode(v) for v in rng.standard_normal(128) * 0.1], np.uint16)
+    gd = np.array([oracle.bf16_decode(b) for b in gam])
+    z = oracle.head_rmsnorm(np.full(128, -3.0, np.float32), gam, 0.0)
+    assert np.allclose(z, -(1.0 + gd), rtol=0, atol=1e-12)
+
+
+def test_rope_identity_rotation_and_norms():
+    z = rng.standard_normal(128)
+    tab = workloads.cos_sin_table(4096)
+    # position 0: cos = 1, sin = 0 exactly in bf16 -> identity
+    assert np.array_equal(oracle.rope_neox(z, tab[0]), z)
+    for p in rng.integers(1, 4096, 50):
+        out = oracle.rope_neox(z, tab[p])
+        assert np.array_equal(out[64:], z[64:])
+        c = np.array([oracle.bf16_decode(b) for b in tab[p][:32]])
+        s = np.array([oracle.bf16_decode(b) for b in tab[p][32:]])
+        n_in = z[:32] ** 2 + z[32:64] ** 2
+        n_out = out[:32] ** 2 + out[32:64] ** 2
+        assert np.allclose(n_out, n_in * (c ** 2 + s ** 2), rtol=1e-12, atol=1e-12)
+        assert np.all(np.abs(c ** 2 + s ** 2 - 1) < 2 ** -6)
+    # a quarter turn (cos 0, sin 1): x' = -y, y' = x
+    quarter = np.array([oracle.bf16_encode(0.0)] * 32 + [oracle.bf16_encode(1.0)] * 32, np.uint16)
+    out = oracle.rope_neox(z, quarter)
+    assert np.array_equal(out[:32], -z[32:64]) and np.array_equal(out[32:64], z[:32])
+
+
+# -------------------------------------------------------------- prologue
+
+def _cfg(H=512, weight_fmt=0, eps=1e-6):
+    return oracle.Config(H, 16, 1, 1, 1, weight_fmt, 0, 16, 8, 0, eps)
+
+
+def test_prologue_residual_matches_torch_f32_sum():
+    H = 512
+    a = torch.randn(H, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16)
+    b = (torch.randn(H, generator=torch.Generator().manual_seed(6)) * 100).to(torch.bfloat16)
+    ref = (a.float() + b.float()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    ar = a.view(torch.int16).numpy().view(np.uint16)
+    res = b.view(torch.int16).numpy().view(np.uint16)
+    residual, xq, xs, _ = oracle.prologue_row(_cfg(H), ar, res, np.zeros(H, np.uint16))
+    assert np.array_equal(residual, ref)
+
+
+def test_prologue_per_token_amax_maps_to_448_and_unit_rms():
+    H = 512
+    for seed in range(5):
+        g = torch.Generator().manual_seed(seed)
+        ar = workloads._bf16_bits(torch.randn(H, generator=g) * 3)
+        res = workloads._bf16_bits(torch.randn(H, generator=g))
+        _, xq, xs, _ = oracle.prologue_row(_cfg(H), ar, res, np.zeros(H, np.uint16))
+        deq = np.array([oracle.e4m3_decode(c) for c in xq])
+        assert np.max(np.abs(deq)) == 448.0
+        n = deq * xs
+        assert abs(math.sqrt(np.mean(n ** 2)) - 1.0) < 0.03  # gamma = 0 -> unit RMS, FP8 noise
+    # a constant row normalises to +-1 * (1 + gamma): every code is +-448
+    ar = np.full(H, oracle.bf16_encode(2.0), np.uint16)
+    res = np.full(H, oracle.bf16_encode(-0.5), np.uint16)
+    _, xq, xs, _ = oracle.prologue_row(_cfg(H, eps=0.0), ar, res, np.zeros(H, np.uint16))
+    assert (xq == 0x7E).all() and xs == np.float32(1.0) / np.float32(448.0)
+
+
+def test_prologue_mx_blocks():
+    H = 512
+    g = torch.Generator().manual_seed(9)
+    ar = workloads._bf16_bits(torch.randn(H, generator=g))
+    res = workloads._bf16_bits(torch.randn(H, generator=g) * 4)
+    _, xq, _, xsf = oracle.prologue_row(_cfg(H, weight_fmt=1), ar, res, np.zeros(H, np.uint16))
+    deq = np.array([oracle.e4m3_decode(c) for c in xq]).reshape(H // 32, 32)
+    bmax = np.abs(deq).max(axis=1)
+    assert np.all((bmax >= 224.0) & (bmax <= 448.0))  # minimal power of two
+    n = deq * np.array([oracle.e8m0_decode(c) for c in xsf])[:, None]
+    assert abs(math.sqrt(np.mean(n ** 2)) - 1.0) < 0.03
+
+
+# ------------------------------------------------------------ projection
+
+@pytest.mark.parametrize("fmt", ["ptpc", "mx"])
+def test_projection_equals_numpy_matmul_of_dequantised_operands(fmt):
+    wl = workloads.tiny().replace(weight_fmt=fmt, M=3)
+    st = workloads.host_state(wl)
+    cfg = oracle.oracle_config(wl)
+    lut = np.array([oracle.e4m3_decode(c) for c in range(256)], np.float64)
+    lut[np.isnan(lut)] = 0
+    W = lut[st["w"]]
+    if fmt == "ptpc":
+        W = W * st["w_scale"].astype(np.float64)[:, None]
+    else:
+        W = W * np.repeat(2.0 ** (st["wsf"].astype(np.float64) - 127), 32, axis=1)
+    for m in range(wl.M):
+        _, xq, xs, xsf = oracle.prologue_row(cfg, st["ar"][m], st["res"][m], st["g_in"])
+        x = lut[xq] * (xs if fmt == "ptpc" else np.repeat(2.0 ** (xsf.astype(np.float64) - 127), 32))
+        ref = W @ x
+        y = oracle.project_row(cfg, xq, xs, xsf if fmt == "mx" else None, st["w"],
+                               st.get("w_scale"), st.get("wsf"))
+        assert np.allclose(y, ref, rtol=1e-6, atol=1e-6)
+
+
+# ----------------------------------------------------------------- layouts
+
+def _load_golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                rows.append([int(v) for v in line.split()])
+    return rows
+
+
+def test_layout_offsets_match_values_worked_from_the_pages():
+    L = oracle.lib()
+    for kind, *args, want in _load_golden("layout_offsets.txt"):
+        if kind == 0:    # fp8 K shuffle: page16, h, nkv, t, d
+            got = L.ora_fp8_k_offset(*args)
+        elif kind == 1:  # fp8 V: page16, h, nkv, t, d
+            got = L.ora_fp8_v_offset(*args)
+        elif kind == 2:  # nvfp4 V-swizzled scale: bs, slot, t, g
+            got = L.ora_nvfp4_sf_vswz_offset(*args)
+        elif kind == 3:  # nvfp4 linear scale: bs, slot, t, g
+            got = L.ora_nvfp4_sf_linear_offset(*args)
+        elif kind == 4:  # nvfp4 data byte: bs, slot, t, d
+            got = L.ora_nvfp4_data_offset(*args)
+        elif kind == 5:  # page16_of: slot, kps
+            got = L.ora_page16_of(*args)
+        elif kind == 6:  # F8_128x4: r, kb, ksf
+            got = L.ora_sf128x4_offset(*args)
+        assert got == want, (kind, args, got, want)
+
+
+def _cute_offset(coord_shape_stride):
+    """Evaluate a CuTe layout (shape, stride) at a flat-per-mode coordinate."""
+    off = 0
+    for idx, shape, stride in coord_shape_stride:
+        if isinstance(shape, tuple):
+            for s, d in zip(shape, stride):
+                off += (idx % s) * d
+                idx //= s
+        else:
+            off += idx * stride
+    return off
+
+
+@pytest.mark.parametrize("bs", [4, 16, 32])
+def test_nvfp4_views_agree_with_the_pages_cute_layouts(bs):
+    L = oracle.lib()
+    slot_bytes = bs * 72
+    for s in range(3):
+        for t in range(bs):
+            for g in range(8):
+                # vsf: ((2,4),(4,bs//4),nslots) : ((4,8),(1,32),slot_bytes) + sf_off
+                want = bs * 64 + _cute_offset([(g, (2, 4), (4, 8)), (t, (4, bs // 4), (1, 32)),
+                                               (s, 0, slot_bytes)])
+                assert L.ora_nvfp4_sf_vswz_offset(bs, s, t, g) == want
+                # sf: (8, bs, nslots) : (1, 8, slot_bytes) + sf_off
+                want = bs * 64 + g + 8 * t + s * slot_bytes
+                assert L.ora_nvfp4_sf_linear_offset(bs, s, t, g) == want
+            for d in range(0, 128, 2):
+                # data as bytes: (32, 2, bs, nslots) : (1, 32, 64, slot_bytes)
+                want = _cute_offset([((d % 64) // 2, 0, 1), (d // 64, 0, 32), (t, 0, 64), (s, 0, slot_bytes)])
+                assert L.ora_nvfp4_data_offset(bs, s, t, d) == want
+
+
+def test_sf128x4_pack_matches_the_pages_permutation():
+    for R, ksf in ((128, 4), (256, 16), (300, 8), (9856, 192)):
+        src = rng.integers(0, 255, (R, ksf)).astype(np.uint8)
+        got = oracle.pack_sf128x4(src, pad=0)
+        rp = (R + 127) // 128 * 128
+        pad = np.zeros((rp, ksf), np.uint8)
+        pad[:R] = src
+        # [R/128, Ksf/4, 32, 4, 4]: (row block, k quad, row % 32, (row % 128) / 32, k % 4)
+        want = pad.reshape(rp // 128, 4, 32, ksf // 4, 4).transpose(0, 3, 2, 1, 4).reshape(-1)
+        assert np.array_equal(got, want)
+
+
+# --------------------------------------------------------- the whole step
+
+def _dequant_fp8_k_token(st, wl, slot, h):
+    p16, t = slot // 16, slot % 16
+    page = st["k_cache"].reshape(-1, wl.nkv, 2048)[p16, h]
+    codes = page.reshape(8, 16, 16)[:, t, :].reshape(128)  # [d/16][t][d%16]
+    return codes
+
+
+def test_step_fp8_caches_touch_only_the_slots_and_decode_consistently():
+    wl = workloads.tiny().replace(q_fp8=True, iq_fp8=True, skip_rows=(2,))
+    st = workloads.host_state(wl)
+    y = oracle.run_rows(wl, st, range(wl.M), want_y=True)
+    fresh = workloads.host_state(wl)
+    touched_pages = set()
+    for m in range(wl.M):
+        slot = int(st["slot_mapping"][m])
+        if slot < 0:
+            continue
+        touched_pages.add(slot // 16)
+    # untouched pages keep the sentinel
+    kc = st["k_cache"].reshape(-1, wl.nkv, 2048)
+    for p in range(wl.num_pages16):
+        if p not in touched_pages:
+            assert (kc[p] == workloads.SENTINEL).all()
+    for m in range(wl.M):
+        slot = int(st["slot_mapping"][m])
+        if slot < 0:
+            continue
+        p16, t = slot // 16, slot % 16
+        # V codes sit transposed ([d][t]); dequantised they match the raw projection
+        vpage = st["v_cache"].reshape(-1, wl.nkv, 2048)[p16, 0].reshape(128, 16)
+        vs = st["v_scale"].reshape(-1, wl.nkv, 16)[p16, 0, t]
+        v = y[m, (wl.n_q + wl.nkv) * 128:(wl.n_q + wl.nkv + 1) * 128]
+        deq = np.array([oracle.e4m3_decode(c) for c in vpage[:, t]]) * vs
+        assert np.allclose(deq, v, rtol=2 ** -3, atol=vs * 2 ** -8)
+        assert abs(np.max(np.abs(v)) / 448.0 - vs) <= 1e-6 * vs
+        # K codes in the shuffle order decode to bf16(norm + rope of k) / ks
+        kcodes = _dequant_fp8_k_token(st, wl, slot, 0)
+        ks = st["k_scale"].reshape(-1, wl.nkv, 16)[p16, 0, t]
+        assert max(abs(oracle.e4m3_decode(c)) for c in kcodes) == 448.0
+        # the k head's q-like output is not written anywhere else: compare
+        # against norm + rope recomputed from y
+        k = y[m, wl.n_q * 128:(wl.n_q + 1) * 128]
+        z = oracle.rope_neox(oracle.head_rmsnorm(k, st["g_k"], wl.eps), st["cos_sin"][st["positions"][m]])
+        deq = np.array([oracle.e4m3_decode(c) for c in kcodes]) * ks
+        assert np.allclose(deq, z, rtol=2 ** -3, atol=ks * 2 ** -8)
+        # the index cache row holds e4m3(bf16(index_k))
+        ik = y[m, (wl.n_heads - 1) * 128:]
+        z = oracle.rope_neox(oracle.head_rmsnorm(ik, st["g_ik"], wl.eps), st["cos_sin"][st["positions"][m]])
+        row = st["index_cache"].reshape(-1, 128)[slot]
+        assert np.allclose([oracle.e4m3_decode(c) for c in row], z, rtol=2 ** -3, atol=2 ** -9)
+    # the skipped row wrote no cache byte but still wrote q
+    assert (st["q_bf16"][2] != 0xA5A5).all()
+    # q_fp8 and q_bf16 agree within FP8 precision
+    qb = np.array([oracle.bf16_decode(b) for b in st["q_bf16"].reshape(-1)])
+    qf = np.array([oracle.e4m3_decode(c) for c in st["q_fp8"].reshape(-1)])
+    assert np.allclose(qf, qb, rtol=2 ** -4, atol=2 ** -9)
+    assert not np.array_equal(fresh["k_cache"], st["k_cache"])
+
+
+def test_step_nvfp4_caches_decode_consistently():
+    wl = workloads.Workload("t4", H=512, nkv=2, M=6, weight_fmt="mx", cache_fmt="nvfp4", seed=7,
+                            positions="uniform", max_pos=512, pool_pages=32, q_fp8=True,
+                            iq_fp8=True, page_pad=64, k_global=0.5, v_global=2.0)
+    st = workloads.host_state(wl)
+    y = oracle.run_rows(wl, st, range(wl.M), want_y=True)
+    bs = wl.block_size
+    for m in range(wl.M):
+        slot = int(st["slot_mapping"][m])
+        page = st["kv_cache"].reshape(wl.kv_pages, wl.kv_page_bytes)[slot // bs]
+        t = slot % bs
+        for h in range(wl.nkv):
+            for role, gsc in (("k", wl.k_global), ("v", wl.v_global)):
+                sl = 2 * h + (role == "v")
+                blk = page[sl * bs * 72:(sl + 1) * bs * 72]
+                data = blk[:bs * 64].reshape(bs, 2, 32)[t].reshape(64)
+                nib = np.stack([data & 15, data >> 4], axis=1).reshape(128)  # even element low
+                sfb = blk[bs * 64:].reshape(bs // 4, 8, 4) if role == "v" else blk[bs * 64:].reshape(bs, 8)
+                if role == "v":  # byte g of token t at (t/4*4 + g/2)*8 + g%2*4 + t%4
+                    sfs = [blk[bs * 64 + ((t // 4) * 4 + g // 2) * 8 + (g % 2) * 4 + t % 4] for g in range(8)]
+                else:
+                    sfs = list(sfb[t])
+                deq = np.array([oracle.e2m1_decode(n) for n in nib]) * np.repeat(
+                    [oracle.e4m3_decode(s) for s in sfs], 16) * gsc
+                if role == "v":
+                    ref = y[m, (wl.n_q + wl.nkv + h) * 128:(wl.n_q + wl.nkv + h + 1) * 128]
+                else:
+                    k = y[m, (wl.n_q + h) * 128:(wl.n_q + h + 1) * 128]
+                    ref = oracle.rope_neox(oracle.head_rmsnorm(k, st["g_k"], wl.eps),
+                                           st["cos_sin"][st["positions"][m]])
+                gmax = np.abs(ref).reshape(8, 16).max(axis=1)
+                tol = np.repeat(gmax, 16) / 6 * 1.07 + 1e-6
+                assert np.all(np.abs(deq - ref) <= tol), (m, h, role)
