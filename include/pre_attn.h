@@ -1,0 +1,252 @@
+/*
+ * pre_attn — GB300 (sm_103a) MiniMax-M3 sparse-layer pre-attention step.
+ *
+ * One call of pre_attn_run() performs, for each of M token rows:
+ *   1. residual add: acc = ar + res in f32, residual_out = bf16(acc)
+ *      (page "vllm.models.minimax_m3.amd.mono.kernels.pre_attn", module
+ *      summary and emit_pre_attn / norm_quant);
+ *   2. Gemma RMSNorm: n = acc * rsqrt(mean(acc^2) + eps) * (1 + g_in);
+ *   3. activation quantisation: per-token FP8 E4M3 (scale = amax / 448, a
+ *      true divide) for PA_WEIGHT_FP8_PER_CHANNEL, or MXFP8 (32-element
+ *      blocks along H with E8M0 scales) for PA_WEIGHT_MXFP8;
+ *   4. the fused projection y = xq . W^T (f32 accumulation) into
+ *      [q x n_q | k x n_kv | v x n_kv | index_q x n_iq | index_k x 1]
+ *      128-dim heads (page "vllm.models.minimax_m3.nvidia.ops.
+ *      qkv_index_fused_epilogue", QkvIndexFusedEpilogueKernel: N layout);
+ *   5. per head: Gemma RMSNorm + partial NeoX RoPE (rotary dim 64 of 128)
+ *      on the f32 accumulator for q, k, index_q and index_k; v stays raw
+ *      (pre_attn page, head_norm_rope; epilogue page, _rms_norm / _rope64);
+ *   6. q and index_q outputs (bf16 and / or E4M3);
+ *   7. K, V and index_k quantised and inserted into paged caches through
+ *      slot_mapping: FP8 with per-token scales (pre_attn page, head tasks)
+ *      or NVFP4 (epilogue page, _nvfp4_quant32 / _nvfp4_cache_views).
+ * The projection y is never written to memory as a whole.
+ *
+ * Conventions (all entry points):
+ *   - Every pointer argument that names tensor data is a DEVICE pointer owned
+ *     by the caller, unless documented as host.  The library owns only its
+ *     handle (host memory) and its compiled kernels.
+ *   - pre_attn_run() is asynchronous on `stream` (a cudaStream_t passed as
+ *     void*; NULL = the legacy default stream), allocates nothing and never
+ *     synchronises.  Host-checkable argument errors return a PA_ERR_* code
+ *     before anything is launched; nothing aborts.
+ *   - Values that live in device memory (positions, slots) cannot be checked
+ *     on the host.  The kernels skip any cache store whose slot is out of the
+ *     cache's range and clamp an out-of-range position into the cos/sin
+ *     table; each such event sets a bit in the workspace's status word
+ *     (PA_DEV_*), read with pre_attn_device_status().
+ *   - All matrices are row-major and densely packed unless a stride is given.
+ *   - bf16 is IEEE binary16-brain; e4m3 is OCP FP8 E4M3 ("fn"); E8M0 is an
+ *     unsigned power-of-two exponent with bias 127; E2M1 is OCP FP4.
+ */
+#ifndef PRE_ATTN_H
+#define PRE_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------ status */
+enum pa_status {
+  PA_OK = 0,
+  PA_ERR_NULL = 1,        /* a required pointer is NULL */
+  PA_ERR_CONFIG = 2,      /* configuration outside the supported set */
+  PA_ERR_SHAPE = 3,       /* M < 0, M > max_tokens, or a size is inconsistent */
+  PA_ERR_ALIGN = 4,       /* a pointer or stride violates its alignment rule */
+  PA_ERR_NO_Q_OUTPUT = 5, /* neither q output requested (epilogue page asserts one) */
+  PA_ERR_NO_IQ_OUTPUT = 6,/* neither index_q output requested */
+  PA_ERR_ALIAS = 7,       /* residual_out overlaps ar or res (not supported) */
+  PA_ERR_WORKSPACE = 8,   /* workspace NULL or smaller than pre_attn_workspace_bytes */
+  PA_ERR_CUDA = 9,        /* a CUDA runtime call failed (launch, attribute, query) */
+  PA_ERR_UNSUPPORTED = 10 /* a valid request this build does not implement */
+};
+
+/* Bits of the device status word (sticky until pre_attn_device_status). */
+enum pa_device_status {
+  PA_DEV_SLOT_RANGE = 1u << 0,  /* a slot pointed outside its cache: store skipped */
+  PA_DEV_POS_RANGE = 1u << 1,   /* a position outside [0, max_pos): clamped */
+  PA_DEV_WAIT_TIMEOUT = 1u << 2 /* a bounded device wait gave up (results invalid) */
+};
+
+/* ---------------------------------------------------------- formats */
+enum pa_weight_format {
+  /* [N, H] e4m3 + [N] f32 per-output-channel scales; activations per-token
+   * FP8 (pre_attn page, GEMV tasks: "ptpc-FP8"). */
+  PA_WEIGHT_FP8_PER_CHANNEL = 0,
+  /* [N, H] e4m3 + E8M0 scales per 32-element K block in the F8_128x4 layout
+   * (epilogue page, prepare_SF); activations MXFP8 with the same blocks. */
+  PA_WEIGHT_MXFP8 = 1
+};
+
+enum pa_cache_format {
+  /* Page-16 FP8 caches with per-token f32 K / V scales (pre_attn page, head
+   * tasks).  Per page16 p and KV head h (page-major, head-minor):
+   *   K byte (p*n_kv + h)*2048 + (d/16)*256 + t*16 + d%16   ("SHUFFLE")
+   *   V byte (p*n_kv + h)*2048 + d*16 + t                     (transposed)
+   *   k_scale / v_scale f32 at (p*n_kv + h)*16 + t
+   * with p = page16_of(slot), t = slot % 16, d the head dim.  The index
+   * cache is [num_index_slots, 128] e4m3 (unit scale) at islot*128 + d. */
+  PA_CACHE_FP8 = 0,
+  /* NVFP4 caches (epilogue page, _nvfp4_cache_views): the KV cache is
+   * kv_pages pages of kv_page_bytes; page = slot / bs holds 2*n_kv slots of
+   * bs*72 bytes (K of KV head h in slot 2h, V in slot 2h+1); within a slot,
+   * token t's 128 E2M1 values take bytes t*64 + (d/64)*32 + (d%64)/2 (even
+   * d in the low nibble), then the 8 E4M3 group scales (16 dims each) sit
+   * after bs*64 data bytes: K and index_k linear at t*8 + g, V swizzled at
+   * (t/4*4 + g/2)*8 + (g%2)*4 + t%4.  The index cache has one slot per page. */
+  PA_CACHE_NVFP4 = 1
+};
+
+enum pa_flags {
+  PA_FLAG_STATIC_KV_SCALE = 1 << 0, /* FP8 caches: K / V scales fixed at 1 */
+  PA_FLAG_FORCE_GEMV = 1 << 1,      /* testing: the skinny path for any M <= 16 */
+  PA_FLAG_FORCE_GEMM = 1 << 2,      /* testing: the tensor-core GEMM path for any M */
+  PA_FLAG_NO_PDL = 1 << 3           /* launch without programmatic dependent launch */
+};
+
+/* ----------------------------------------------------------- config */
+typedef struct pa_config {
+  int hidden;        /* H, the projection's K: a multiple of 128, <= 16384 */
+  int n_kv_heads;    /* n_kv in {1, 2, 4} (epilogue page, kernel __init__) */
+  int n_q_heads;     /* 0 -> 16 * n_kv (the pages' layout) */
+  int n_iq_heads;    /* 0 -> n_kv */
+  int weight_format; /* enum pa_weight_format */
+  int cache_format;  /* enum pa_cache_format */
+  int block_size;    /* tokens per cache page: 16 for PA_CACHE_FP8; for
+                        PA_CACHE_NVFP4 a multiple of 4 (V scale swizzle) */
+  int kv_page_stride;/* FP8 page16_of (pre_attn page): page-16 blocks per
+                        128-token block; 0 or 8 -> page16 = slot / 16 */
+  float eps;         /* RMSNorm epsilon, input and head norms */
+  int max_tokens;    /* largest M pre_attn_run accepts (sizes the workspace) */
+  int flags;         /* enum pa_flags */
+  int gemm_grid;     /* testing: persistent GEMM grid override (0 = auto) */
+} pa_config;
+
+typedef struct pa_handle pa_handle;
+
+/* Per-layer parameters; static across steps.  All device pointers. */
+typedef struct pa_weights {
+  const void *w;        /* [N, H] e4m3, row-major (K-major), N = n_heads*128 */
+  const void *w_scale;  /* per-channel: [N] f32.  MXFP8: E8M0 in the
+                           F8_128x4 layout of [N, H/32] (pre_attn_pack_scales) */
+  const void *g_in;     /* [H] bf16 input-norm gamma */
+  const void *g_q, *g_k, *g_iq, *g_ik; /* [128] bf16 head-norm gammas */
+  const void *cos_sin;  /* [max_pos, 64] bf16: cos[32] | sin[32] per position */
+  int64_t max_pos;
+} pa_weights;
+
+/* Per-step inputs.  All device pointers. */
+typedef struct pa_step_inputs {
+  const void *ar;                    /* [M, H] bf16: the all-reduce output */
+  const void *res;                   /* [M, H] bf16: the residual stream */
+  const int64_t *positions;          /* [M] token positions (cos_sin rows) */
+  const int64_t *slot_mapping;       /* [M] KV-cache slots, -1 = skip */
+  const int64_t *index_slot_mapping; /* [M] index-cache slots, -1 = skip;
+                                        NULL -> slot_mapping */
+} pa_step_inputs;
+
+/* Caches, written in place at the rows' slots.  Device pointers. */
+typedef struct pa_caches {
+  /* PA_CACHE_FP8 */
+  void *k_cache, *v_cache;      /* num_pages16 * n_kv * 2048 bytes each */
+  float *k_scale, *v_scale;     /* num_pages16 * n_kv * 16 f32 each */
+  void *index_cache;            /* num_index_slots * 128 bytes */
+  int64_t num_pages16;
+  int64_t num_index_slots;
+  /* PA_CACHE_NVFP4 (base pointers and page strides: multiples of 32) */
+  void *kv_cache;
+  int64_t kv_pages, kv_page_bytes;   /* kv_page_bytes >= 2*n_kv*bs*72 */
+  void *idx_cache;
+  int64_t idx_pages, idx_page_bytes; /* idx_page_bytes >= bs*72 */
+  float k_global_scale, v_global_scale; /* NVFP4 dequantisation scales (> 0) */
+} pa_caches;
+
+/* Outputs.  Device pointers; NULL = not written.  At least one q output and
+ * one index_q output must be given. */
+typedef struct pa_outputs {
+  void *residual;   /* [M, H] bf16 = bf16(ar + res); must not overlap ar/res */
+  void *q;          /* [M, n_q*128] bf16, normed + roped */
+  void *q_fp8;      /* [M, n_q*128] e4m3 of q * (1 / q_fp8_scale) */
+  void *iq;         /* [M, n_iq*128] bf16 index_q */
+  void *iq_fp8;     /* [M, n_iq*128] e4m3 index_q, unit scale */
+  float q_fp8_scale;/* dequantisation scale of q_fp8 (> 0) */
+} pa_outputs;
+
+/* --------------------------------------------------------- entry points */
+
+/* Validate `cfg` and create a handle (host memory only; no CUDA call).
+ * Errors: PA_ERR_NULL, PA_ERR_CONFIG (n_kv not in {1,2,4}, H % 128 != 0 or
+ * H > 16384, head counts < 1, FP8 caches with block_size != 16, NVFP4 with
+ * block_size % 4 != 0, eps < 0, max_tokens < 0, unknown format). */
+int pre_attn_init(const pa_config *cfg, pa_handle **out);
+
+/* Free a handle (NULL is ignored). */
+void pre_attn_destroy(pa_handle *h);
+
+/* A static English description of a pa_status code. */
+const char *pre_attn_strerror(int status);
+
+/* The fused projection's output width N = n_heads * 128 for this handle. */
+int pre_attn_out_features(const pa_handle *h);
+
+/* Bytes of device workspace pre_attn_run needs for up to M rows (M <= the
+ * handle's max_tokens), including a status word and the skinny path's
+ * per-head arrival counters.  Returns 0 for an invalid handle or M. */
+size_t pre_attn_workspace_bytes(const pa_handle *h, int M);
+
+/* Zero a freshly allocated workspace (cudaMemsetAsync on `stream`).  Must be
+ * called once before the workspace's first pre_attn_run; the kernels keep
+ * it valid afterwards.  Errors: PA_ERR_NULL, PA_ERR_CUDA. */
+int pre_attn_workspace_init(void *workspace, size_t bytes, void *stream);
+
+/* Bytes of the F8_128x4 layout for an [rows, hidden/32] E8M0 grid
+ * (rows padded to a multiple of 128). */
+size_t pre_attn_packed_scale_bytes(int rows, int hidden);
+
+/* Re-lay a row-major [rows, hidden/32] E8M0 scale grid (device, src) into
+ * the F8_128x4 layout (epilogue page, prepare_SF: [R/128, Ksf/4, 32, 4, 4])
+ * that PA_WEIGHT_MXFP8 expects in pa_weights.w_scale (device, dst of
+ * pre_attn_packed_scale_bytes bytes; padding rows get code 127).  Run once
+ * when the weights are loaded.  Asynchronous on `stream`.
+ * Errors: PA_ERR_NULL, PA_ERR_SHAPE (rows < 1, hidden % 128), PA_ERR_CUDA. */
+int pre_attn_pack_scales(const void *src, void *dst, int rows, int hidden, void *stream);
+
+/* Run the step on M rows (0 <= M <= max_tokens; M == 0 launches nothing).
+ * `workspace` is a device buffer of at least pre_attn_workspace_bytes(h, M)
+ * bytes, initialised once with pre_attn_workspace_init; calls that share a
+ * workspace must be ordered on the GPU (one stream, or events).
+ * Alignment: ar, res, residual, w, g_in and the outputs 16 bytes; NVFP4
+ * cache bases and page strides 32 bytes (epilogue page, argument asserts).
+ * Errors (nothing is launched): PA_ERR_NULL, PA_ERR_SHAPE, PA_ERR_ALIGN,
+ * PA_ERR_NO_Q_OUTPUT, PA_ERR_NO_IQ_OUTPUT, PA_ERR_ALIAS, PA_ERR_WORKSPACE,
+ * PA_ERR_CONFIG (bad cache geometry or scales); PA_ERR_CUDA if a launch
+ * fails (an earlier kernel of the call may have run). */
+int pre_attn_run(pa_handle *h, int M, const pa_step_inputs *in, const pa_weights *wt,
+                 const pa_caches *caches, const pa_outputs *out, void *workspace,
+                 size_t workspace_bytes, void *stream);
+
+/* Read and clear the workspace's device status word (PA_DEV_* bits) into
+ * *flags (host).  Synchronises `stream`.  Errors: PA_ERR_NULL, PA_ERR_CUDA. */
+int pre_attn_device_status(void *workspace, uint32_t *flags, void *stream);
+
+/* Profiling aid (the equivalent of the pre_attn page's `timeline` stamps):
+ * when set, every later pre_attn_run() on this handle records `before_main`
+ * and `after_main` (cudaEvent_t passed as void*; NULL = none) on its stream
+ * immediately before and after the step's main kernel (the skinny GEMV or
+ * the tensor-core GEMM), so cudaEventElapsedTime gives that kernel's device
+ * time.  Recording between the kernels serialises them (no programmatic
+ * overlap of the main kernel with the prologue), so use it for kernel timing
+ * only.  The caller owns the events.  Errors: PA_ERR_NULL (h). */
+int pre_attn_set_profile_events(pa_handle *h, void *before_main, void *after_main);
+
+/* The last CUDA error string seen by this thread's calls ("" if none). */
+const char *pre_attn_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PRE_ATTN_H */

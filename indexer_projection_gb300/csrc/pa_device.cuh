@@ -1,0 +1,468 @@
+// Device-side building blocks of the pre-attention step for sm_103a:
+// kernel parameters, PTX wrappers (mbarrier, bulk copies, programmatic
+// dependent launch, legacy mma.sync for the skinny path), FP8 / FP4 codecs
+// and the per-head epilogue (Gemma RMSNorm, partial NeoX RoPE, q / index_q
+// outputs, FP8 and NVFP4 paged-cache insertion).
+//
+// Pages cited:
+//   [K1]  "vllm.models.minimax_m3.amd.mono.kernels.pre_attn" (K1 mono_pre)
+//   [EPI] "vllm.models.minimax_m3.nvidia.ops.qkv_index_fused_epilogue"
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+constexpr int kHeadDim = 128;
+constexpr int kRotDim = 64;
+constexpr int kHalfRot = 32;
+constexpr float kFp8Max = 448.0f;
+constexpr uint32_t kDevSlotRange = 1u << 0;
+constexpr uint32_t kDevPosRange = 1u << 1;
+constexpr uint32_t kDevWaitTimeout = 1u << 2;
+
+// Everything a kernel of the step reads or writes.  Passed by value.
+struct Params {
+  int M, H, N, n_heads;
+  int n_q, n_kv, n_iq;
+  int k0, v0, iq0, ik0;  // first head of each role
+  int weight_fmt;        // 0 per-channel FP8, 1 MXFP8
+  int cache_fmt;         // 0 FP8, 1 NVFP4
+  int bs;                // tokens per page
+  int kps;               // FP8 page16_of stride (8 = identity)
+  int static_kv;         // FP8 caches: K / V scale fixed at 1
+  float eps;
+  // inputs
+  const __nv_bfloat16 *ar, *res, *g_in;
+  const uint8_t *w;
+  const float *w_scale;      // per-channel [N]
+  const uint8_t *wsf;        // MXFP8, F8_128x4 layout of [N, H/32]
+  const __nv_bfloat16 *g_q, *g_k, *g_iq, *g_ik, *cos_sin;
+  int64_t max_pos;
+  const int64_t *pos, *slot, *islot;
+  // caches
+  uint8_t *k_cache, *v_cache, *index_cache;
+  float *k_scale, *v_scale;
+  int64_t num_pages16, num_index_slots;
+  uint8_t *kv_cache, *idx_cache;
+  int64_t kv_pages, kv_page_bytes, idx_pages, idx_page_bytes;
+  float k_gs_inv, v_gs_inv;  // 1 / global NVFP4 scales (f32 reciprocal)
+  // outputs
+  __nv_bfloat16 *residual, *q, *iq;
+  uint8_t *q_fp8, *iq_fp8;
+  float q_fp8_inv;           // 1 / q_fp8_scale (f32 reciprocal)
+  // workspace
+  uint32_t *status;
+  int *head_cnt;             // [n_heads] arrival counters (skinny path)
+  uint8_t *xq;               // [M, H] e4m3 activations
+  float *x_scale;            // [M] per-token scales (per-channel format)
+  uint8_t *xsf;              // MXFP8 activation scales, F8_128x4 of [Mpad, H/32]
+  float *y;                  // [M, N] f32 projection rows (skinny path only)
+  int m_pad;                 // M rounded up to 128 (MXFP8 scale rows)
+};
+
+// ------------------------------------------------------------ small utils
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+__device__ __forceinline__ float bf16_round(float f) { return bf16_to_f32(f32_to_bf16_bits(f)); }
+
+// Two f32 -> two E4M3 (round to nearest even, saturate to +-448); lo in the low byte.
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  return (uint32_t)e4m3x2(a, b) | ((uint32_t)e4m3x2(c, d) << 16);
+}
+__device__ __forceinline__ uint8_t e4m3(float a) { return (uint8_t)(e4m3x2(a, 0.0f) & 0xff); }
+__device__ __forceinline__ float e4m3_to_f32(uint8_t c) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((uint16_t)c));
+  return __half2float(__ushort_as_half((uint16_t)(h & 0xffff)));
+}
+// Two f32 -> two E2M1 nibbles (round to nearest even, saturate to +-6); lo in bits 0-3.
+__device__ __forceinline__ uint8_t e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{.reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t;}"
+      : "=r"(r) : "f"(hi), "f"(lo));
+  return (uint8_t)r;
+}
+// f32 product rounded toward zero ([EPI] _nvfp4_quant32).
+__device__ __forceinline__ float mul_rz(float a, float b) { return __fmul_rz(a, b); }
+// E8M0 code -> f32 power of two (code 0 -> 2^-127, a subnormal).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t c) {
+  return c == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(c << 23);
+}
+
+__device__ __forceinline__ void set_status(uint32_t *st, uint32_t bit) { atomicOr(st, bit); }
+
+__device__ __forceinline__ int64_t ld_i64(const int64_t *p) { return __ldg(p); }
+
+// Offset of (row r, K-block kb) in the F8_128x4 scale layout ([EPI]
+// prepare_SF): [R/128, Ksf/4, 32, 4, 4].
+__device__ __forceinline__ int64_t sf128x4_offset(int64_t r, int kb, int ksf) {
+  return ((r >> 7) * (ksf >> 2) + (kb >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (kb & 3);
+}
+
+// ------------------------------------------------ programmatic dependent launch
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{.reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p;}"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait for phase `parity` of an mbarrier, giving up after about a second:
+// the caller's results are then invalid and PA_DEV_WAIT_TIMEOUT is raised.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *status) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    if (mbar_try_wait(a, parity)) return true;
+    if (globaltimer() - t0 > 1000000000ull) {
+      set_status(status, kDevWaitTimeout);
+      return false;
+    }
+  }
+}
+
+// 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ---------------------------------------------------- legacy warp MMA (FP8)
+// D[16x8] += A[16x32] * B[32x8], e4m3 inputs, f32 accumulate.  Fragments:
+// a0: (row g, k 4t..4t+3), a1: (g+8, 4t..), a2: (g, 16+4t..), a3: (g+8, 16+4t..);
+// b0: (k 4t.., col g), b1: (k 16+4t.., col g); c0,c1: (g, 2t, 2t+1), c2,c3: (g+8, ..).
+__device__ __forceinline__ void mma_e4m3_16832(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ================================================================ epilogue
+//
+// One 128-dim head row of one token is held by G = 128 / E consecutive lanes,
+// E consecutive dims each (E = 4: a warp per row, as the pre_attn page's half
+// wave; E = 128: a thread per row, as the epilogue page's TMEM drain).
+template <int E>
+struct Row {
+  static constexpr int G = kHeadDim / E;
+  static_assert(G >= 1 && G <= 32 && (G & (G - 1)) == 0, "E must divide 128");
+  __device__ static __forceinline__ float sum(float x) {
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+  }
+  __device__ static __forceinline__ float max(float x) {
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+  }
+};
+
+// Gemma RMSNorm of a head row in place: v * rsqrt(mean(v^2) + eps) * (1 + gamma)
+// ([K1] head_norm_rope, [EPI] _rms_norm).
+template <int E>
+__device__ __forceinline__ void head_rmsnorm(float (&v)[E], int d0, const __nv_bfloat16 *gamma, float eps) {
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < E; ++i) ss = fmaf(v[i], v[i], ss);
+  ss = Row<E>::sum(ss);
+  const float rr = rsqrtf(ss * (1.0f / kHeadDim) + eps);
+  const uint2 *g = reinterpret_cast<const uint2 *>(gamma + d0);
+#pragma unroll
+  for (int q = 0; q < E / 4; ++q) {
+    uint2 gw = __ldg(g + q);
+    float gg[4] = {bf16_to_f32(gw.x & 0xffff), bf16_to_f32(gw.x >> 16), bf16_to_f32(gw.y & 0xffff),
+                   bf16_to_f32(gw.y >> 16)};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float n = v[4 * q + j] * rr;
+      v[4 * q + j] = fmaf(n, gg[j], n);
+    }
+  }
+}
+
+// Partial NeoX RoPE over dims [0, 64) ([K1] head_norm_rope, [EPI] _rope64):
+// x' = x c - y s, y' = y c + x s with x = dim i, y = dim i + 32, c / s the
+// bf16 cos_sin[pos][i], cos_sin[pos][32 + i].
+template <int E>
+__device__ __forceinline__ void head_rope(float (&v)[E], int d0, const __nv_bfloat16 *cs_row) {
+  if constexpr (E >= kRotDim) {
+    // the thread holds dims [d0, d0 + E); d0 = 0 whenever it holds [0, 64)
+    if (d0 == 0) {
+#pragma unroll
+      for (int i = 0; i < kHalfRot; i += 2) {
+        uint32_t cw = __ldg(reinterpret_cast<const uint32_t *>(cs_row + i));
+        uint32_t sw = __ldg(reinterpret_cast<const uint32_t *>(cs_row + kHalfRot + i));
+        float c[2] = {bf16_to_f32(cw & 0xffff), bf16_to_f32(cw >> 16)};
+        float s[2] = {bf16_to_f32(sw & 0xffff), bf16_to_f32(sw >> 16)};
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          float x = v[i + j], y = v[i + j + kHalfRot];
+          v[i + j] = x * c[j] - y * s[j];
+          v[i + j + kHalfRot] = y * c[j] + x * s[j];
+        }
+      }
+    }
+  } else {
+    // partner dims (i +- 32) sit 32 / E lanes away
+    constexpr int kLanes = kHalfRot / E;
+    const bool first = d0 < kHalfRot;
+    const bool in_rope = d0 < kRotDim;
+    const int ib = first ? d0 : d0 - kHalfRot;
+    float c[E], s[E];
+    if (in_rope) {
+#pragma unroll
+      for (int j = 0; j < E; ++j) {
+        c[j] = __bfloat162float(cs_row[ib + j]);
+        s[j] = __bfloat162float(cs_row[kHalfRot + ib + j]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+      float p = __shfl_xor_sync(0xffffffffu, v[j], kLanes);
+      if (in_rope) v[j] = first ? (v[j] * c[j] - p * s[j]) : (v[j] * c[j] + p * s[j]);
+    }
+  }
+}
+
+// [K1] page16_of: page-16 id of a slot under the K / V block page stride.
+__device__ __forceinline__ int64_t page16_of(int64_t slot, int kps) {
+  if (kps == 8) return slot >> 4;
+  return (slot >> 7) * kps + ((slot & 127) >> 4);
+}
+
+// NVFP4 group quantiser ([EPI] _nvfp4_quant32) for 4 values of a 16-dim
+// group whose max magnitude is gmax: returns the scale byte, fills two
+// packed bytes (even dim in the low nibble, zero magnitudes unsigned).
+__device__ __forceinline__ uint8_t nvfp4_scale(float gmax, bool has_gs, float gs_inv, float &r) {
+  float a = gmax * (1.0f / 6.0f);
+  if (has_gs) a = a * gs_inv;
+  a = fmaxf(a, 0x1p-9f);
+  const uint8_t sf = e4m3(a);
+  r = __frcp_rn(e4m3_to_f32(sf));
+  if (has_gs) r = r * gs_inv;
+  return sf;
+}
+__device__ __forceinline__ uint16_t nvfp4_quad(const float *v4, float r) {
+  uint32_t b0 = e2m1x2(mul_rz(v4[0], r), mul_rz(v4[1], r));
+  uint32_t b1 = e2m1x2(mul_rz(v4[2], r), mul_rz(v4[3], r));
+  uint32_t w = b0 | (b1 << 8);
+  const uint32_t m = 0x7777u;
+  w = w & (((w & m) + m) | m);  // clear the sign of zero magnitudes
+  return (uint16_t)w;
+}
+
+// Everything the epilogue of one (token, head) needs besides the values.
+struct HeadCtx {
+  int m;        // token row
+  int head;     // head index in [0, n_heads)
+  int64_t pos;  // clamped position
+  int64_t slot, islot;
+};
+
+__device__ __forceinline__ int64_t load_pos(const Params &p, int m) {
+  int64_t pos = ld_i64(p.pos + m);
+  if (pos < 0 || pos >= p.max_pos) {
+    set_status(p.status, kDevPosRange);
+    pos = pos < 0 ? 0 : p.max_pos - 1;
+  }
+  return pos;
+}
+
+// Run the role logic of one head row.  v: this thread's E values (dims
+// d0 .. d0 + E - 1) of the f32 projection.  Heads are
+// [q x n_q | k x n_kv | v x n_kv | index_q x n_iq | index_k]
+// ([EPI] QkvIndexFusedEpilogueKernel.__init__); per role ([K1] head tasks,
+// [EPI] kernel epilogue):
+//   q       norm + rope -> bf16 and / or e4m3(z * (1/q_fp8_scale))
+//   k       norm + rope -> FP8: e4m3(bf16(z) / ks), ks = amax / 448;
+//                          NVFP4 with 1/k_global, linear scale bytes
+//   v       raw         -> FP8: e4m3(y / vs);  NVFP4 with 1/v_global, V-swizzled scales
+//   index_q norm + rope -> bf16 and / or e4m3(z)
+//   index_k norm + rope -> FP8: e4m3(bf16(z)) in the index cache; NVFP4 unit scale
+// A slot < 0 skips that cache; a slot beyond the cache skips it and flags.
+template <int E>
+__device__ __forceinline__ void head_epilogue(const Params &p, const HeadCtx &hc, float (&v)[E], int d0) {
+  const int h = hc.head;
+  const bool is_q = h < p.k0, is_k = h >= p.k0 && h < p.v0, is_v = h >= p.v0 && h < p.iq0;
+  const bool is_iq = h >= p.iq0 && h < p.ik0;
+  if (!is_v) {
+    const __nv_bfloat16 *g = is_q ? p.g_q : is_k ? p.g_k : is_iq ? p.g_iq : p.g_ik;
+    head_rmsnorm<E>(v, d0, g, p.eps);
+    head_rope<E>(v, d0, p.cos_sin + hc.pos * kRotDim);
+  }
+  const int m = hc.m;
+  if (is_q || is_iq) {
+    const int nh = is_q ? p.n_q : p.n_iq;
+    const int j = is_q ? h : h - p.iq0;
+    __nv_bfloat16 *ob = is_q ? p.q : p.iq;
+    uint8_t *of = is_q ? p.q_fp8 : p.iq_fp8;
+    const float sc = is_q ? p.q_fp8_inv : 1.0f;
+    const int64_t base = (int64_t)m * nh * kHeadDim + (int64_t)j * kHeadDim + d0;
+    if (ob) {
+#pragma unroll
+      for (int q = 0; q < E / 4; ++q) {
+        uint2 w;
+        w.x = (uint32_t)f32_to_bf16_bits(v[4 * q]) | ((uint32_t)f32_to_bf16_bits(v[4 * q + 1]) << 16);
+        w.y = (uint32_t)f32_to_bf16_bits(v[4 * q + 2]) | ((uint32_t)f32_to_bf16_bits(v[4 * q + 3]) << 16);
+        *reinterpret_cast<uint2 *>(ob + base + 4 * q) = w;
+      }
+    }
+    if (of) {
+#pragma unroll
+      for (int q = 0; q < E / 4; ++q) {
+        uint32_t w = is_q ? e4m3x4(v[4 * q] * sc, v[4 * q + 1] * sc, v[4 * q + 2] * sc, v[4 * q + 3] * sc)
+                          : e4m3x4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        *reinterpret_cast<uint32_t *>(of + base + 4 * q) = w;
+      }
+    }
+    return;
+  }
+  const bool is_ik = !is_k && !is_v;
+  const int64_t slot = is_ik ? hc.islot : hc.slot;
+  if (slot < 0) return;
+  if (p.cache_fmt == 0) {
+    // ---------------------------------------------------------- FP8 caches
+    if (is_ik) {
+      if (slot >= p.num_index_slots) {
+        if (d0 == 0) set_status(p.status, kDevSlotRange);
+        return;
+      }
+      uint8_t *dst = p.index_cache + slot * kHeadDim + d0;
+#pragma unroll
+      for (int q = 0; q < E / 4; ++q)
+        *reinterpret_cast<uint32_t *>(dst + 4 * q) = e4m3x4(bf16_round(v[4 * q]), bf16_round(v[4 * q + 1]),
+                                                            bf16_round(v[4 * q + 2]), bf16_round(v[4 * q + 3]));
+      return;
+    }
+    const int kvh = is_k ? h - p.k0 : h - p.v0;
+    const int64_t p16 = page16_of(slot, p.kps);
+    if (p16 >= p.num_pages16) {
+      if (d0 == 0) set_status(p.status, kDevSlotRange);
+      return;
+    }
+    const int t = (int)(slot & 15);
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < E; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    amax = Row<E>::max(amax);
+    const float s = p.static_kv ? 1.0f : (amax == 0.f ? 1.0f : __fdiv_rn(amax, kFp8Max));
+    const int64_t page = (p16 * p.n_kv + kvh) * 2048;
+    if (is_k) {
+#pragma unroll
+      for (int q = 0; q < E / 4; ++q) {
+        const int d = d0 + 4 * q;
+        uint32_t w = e4m3x4(__fdiv_rn(bf16_round(v[4 * q]), s), __fdiv_rn(bf16_round(v[4 * q + 1]), s),
+                            __fdiv_rn(bf16_round(v[4 * q + 2]), s), __fdiv_rn(bf16_round(v[4 * q + 3]), s));
+        *reinterpret_cast<uint32_t *>(p.k_cache + page + (d >> 4) * 256 + t * 16 + (d & 15)) = w;
+      }
+      if (d0 == 0) p.k_scale[(p16 * p.n_kv + kvh) * 16 + t] = s;
+    } else {
+#pragma unroll
+      for (int i = 0; i < E; ++i) p.v_cache[page + (d0 + i) * 16 + t] = e4m3(__fdiv_rn(v[i], s));
+      if (d0 == 0) p.v_scale[(p16 * p.n_kv + kvh) * 16 + t] = s;
+    }
+    return;
+  }
+  // ------------------------------------------------------------ NVFP4 caches
+  const int bs = p.bs;
+  const int64_t page = slot / bs;
+  const int t = (int)(slot - page * bs);
+  uint8_t *base;
+  int sl;
+  bool has_gs = true;
+  float gs_inv;
+  if (is_ik) {
+    if (page >= p.idx_pages) {
+      if (d0 == 0) set_status(p.status, kDevSlotRange);
+      return;
+    }
+    base = p.idx_cache + page * p.idx_page_bytes;
+    sl = 0;
+    has_gs = false;
+    gs_inv = 1.0f;
+  } else {
+    if (page >= p.kv_pages) {
+      if (d0 == 0) set_status(p.status, kDevSlotRange);
+      return;
+    }
+    base = p.kv_cache + page * p.kv_page_bytes;
+    sl = is_k ? 2 * (h - p.k0) : 2 * (h - p.v0) + 1;
+    gs_inv = is_k ? p.k_gs_inv : p.v_gs_inv;
+  }
+  uint8_t *slot_base = base + (int64_t)sl * bs * 72;
+  // groups of 16 dims = 4 quads; a group spans 16 / E lanes when E < 16
+#pragma unroll
+  for (int q0 = 0; q0 < (E >= 16 ? E / 4 : 1); q0 += (E >= 16 ? 4 : 1)) {
+    float gmax = 0.f;
+    constexpr int QPG = E >= 16 ? 4 : E / 4;  // quads of this group in this thread
+#pragma unroll
+    for (int q = 0; q < QPG; ++q)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) gmax = fmaxf(gmax, fabsf(v[4 * (q0 + q) + j]));
+    if constexpr (E < 16) {
+#pragma unroll
+      for (int o = 1; o < 16 / E; o <<= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
+    }
+    float r;
+    const uint8_t sf = nvfp4_scale(gmax, has_gs, gs_inv, r);
+#pragma unroll
+    for (int q = 0; q < QPG; ++q) {
+      const int d = d0 + 4 * (q0 + q);
+      const uint16_t w = nvfp4_quad(&v[4 * (q0 + q)], r);
+      *reinterpret_cast<uint16_t *>(slot_base + t * 64 + (d >> 6) * 32 + ((d & 63) >> 1)) = w;
+    }
+    const int dg = d0 + 4 * q0;  // first dim of the group part held here
+    if ((dg & 15) == 0) {
+      const int g = dg >> 4;
+      const int off = is_v ? ((t >> 2) * 4 + (g >> 1)) * 8 + (g & 1) * 4 + (t & 3) : t * 8 + g;
+      slot_base[bs * 64 + off] = sf;
+    }
+  }
+}
+
+}  // namespace pa

@@ -1,0 +1,22 @@
+// Host-side launchers of the pre-attention kernels (one per translation unit).
+#pragma once
+
+#include <cuda_runtime.h>
+
+namespace pa {
+
+struct Params;
+
+// Prologue over `grid` CTAs (M rows, plus padding rows of the MXFP8 scale grid).
+cudaError_t launch_prologue(const Params &p, int grid, bool pdl, cudaStream_t stream);
+// Row-major [rows, ksf] E8M0 -> F8_128x4 layout.
+cudaError_t launch_pack_scales(const uint8_t *src, uint8_t *dst, int rows, int ksf, cudaStream_t stream);
+
+// Skinny-M path (M <= 16): weight-streaming FP8 GEMV with the per-head
+// epilogue run by the last CTA to finish each head.
+cudaError_t launch_gemv(const Params &p, int num_sms, bool pdl, cudaStream_t stream);
+
+// Tensor-core path: persistent tcgen05 GEMM with the fused head epilogue.
+cudaError_t launch_gemm(const Params &p, int num_sms, int grid_override, bool pdl, cudaStream_t stream);
+
+}  // namespace pa

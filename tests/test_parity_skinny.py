@@ -1,0 +1,111 @@
+"""GPU parity of the skinny-M path (M <= 16: prologue + weight-streaming GEMV
++ last-arriver head epilogue) against the CPU oracle, through the C-ABI."""
+
+import numpy as np
+import pytest
+
+import workloads
+from tests import harness
+
+pytestmark = pytest.mark.gpu
+
+
+def _gemv_flags():
+    from indexer_projection_gb300 import binding as B
+    return B.PA_FLAG_FORCE_GEMV
+
+
+def check(wl, flags=None, rows=None, runs=1):
+    st = workloads.host_state(wl)
+    g = harness.GpuRun(wl, st, flags=_gemv_flags() if flags is None else flags)
+    for _ in range(runs):
+        g.run()
+    got = g.results()
+    rows = list(range(wl.M)) if rows is None else rows
+    ref = harness.oracle_run(wl, st, rows)
+    harness.compare(wl, got, ref, rows, all_rows=range(wl.M))
+    assert g.runner.device_status() == 0
+    return g
+
+
+def test_tiny():
+    check(workloads.tiny())
+
+
+def test_decode():
+    check(workloads.decode())
+
+
+def test_decode_every_output_and_nvfp4_mx():
+    check(workloads.decode().replace(q_fp8=True, iq_fp8=True, q_fp8_scale=0.37))
+    check(workloads.decode().replace(weight_fmt="mx", cache_fmt="nvfp4", pool_pages=4096, q_fp8=True,
+                                     iq_fp8=True, k_global=0.5, v_global=3.0))
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 8, 9, 13, 16])
+def test_token_counts(M):
+    check(workloads.tiny().replace(M=M, q_fp8=True, iq_fp8=True))
+
+
+@pytest.mark.parametrize("nkv", [2, 4])
+@pytest.mark.parametrize("fmt", ["ptpc", "mx"])
+def test_kv_heads_and_formats(nkv, fmt):
+    check(workloads.tiny().replace(nkv=nkv, n_q=0, n_iq=0, weight_fmt=fmt, M=7, iq_fp8=True))
+
+
+def test_skipped_slots_static_scale_separate_index_slots():
+    check(workloads.tiny().replace(M=8, skip_rows=(0, 5), static_kv_scale=True, separate_index_slots=True))
+
+
+def test_nvfp4_block_sizes_and_page_padding():
+    for bs, pad in ((16, 0), (4, 32), (32, 96)):
+        check(workloads.Workload(f"nv_bs{bs}", H=512, nkv=2, M=9, weight_fmt="ptpc", cache_fmt="nvfp4",
+                                 seed=11 + bs, positions="uniform", max_pos=300, pool_pages=40, block_size=bs,
+                                 page_pad=pad, q_fp8=True, iq_fp8=True, skip_rows=(3,)))
+
+
+def test_outlier_rows_and_custom_heads():
+    check(workloads.Workload("odd", H=1024, nkv=2, n_q=8, n_iq=3, M=12, weight_fmt="mx", cache_fmt="fp8",
+                             seed=5, positions="uniform", max_pos=1000, pool_pages16=128, outlier_frac=0.2,
+                             q_fp8=True, iq_fp8=True))
+
+
+def test_kv_page_stride_16():
+    wl = workloads.tiny().replace(M=6, kv_page_stride=16, pool_pages16=128)
+    st = workloads.host_state(wl)
+    st["slot_mapping"] = st["slot_mapping"] % (64 * 16)  # page16 ids stay below 128
+    g = harness.GpuRun(wl, st, flags=_gemv_flags())
+    g.run()
+    ref = harness.oracle_run(wl, st, range(wl.M))
+    harness.compare(wl, g.results(), ref, range(wl.M))
+
+
+def test_repeated_calls_reuse_the_workspace():
+    # the per-head arrival counters must be back at zero after every call
+    check(workloads.decode(), runs=3)
+
+
+def test_out_of_range_slots_and_positions_are_flagged_not_written():
+    from indexer_projection_gb300 import binding as B
+    wl = workloads.tiny().replace(M=4)
+    st = workloads.host_state(wl)
+    st["slot_mapping"][1] = wl.num_pages16 * 16 + 5      # beyond the cache
+    st["index_slot_mapping"][1] = wl.num_index_slots + 9
+    g = harness.GpuRun(wl, st, flags=_gemv_flags())
+    g.run()
+    got = g.results()
+    assert g.runner.device_status() == B.PA_DEV_SLOT_RANGE
+    ok_rows = [0, 2, 3]
+    ref = harness.oracle_run(wl, st, ok_rows)
+    harness.compare(wl, got, ref, ok_rows, all_rows=ok_rows)
+    st2 = workloads.host_state(wl)
+    st2["positions"][2] = wl.max_pos + 100
+    g2 = harness.GpuRun(wl, st2, flags=_gemv_flags())
+    g2.run()
+    g2.results()
+    assert g2.runner.device_status() == B.PA_DEV_POS_RANGE
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16])
+def test_sweep_config_skinny_points(M):
+    check(workloads.sweep(M), flags=0)
