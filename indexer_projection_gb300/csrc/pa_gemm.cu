@@ -346,7 +346,7 @@ cudaError_t launch_gemm(const Params &p, int num_sms, int grid_override, bool pd
   int grid = grid_override > 0 ? grid_override : num_sms;
   if (grid > tiles) grid = tiles;
   auto kern = p.weight_fmt == 0 ? gemm_kernel<0> : gemm_kernel<1>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), kGemmSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];

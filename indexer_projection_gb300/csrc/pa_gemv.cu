@@ -249,7 +249,7 @@ static GemvPlan plan_gemv(const Params &p, int num_sms) {
 template <int WFMT, int NT>
 static cudaError_t launch_gemv_t(const Params &p, const GemvPlan &g, bool pdl, cudaStream_t stream) {
   auto kern = gemv_kernel<WFMT, NT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem);
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), g.smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];

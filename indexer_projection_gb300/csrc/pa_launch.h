@@ -7,6 +7,27 @@ namespace pa {
 
 struct Params;
 
+// Raise a kernel's dynamic shared-memory limit once per (kernel, device),
+// kept out of the per-call path so the launch sequence also works inside
+// stream capture.  Keyed on the kernel's address: template instances share
+// one C++ type.
+inline cudaError_t ensure_smem_attr(const void *kern, int bytes) {
+  struct Entry {
+    const void *k;
+    int dev, bytes;
+  };
+  static Entry table[64];
+  static int n = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  for (int i = 0; i < n; ++i)
+    if (table[i].k == kern && table[i].dev == dev && table[i].bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && n < 64) table[n++] = Entry{kern, dev, bytes};
+  return e;
+}
+
 // Prologue over `grid` CTAs (M rows, plus padding rows of the MXFP8 scale grid).
 cudaError_t launch_prologue(const Params &p, int grid, bool pdl, cudaStream_t stream);
 // Row-major [rows, ksf] E8M0 -> F8_128x4 layout.

@@ -231,8 +231,11 @@ cudaError_t launch_prologue(const Params &p, int grid, bool pdl, cudaStream_t st
 cudaError_t launch_pack_scales(const uint8_t *src, uint8_t *dst, int rows, int ksf, cudaStream_t stream) {
   const int64_t total = ((int64_t)rows + 127) / 128 * 128 * ksf;
   const int grid = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
-  pack_scales_kernel<<<grid, 256, 0, stream>>>(src, dst, rows, ksf);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, pack_scales_kernel, src, dst, rows, ksf);
 }
 
 }  // namespace pa
