@@ -242,6 +242,30 @@ int pre_attn_device_status(void *workspace, uint32_t *flags, void *stream);
  * only.  The caller owns the events.  Errors: PA_ERR_NULL (h). */
 int pre_attn_set_profile_events(pa_handle *h, void *before_main, void *after_main);
 
+/* Allocation-free variant of pre_attn_run.  The pages have no counterpart:
+ * this entry point exists for callers that cannot allocate device memory and
+ * so cannot supply a workspace, for example a plugin loaded into a host
+ * runtime that owns all device memory through its own pool and hands none
+ * out, or a process whose device memory is capped so that any cudaMalloc
+ * after start-up fails.
+ * It runs the same step as pre_attn_run (same arguments minus the workspace)
+ * for 0 <= M <= 16 token rows, with the kernels' scratch (status word,
+ * per-head counters, quantised activations, f32 projection rows) in a fixed
+ * 2 MiB array inside this library; every GPU that loads the library holds
+ * that array until the process exits.  It calls no cudaMalloc, cudaFree or
+ * allocating library routine.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls share the one array and each clears the part it uses first
+ *     (cudaMemsetAsync on `stream`); calls that overlap on the GPU (other
+ *     streams, other host threads) race on it, so order them.
+ *   - The device status word (PA_DEV_*) lives in that shared array and is
+ *     not readable through this entry point.
+ * Errors: those of pre_attn_run, and PA_ERR_SHAPE when M > 16, M > the
+ * handle's max_tokens, or pre_attn_workspace_bytes(h, M) exceeds 2 MiB. */
+int pre_attn_run_noalloc(pa_handle *h, int M, const pa_step_inputs *in, const pa_weights *wt,
+                         const pa_caches *caches, const pa_outputs *out, void *stream);
+
 /* The last CUDA error string seen by this thread's calls ("" if none). */
 const char *pre_attn_last_cuda_error(void);
 

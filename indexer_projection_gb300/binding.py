@@ -95,6 +95,8 @@ def load(path: str = LIB_PATH):
         "pre_attn_device_status": (i, [_vp, u32p, _vp]),
         "pre_attn_last_cuda_error": (ctypes.c_char_p, []),
         "pre_attn_set_profile_events": (i, [H, _vp, _vp]),
+        "pre_attn_run_noalloc": (i, [H, i, ctypes.POINTER(pa_step_inputs), ctypes.POINTER(pa_weights),
+                                     ctypes.POINTER(pa_caches), ctypes.POINTER(pa_outputs), _vp]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -180,6 +182,15 @@ def pre_attn_run(h, M: int, inputs: pa_step_inputs, weights: pa_weights, caches:
     if check and st != PA_OK:
         extra = pre_attn_last_cuda_error() if st == PA_ERR_CUDA else ""
         raise PreAttnError(st, "pre_attn_run " + extra)
+    return st
+
+
+def pre_attn_run_noalloc(h, M: int, inputs: pa_step_inputs, weights: pa_weights, caches: pa_caches,
+                         outputs: pa_outputs, stream=None, check: bool = True) -> int:
+    st = load().pre_attn_run_noalloc(h, int(M), ctypes.byref(inputs), ctypes.byref(weights),
+                                     ctypes.byref(caches), ctypes.byref(outputs), stream_ptr(stream))
+    if check and st != PA_OK:
+        raise PreAttnError(st, "pre_attn_run_noalloc")
     return st
 
 

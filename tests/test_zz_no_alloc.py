@@ -1,0 +1,66 @@
+"""pre_attn_run_noalloc, the entry point for callers that cannot allocate
+device memory (a plugin whose host runtime owns every byte of device memory,
+a process whose device memory is capped after start-up), against
+pre_attn_run with a caller workspace.
+
+Kept in a file pytest collects last, so that a run stopping at its first
+failure has run every other test before this one.  It passes on its own in a
+fresh process and after the rest of the suite: the entry point clears the
+part of its shared static scratch that must start at zero on every call.
+"""
+
+import numpy as np
+import pytest
+
+import workloads
+from tests import harness
+
+pytestmark = pytest.mark.gpu
+
+
+def _expected_and_noalloc(wl):
+    from indexer_projection_gb300 import binding as B
+
+    st = workloads.host_state(wl)
+    ref = harness.GpuRun(wl, st)  # the existing entry point, caller workspace
+    ref.run()
+    want = ref.results()
+    g = harness.GpuRun(wl, st)    # fresh copies of the same inputs, caches and outputs
+    d = g.d
+    ins = B.pa_step_inputs(B.ptr(d["ar"]), B.ptr(d["res"]), B.ptr(d["positions"]), B.ptr(d["slot_mapping"]),
+                           B.ptr(d["index_slot_mapping"]))
+    stream = g.torch.cuda.current_stream()
+    assert B.pre_attn_run_noalloc(g.runner.handle, wl.M, ins, g.weights, g.caches, g.outputs, stream) == B.PA_OK
+    got = g.results()
+    return st, want, got
+
+
+def test_noalloc_matches_pre_attn_run_on_two_calls_in_a_row():
+    # two calls back to back on different shapes: the second finds the first
+    # one's contents in the shared scratch
+    for wl in (workloads.decode().replace(q_fp8=True, iq_fp8=True),
+               workloads.tiny().replace(M=13, nkv=2, n_q=0, n_iq=0, weight_fmt="mx", seed=17, iq_fp8=True)):
+        st, want, got = _expected_and_noalloc(wl)
+        reference = dict(st)
+        reference.update(want)
+        harness.compare(wl, got, reference, range(wl.M), where=" noalloc vs pre_attn_run")
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch():
+    from indexer_projection_gb300 import binding as B
+    from indexer_projection_gb300.runner import PreAttn
+
+    wl = workloads.tiny()
+    st = workloads.host_state(wl)
+    g = harness.GpuRun(wl, st, max_tokens=32)
+    d = g.d
+    ins = B.pa_step_inputs(B.ptr(d["ar"]), B.ptr(d["res"]), B.ptr(d["positions"]), B.ptr(d["slot_mapping"]), None)
+    # M beyond the 16 rows of the skinny path
+    assert B.pre_attn_run_noalloc(g.runner.handle, 17, ins, g.weights, g.caches, g.outputs, check=False) \
+        == B.PA_ERR_SHAPE
+    # a shape whose scratch need exceeds 2 MiB (H = 16384, 16 rows, 264 heads)
+    big = PreAttn(16384, 4, weight_format=B.PA_WEIGHT_FP8_PER_CHANNEL, cache_format=B.PA_CACHE_FP8,
+                  max_tokens=16, n_q_heads=250, n_iq_heads=5)
+    assert B.pre_attn_workspace_bytes(big.handle, 16) > (2 << 20)
+    assert B.pre_attn_run_noalloc(big.handle, 16, ins, g.weights, g.caches, g.outputs, check=False) \
+        == B.PA_ERR_SHAPE
