@@ -104,7 +104,9 @@ enum pa_flags {
   PA_FLAG_STATIC_KV_SCALE = 1 << 0, /* FP8 caches: K / V scales fixed at 1 */
   PA_FLAG_FORCE_GEMV = 1 << 1,      /* testing: the skinny path for any M <= 16 */
   PA_FLAG_FORCE_GEMM = 1 << 2,      /* testing: the tensor-core GEMM path for any M */
-  PA_FLAG_NO_PDL = 1 << 3           /* launch without programmatic dependent launch */
+  PA_FLAG_NO_PDL = 1 << 3,          /* launch without programmatic dependent launch */
+  PA_FLAG_GEMM_SINGLE = 1 << 4,     /* testing: tensor-core path on single CTAs (128 x 128 tiles) */
+  PA_FLAG_GEMM_PAIR = 1 << 5        /* testing: tensor-core path on CTA pairs (256 x 256 tiles) */
 };
 
 /* ----------------------------------------------------------- config */

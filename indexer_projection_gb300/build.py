@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libpre_attn.so")
-SOURCES = ["pa_api.cu", "pa_prologue.cu", "pa_gemv.cu", "pa_gemm.cu", "pa_noalloc.cu"]
+SOURCES = ["pa_api.cu", "pa_prologue.cu", "pa_gemv.cu", "pa_gemm.cu", "pa_gemm2.cu", "pa_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
               "-Xptxas", "-v", "--expt-relaxed-constexpr"]

@@ -32,8 +32,10 @@ int cuda_fail(cudaError_t e) {
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Workspace layout for M rows.  The status word and the per-head counters
-// sit at fixed offsets (they carry state between calls); the rest is scratch.
+// Workspace layout for M rows.  The first 256 bytes hold the status word
+// (offset 0), the fused skinny path's finished-CTA counter (8) and its 16
+// row flags (128); the per-head counters follow at 256.  These carry state
+// between calls (each call leaves them zero); the rest is scratch.
 struct WsLayout {
   size_t status, cnt, x_scale, xsf, xq, y, total;
   int m_pad;
@@ -105,6 +107,7 @@ int pre_attn_init(const pa_config *cfg, pa_handle **out) {
   }
   if (!(c.eps >= 0.0f) || c.max_tokens < 0 || c.gemm_grid < 0) return PA_ERR_CONFIG;
   if ((c.flags & PA_FLAG_FORCE_GEMV) && (c.flags & PA_FLAG_FORCE_GEMM)) return PA_ERR_CONFIG;
+  if ((c.flags & PA_FLAG_GEMM_SINGLE) && (c.flags & PA_FLAG_GEMM_PAIR)) return PA_ERR_CONFIG;
   pa_handle *h = new (std::nothrow) pa_handle;
   if (!h) return PA_ERR_CONFIG;
   h->cfg = c;
@@ -297,15 +300,35 @@ int pre_attn_run(pa_handle *h, int M, const pa_step_inputs *in, const pa_weights
   p.xsf = ws + L.xsf;
   p.xq = ws + L.xq;
   p.y = reinterpret_cast<float *>(ws + L.y);
+  p.done_cnt = reinterpret_cast<int *>(ws + L.status + 8);
+  p.row_flag = reinterpret_cast<int *>(ws + L.status + 128);
   p.m_pad = L.m_pad;
 
   const bool pdl = !(c.flags & PA_FLAG_NO_PDL);
   cudaStream_t s = (cudaStream_t)stream;
-  const int pro_grid = (!gemv && c.weight_format == PA_WEIGHT_MXFP8) ? L.m_pad : M;
-  e = pa::launch_prologue(p, pro_grid, pdl, s);
-  if (e != cudaSuccess) return cuda_fail(e);
+  // the skinny path normalises the rows inside its own launch when it can
+  const bool fused = gemv && pa::gemv_fuses_prologue(p);
+  if (!fused) {
+    const int pro_grid = (!gemv && c.weight_format == PA_WEIGHT_MXFP8) ? L.m_pad : M;
+    e = pa::launch_prologue(p, pro_grid, pdl, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
   if (h->prof_before && (e = cudaEventRecord(h->prof_before, s)) != cudaSuccess) return cuda_fail(e);
-  e = gemv ? pa::launch_gemv(p, h->num_sms, pdl, s) : pa::launch_gemm(p, h->num_sms, c.gemm_grid, pdl, s);
+  if (gemv) {
+    e = pa::launch_gemv(p, h->num_sms, pdl, fused, s);
+  } else {
+    // 256 x 256 pair tiles cost about 1.5x a 128 x 128 tile on one SM: use the
+    // pairs unless wave quantisation favours the finer tiles
+    const int64_t t1 = (int64_t)((M + 127) / 128) * (h->N / 128);
+    const int64_t t2 = (int64_t)((M + 255) / 256) * ((h->N + 255) / 256);
+    const int64_t w1 = (t1 + h->num_sms - 1) / h->num_sms;
+    const int64_t w2 = (t2 + h->num_sms / 2 - 1) / (h->num_sms / 2);
+    bool pair = 3 * w2 <= 2 * w1;
+    if (c.flags & PA_FLAG_GEMM_SINGLE) pair = false;
+    if (c.flags & PA_FLAG_GEMM_PAIR) pair = true;
+    e = pair ? pa::launch_gemm_pair(p, h->num_sms, c.gemm_grid, pdl, s)
+             : pa::launch_gemm(p, h->num_sms, c.gemm_grid, pdl, s);
+  }
   if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return cuda_fail(e);
   if (h->prof_after && (e = cudaEventRecord(h->prof_after, s)) != cudaSuccess) return cuda_fail(e);

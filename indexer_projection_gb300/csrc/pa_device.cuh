@@ -60,6 +60,8 @@ struct Params {
   float *x_scale;            // [M] per-token scales (per-channel format)
   uint8_t *xsf;              // MXFP8 activation scales, F8_128x4 of [Mpad, H/32]
   float *y;                  // [M, N] f32 projection rows (skinny path only)
+  int *row_flag;             // [16] fused skinny path: row m's activations are published
+  int *done_cnt;             // fused skinny path: CTAs finished (the last one resets the flags)
   int m_pad;                 // M rounded up to 128 (MXFP8 scale rows)
 };
 
@@ -101,8 +103,19 @@ __device__ __forceinline__ float e8m0_to_f32(uint32_t c) {
 }
 
 __device__ __forceinline__ void set_status(uint32_t *st, uint32_t bit) { atomicOr(st, bit); }
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
 
 __device__ __forceinline__ int64_t ld_i64(const int64_t *p) { return __ldg(p); }
+__device__ __forceinline__ int ld_acquire(const int *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(int *p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
 // Offset of (row r, K-block kb) in the F8_128x4 scale layout ([EPI]
 // prepare_SF): [R/128, Ksf/4, 32, 4, 4].
@@ -214,7 +227,7 @@ __device__ __forceinline__ void head_rmsnorm(float (&v)[E], int d0, const __nv_b
   const uint2 *g = reinterpret_cast<const uint2 *>(gamma + d0);
 #pragma unroll
   for (int q = 0; q < E / 4; ++q) {
-    uint2 gw = __ldg(g + q);
+    const uint2 gw = g[q];
     float gg[4] = {bf16_to_f32(gw.x & 0xffff), bf16_to_f32(gw.x >> 16), bf16_to_f32(gw.y & 0xffff),
                    bf16_to_f32(gw.y >> 16)};
 #pragma unroll
@@ -235,8 +248,8 @@ __device__ __forceinline__ void head_rope(float (&v)[E], int d0, const __nv_bflo
     if (d0 == 0) {
 #pragma unroll
       for (int i = 0; i < kHalfRot; i += 2) {
-        uint32_t cw = __ldg(reinterpret_cast<const uint32_t *>(cs_row + i));
-        uint32_t sw = __ldg(reinterpret_cast<const uint32_t *>(cs_row + kHalfRot + i));
+        const uint32_t cw = *reinterpret_cast<const uint32_t *>(cs_row + i);
+        const uint32_t sw = *reinterpret_cast<const uint32_t *>(cs_row + kHalfRot + i);
         float c[2] = {bf16_to_f32(cw & 0xffff), bf16_to_f32(cw >> 16)};
         float s[2] = {bf16_to_f32(sw & 0xffff), bf16_to_f32(sw >> 16)};
 #pragma unroll
@@ -297,11 +310,13 @@ __device__ __forceinline__ uint16_t nvfp4_quad(const float *v4, float r) {
 }
 
 // Everything the epilogue of one (token, head) needs besides the values.
+// The gamma and cos/sin pointers may point to global or shared memory.
 struct HeadCtx {
   int m;        // token row
   int head;     // head index in [0, n_heads)
-  int64_t pos;  // clamped position
   int64_t slot, islot;
+  const __nv_bfloat16 *cs_row;            // cos_sin row of the token's (clamped) position
+  const __nv_bfloat16 *g_q, *g_k, *g_iq, *g_ik;
 };
 
 __device__ __forceinline__ int64_t load_pos(const Params &p, int m) {
@@ -331,9 +346,9 @@ __device__ __forceinline__ void head_epilogue(const Params &p, const HeadCtx &hc
   const bool is_q = h < p.k0, is_k = h >= p.k0 && h < p.v0, is_v = h >= p.v0 && h < p.iq0;
   const bool is_iq = h >= p.iq0 && h < p.ik0;
   if (!is_v) {
-    const __nv_bfloat16 *g = is_q ? p.g_q : is_k ? p.g_k : is_iq ? p.g_iq : p.g_ik;
+    const __nv_bfloat16 *g = is_q ? hc.g_q : is_k ? hc.g_k : is_iq ? hc.g_iq : hc.g_ik;
     head_rmsnorm<E>(v, d0, g, p.eps);
-    head_rope<E>(v, d0, p.cos_sin + hc.pos * kRotDim);
+    head_rope<E>(v, d0, hc.cs_row);
   }
   const int m = hc.m;
   if (is_q || is_iq) {

@@ -293,9 +293,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       HeadCtx hc;
       hc.m = m;
       hc.head = nt;
-      hc.pos = load_pos(p, m);
+      hc.cs_row = p.cos_sin + load_pos(p, m) * kRotDim;
       hc.slot = ld_i64(p.slot + m);
       hc.islot = ld_i64(p.islot + m);
+      hc.g_q = p.g_q;
+      hc.g_k = p.g_k;
+      hc.g_iq = p.g_iq;
+      hc.g_ik = p.g_ik;
       head_epilogue<kBN>(p, hc, v, 0);
     }
   }

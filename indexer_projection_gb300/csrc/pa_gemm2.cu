@@ -1,0 +1,412 @@
+// Tensor-core path on CTA pairs (cta_group::2): a persistent tcgen05 GEMM
+// whose 2-CTA cluster computes a 256 x 256 output tile per step of K, with
+// the per-head epilogue fused behind the TMEM accumulator.
+//
+//   pair      CTA r of the cluster owns token rows (2*mp + r)*128 .. +128 and
+//             loads the B rows n*256 + r*128 .. +128 (half of the tile's N);
+//             one m256 n256 k32 MMA, issued by CTA 0, reads both CTAs' A and
+//             B ("vllm.models.minimax_m3.nvidia.ops.qkv_index_fused_epilogue",
+//             QkvIndexFusedEpilogueKernel, cta_group=2).  Per FLOP each SM
+//             reads half the shared-memory operand bytes of a 128 x 128 tile,
+//             and the ring covers twice the load latency.
+//   TMEM      each CTA: a 256-column accumulator (its 128 rows x the two
+//             heads of the tile) and 12 scale-factor columns; the epilogue
+//             drains it into registers and releases it at once, so the next
+//             tile's MMAs overlap the epilogue's arithmetic and stores.
+//   warps     0-7 epilogue (warpgroup g takes head 2n + g, a thread a row),
+//             8 TMA producer, 9 TMEM allocator + MMA issuer (CTA 0 issues).
+//   loads     A, B: 128 x 128-byte TMA tiles, 128B swizzle; MXFP8 scales:
+//             the F8_128x4 atoms (512 B) by TMA, SFA for the CTA's own rows,
+//             SFB for both halves of N (each CTA needs all 256 columns'
+//             scales; no multicast).  Every load of both CTAs completes on
+//             CTA 0's stage barrier (TMA .cta_group::2).
+//   odd head count: the last N tile's second head is zero-filled by TMA and
+//             never stored.
+// Every mbarrier wait is bounded (about a second); a timeout raises
+// PA_DEV_WAIT_TIMEOUT and the kernel still reaches its final cluster barrier
+// and frees its TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "pa_device.cuh"
+#include "pa_launch.h"
+
+namespace pa {
+namespace g2 {
+
+constexpr int kBM = 128, kBN = 256, kBK = 128;  // per CTA: 128 rows x the pair's 256 columns
+constexpr int kStages = 6;
+constexpr int kTile = 128 * kBK;  // 16 KB: A tile, or this CTA's half of B
+constexpr int kSf = 512;          // one F8_128x4 atom
+constexpr int kThreads = 320;
+constexpr int kEpiThreads = 256;
+constexpr int kTmemCols = 512;
+constexpr int kSfaCol = 256, kSfbCol = 260;
+
+struct Smem {  // offsets from the 1024-aligned base
+  static constexpr int a = 0;
+  static constexpr int b = a + kStages * kTile;
+  static constexpr int sfa = b + kStages * kTile;
+  static constexpr int sfb = sfa + kStages * 1024;          // 1024-aligned slots
+  static constexpr int bars = sfb + kStages * 1024;          // full[S], empty[S], tfull, tempty
+  static constexpr int tmem_addr = bars + (2 * kStages + 2) * 8;
+  static constexpr int ok = tmem_addr + 8;                   // 2 x int
+  static constexpr int wscale = ok + 8;                      // [2 parity][2 heads][128] f32
+  static constexpr int total = wscale + 2 * 2 * 128 * 4;
+};
+constexpr int kSmemBytes = Smem::total + 1024;
+
+// ------------------------------------------------------------- cluster PTX
+__device__ __forceinline__ uint32_t cta_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void arrive_remote(uint32_t caddr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
+__device__ __forceinline__ void expect_tx_remote(uint32_t caddr, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(caddr), "r"(bytes)
+               : "memory");
+}
+// 2-D TMA load into this CTA's shared memory, completing on a barrier that
+// may sit in the peer CTA (cta_group::2).
+__device__ __forceinline__ void tma_2d_pair(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t cbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(cbar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+__device__ __forceinline__ uint64_t sdesc_sf(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
+}
+// M = 256 (the pair), N = 256, A and B E4M3, K-major.
+constexpr uint32_t kIdescF8 = (1u << 4) | ((uint32_t)(256 >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+constexpr uint32_t kIdescMx = ((uint32_t)(256 >> 3) << 17) | (1u << 23) | ((uint32_t)(256 >> 4) << 24);
+
+__device__ __forceinline__ void mma_f8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{.reg .pred p; setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_mx(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                       uint32_t acc) {
+  asm volatile(
+      "{.reg .pred p; setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+// arrive once on the barrier at this offset in both CTAs of the pair
+__device__ __forceinline__ void tc_commit_pair(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"((uint16_t)3)
+      : "memory");
+}
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+template <int WFMT>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB, Params p,
+                 int use_pdl) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + Smem::bars);
+  uint64_t *empty = full + kStages;
+  uint64_t *tfull = empty + kStages;
+  uint64_t *tempty = tfull + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Smem::tmem_addr);
+  volatile int *ok_s = reinterpret_cast<volatile int *>(smem + Smem::ok);
+  float *ws_s = reinterpret_cast<float *>(smem + Smem::wscale);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cta_rank();
+  const int M = p.M, K = p.H;
+  const int m_pairs = (M + 255) / 256, n_tiles = (p.N + kBN - 1) / kBN;
+  const int tiles = m_pairs * n_tiles;
+  const int cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
+  const int ksteps = K / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 2);   // one expect_tx arrival per CTA of the pair
+      mbar_init(&empty[s], 1);  // the MMA's commit
+    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, 2 * kEpiThreads);
+    fence_mbar_init();
+  }
+  if (warp == 8 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+  }
+  if (warp == 9) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the peer's barriers are initialised before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (use_pdl) {
+    pdl_trigger();
+    pdl_wait();
+  }
+  const uint32_t full0 = mapa(smem_u32(full), 0);      // stage barriers of CTA 0
+  const uint32_t tempty0 = mapa(smem_u32(tempty), 0);  // accumulator-free barrier of CTA 0
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      const uint32_t tx = 2 * kTile + (WFMT == 1 ? 3 * kSf : 0);
+      bool ok = true;
+      for (int t = cluster; t < tiles && ok; t += clusters) {
+        const int mp = t / n_tiles, nt = t - mp * n_tiles;
+        const int m_tile = 2 * mp + (int)rank;
+        for (int ks = 0; ks < ksteps; ++ks) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, p.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full0 + stage * 8;
+          expect_tx_remote(fb, tx);
+          tma_2d_pair(smem_u32(smem + Smem::a + stage * kTile), &tmA, ks * kBK, m_tile * kBM, fb);
+          tma_2d_pair(smem_u32(smem + Smem::b + stage * kTile), &tmB, ks * kBK, nt * kBN + (int)rank * 128, fb);
+          if (WFMT == 1) {
+            tma_2d_pair(smem_u32(smem + Smem::sfa + stage * 1024), &tmSFA, ks * 64, m_tile, fb);
+            tma_2d_pair(smem_u32(smem + Smem::sfb + stage * 1024), &tmSFB, ks * 64, 2 * nt, fb);
+            tma_2d_pair(smem_u32(smem + Smem::sfb + stage * 1024 + kSf), &tmSFB, ks * 64, 2 * nt + 1, fb);
+          }
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // -------------------------------------------------- MMA issuer (CTA 0)
+    if (rank == 0 && lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, aphase = 0;
+      bool ok = true;
+      const uint32_t a0 = smem_u32(smem + Smem::a), b0 = smem_u32(smem + Smem::b);
+      const uint32_t sfa0 = smem_u32(smem + Smem::sfa), sfb0 = smem_u32(smem + Smem::sfb);
+      for (int t = cluster; t < tiles && ok; t += clusters) {
+        if (!mbar_wait(tempty, aphase ^ 1, p.status)) break;
+        tc_fence_after();
+        for (int ks = 0; ks < ksteps; ++ks) {
+          if (!mbar_wait(&full[stage], phase, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sdesc_sw128(a0 + stage * kTile), bd = sdesc_sw128(b0 + stage * kTile);
+          if (WFMT == 1) {
+            tc_cp_sf(tmem + kSfaCol, sdesc_sf(sfa0 + stage * 1024));
+            tc_cp_sf(tmem + kSfbCol, sdesc_sf(sfb0 + stage * 1024));
+            tc_cp_sf(tmem + kSfbCol + 4, sdesc_sf(sfb0 + stage * 1024 + kSf));
+          }
+#pragma unroll
+          for (int k = 0; k < kBK / 32; ++k) {
+            const uint32_t acc = (ks | k) != 0;
+            if (WFMT == 0) {
+              mma_f8(tmem, ad + 2 * k, bd + 2 * k, kIdescF8, acc);
+            } else {
+              const uint32_t idesc = kIdescMx | ((uint32_t)k << 4) | ((uint32_t)k << 29);
+              mma_mx(tmem, ad + 2 * k, bd + 2 * k, idesc, tmem + kSfaCol, tmem + kSfbCol, acc);
+            }
+          }
+          tc_commit_pair(&empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        tc_commit_pair(tfull);
+        aphase ^= 1;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int wg = warp >> 2;              // head of the tile
+    const int row = (warp & 3) * 32 + lane;  // TMEM lane and tile row
+    const int erow = wg * 128 + row;       // 0..255 across both warpgroups
+    uint32_t aphase = 0;
+    int it = 0;
+    for (int t = cluster; t < tiles; t += clusters, ++it) {
+      const int mp = t / n_tiles, nt = t - mp * n_tiles;
+      const int head = 2 * nt + wg;
+      if (erow == 0) ok_s[it & 1] = mbar_wait(tfull, aphase, p.status) ? 1 : 0;
+      if (WFMT == 0) {
+        const int n = head * 128 + row;
+        ws_s[((it & 1) * 2 + wg) * 128 + row] = n < p.N ? __ldg(p.w_scale + n) : 0.f;
+      }
+      named_bar_sync(1, kEpiThreads);
+      if (!ok_s[it & 1]) break;
+      tc_fence_after();
+      float v[128];
+      const uint32_t base = tmem + ((uint32_t)((warp & 3) * 32) << 16) + wg * 128;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float part[32];
+        tc_ld32(base + c * 32, part);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[c * 32 + i] = part[i];
+      }
+      tc_wait_ld();
+      tc_fence_before();
+      arrive_remote(tempty0);  // the accumulator is in registers: CTA 0 may overwrite it
+      aphase ^= 1;
+      const int m = (2 * mp + (int)rank) * kBM + row;
+      if (m >= M || head >= p.n_heads) continue;
+      if (WFMT == 0) {
+        const float xs = __ldcg(p.x_scale + m);
+        const float *wsb = ws_s + ((it & 1) * 2 + wg) * 128;
+#pragma unroll
+        for (int i = 0; i < 128; ++i) v[i] = v[i] * xs * wsb[i];
+      }
+      HeadCtx hc;
+      hc.m = m;
+      hc.head = head;
+      hc.cs_row = p.cos_sin + load_pos(p, m) * kRotDim;
+      hc.slot = ld_i64(p.slot + m);
+      hc.islot = ld_i64(p.islot + m);
+      hc.g_q = p.g_q;
+      hc.g_k = p.g_k;
+      hc.g_iq = p.g_iq;
+      hc.g_ik = p.g_ik;
+      head_epilogue<128>(p, hc, v, 0);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // neither CTA leaves while the pair may still signal it
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+}  // namespace g2
+
+// ------------------------------------------------------------------- host
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode2() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// [rows, K] e4m3, K-major: 128 x 128-byte boxes, 128-byte swizzle, rows past
+// the end read as zero.
+static bool map_operand(CUtensorMap *map, const void *base, int rows, int K) {
+  auto enc = get_encode2();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K};
+  cuuint32_t box[2] = {g2::kBK, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// F8_128x4 scale atoms as a [row blocks, ksf*16] int64 grid: one box = one
+// 512-byte atom (128 rows x 4 K-blocks); row blocks past the end read as zero.
+static bool map_scales(CUtensorMap *map, const void *base, int row_blocks, int ksf) {
+  auto enc = get_encode2();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)ksf * 16, (cuuint64_t)row_blocks};
+  cuuint64_t strides[1] = {(cuuint64_t)ksf * 128};
+  cuuint32_t box[2] = {64, 1};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_INT64, 2, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_gemm_pair(const Params &p, int num_sms, int grid_override, bool pdl, cudaStream_t stream) {
+  if (p.H % g2::kBK || p.N % 128) return cudaErrorInvalidValue;
+  CUtensorMap tmA, tmB, tmSFA, tmSFB;
+  const int ksf = p.H / 32;
+  if (!map_operand(&tmA, p.xq, p.M, p.H) || !map_operand(&tmB, p.w, p.N, p.H)) return cudaErrorInvalidValue;
+  if (p.weight_fmt == 1) {
+    if (!map_scales(&tmSFA, p.xsf, p.m_pad / 128, ksf) || !map_scales(&tmSFB, p.wsf, p.N / 128, ksf))
+      return cudaErrorInvalidValue;
+  } else {
+    tmSFA = tmA;  // unused by the per-channel kernel
+    tmSFB = tmB;
+  }
+  const int tiles = ((p.M + 255) / 256) * ((p.N + 255) / 256);
+  int clusters = (grid_override > 0 ? grid_override : num_sms) / 2;
+  if (clusters > tiles) clusters = tiles;
+  if (clusters < 1) clusters = 1;
+  auto kern = p.weight_fmt == 0 ? g2::gemm2_kernel<0> : g2::gemm2_kernel<1>;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), g2::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(2 * clusters);
+  cfg.blockDim = dim3(g2::kThreads);
+  cfg.dynamicSmemBytes = g2::kSmemBytes;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmSFA, tmSFB, p, (int)pdl);
+}
+
+}  // namespace pa

@@ -1,0 +1,226 @@
+// Row normalisation of the pre-attention step, shared by the prologue kernel
+// and the fused skinny-M kernel:
+//   acc = ar + res (f32), residual = bf16(acc)
+//   n = acc * rsqrt(mean(acc^2) + eps) * (1 + g_in)            (Gemma RMSNorm)
+//   per-channel format: s = amax(n) / 448 (1 if 0), xq = e4m3(n / s), a true
+//     f32 divide ("vllm.models.minimax_m3.amd.mono.kernels.pre_attn",
+//     emit_pre_attn / norm_quant)
+//   MXFP8 format: per 32-element block an E8M0 exponent e, the smallest with
+//     448 * 2^e >= amax(block), xq = e4m3(n * 2^-e); the scale codes go to
+//     the F8_128x4 layout ("vllm.models.minimax_m3.nvidia.ops.
+//     qkv_index_fused_epilogue", prepare_SF).
+// The normalised row is rounded to f32 once, from an (almost) exact value:
+// an activation code that moved by one step would shift the whole token's
+// projection, so n (and everything quantised from it) follows the definition
+// rather than one particular rounding order.
+#pragma once
+
+#include "pa_device.cuh"
+
+namespace pa {
+
+// Error-free transformations (Knuth two-sum, FMA two-product): a + b = s + e
+// and a * b = p + e exactly.  Explicit _rn intrinsics keep the compiler from
+// contracting or reassociating them.
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+__device__ __forceinline__ void two_prod(float a, float b, float &p, float &e) {
+  p = __fmul_rn(a, b);
+  e = __fmaf_rn(a, b, -p);
+}
+// (hi, lo) double-float accumulation of sum(acc^2): each square is exact as
+// a pair and the running sum carries its rounding error, so the total is
+// exact to about 2^-48 whatever the summation order.
+__device__ __forceinline__ void dd_add(float &hi, float &lo, float x, float xl) {
+  float s, e;
+  two_sum(hi, x, s, e);
+  hi = s;
+  lo = __fadd_rn(lo, __fadd_rn(e, xl));
+}
+// rstd = 1 / sqrt(sum / H + eps) from the block's (hi, lo) partial sums, as
+// an unevaluated f32 pair rh + rl accurate to about 2^-44 relative (no FP64:
+// it is slow on this part).  sum / H and + eps are carried as double-floats;
+// rsqrtf gives r0, and one Newton step with its second-order term,
+// r = r0 (1 - t/2 + 3t^2/8) with t = x r0^2 - 1 evaluated with FMAs, gives
+// the rest.  Every thread ends with the same pair.
+template <int NTHR>
+__device__ __forceinline__ void block_rstd_dd(float hi, float lo, float2 *red, int H, float eps, float &rh,
+                                              float &rl) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float oh = __shfl_xor_sync(0xffffffffu, hi, o), ol = __shfl_xor_sync(0xffffffffu, lo, o);
+    dd_add(hi, lo, oh, ol);
+  }
+  if (lane == 0) red[warp] = make_float2(hi, lo);
+  __syncthreads();
+  float sh = red[0].x, sl = red[0].y;
+#pragma unroll
+  for (int w = 1; w < NTHR / 32; ++w) dd_add(sh, sl, red[w].x, red[w].y);
+  // x = sum / H + eps
+  const float fh = (float)H;
+  const float qh = __fdiv_rn(sh, fh);
+  const float rem = __fmaf_rn(-qh, fh, sh);  // exact: sh - qh * H
+  const float ql = __fdiv_rn(__fadd_rn(rem, sl), fh);
+  float xh, xe;
+  two_sum(qh, eps, xh, xe);
+  const float xl = __fadd_rn(ql, xe);
+  const float r0 = rsqrtf(xh);
+  float p, pe;
+  two_prod(r0, r0, p, pe);
+  float t = __fmaf_rn(xh, p, -1.0f);
+  t = __fmaf_rn(xh, pe, t);
+  t = __fmaf_rn(xl, p, t);
+  rh = r0;
+  rl = __fmul_rn(__fmul_rn(r0, t), __fmaf_rn(0.375f, t, -0.5f));
+}
+
+// The smallest e with 448 * 2^e >= amax (amax > 0), clamped to [-127, 127];
+// exact, from the bits of amax: amax = (1 + f) 2^E and 448 = 1.75 * 2^8.
+__device__ __forceinline__ int mx_exponent(float amax) {
+  if (!(amax > 0.f)) return 0;
+  const uint32_t b = __float_as_uint(amax);
+  const int E = (int)((b >> 23) & 255);
+  if (E == 0) return -127;
+  const int e = (E - 127) - 8 + ((b & 0x7fffffu) > 0x600000u ? 1 : 0);
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+__device__ __forceinline__ float pow2_neg(int e) {  // 2^-e, e in [-127, 127]
+  return e == 127 ? __uint_as_float(0x00400000u) : __uint_as_float((uint32_t)(127 - e) << 23);
+}
+
+template <int NTHR>
+__device__ __forceinline__ float block_max(float v, float *red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  __syncthreads();  // red may still be read by a previous reduction
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float r = red[0];
+#pragma unroll
+  for (int w = 1; w < NTHR / 32; ++w) r = fmaxf(r, red[w]);
+  return r;
+}
+
+// Normalise and quantise token row m with the NTHR threads of the block
+// (every thread must call it).  Chunks of 8 elements: thread tid holds chunks
+// tid + NTHR * j, j < MAXC, so H <= 8 * NTHR * MAXC; NTHR % 4 == 0 keeps the
+// four chunks of a 32-element MXFP8 block in lanes 4i .. 4i + 3.
+template <int WFMT, int NTHR, int MAXC>
+__device__ __forceinline__ void norm_quant_row(const Params &p, const int m, float *red, float2 *red2) {
+  static_assert(NTHR % 32 == 0, "whole warps");
+  const int tid = threadIdx.x;
+  const int H = p.H, nch = H >> 3, ksf = H >> 5;
+  const uint4 *ar = reinterpret_cast<const uint4 *>(p.ar + (int64_t)m * H);
+  const uint4 *res = reinterpret_cast<const uint4 *>(p.res + (int64_t)m * H);
+  uint4 *rout = p.residual ? reinterpret_cast<uint4 *>(p.residual + (int64_t)m * H) : nullptr;
+  float acc[MAXC][8];
+  float ss = 0.f, ss_lo = 0.f;
+  uint4 gpre[MAXC];  // the input-norm gamma, loaded with the row
+  const uint4 *g4 = reinterpret_cast<const uint4 *>(p.g_in);
+#pragma unroll
+  for (int j = 0; j < MAXC; ++j) {
+    const int c = tid + NTHR * j;
+    if (c < nch) gpre[j] = __ldg(g4 + c);
+  }
+#pragma unroll
+  for (int j = 0; j < MAXC; ++j) {
+    const int c = tid + NTHR * j;
+    if (c < nch) {
+      const uint4 a = __ldcs(ar + c), r = __ldcs(res + c);
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, rw[4] = {r.x, r.y, r.z, r.w};
+      uint32_t ow[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float lo = bf16_to_f32(aw[i] & 0xffff) + bf16_to_f32(rw[i] & 0xffff);
+        float hi = bf16_to_f32(aw[i] >> 16) + bf16_to_f32(rw[i] >> 16);
+        acc[j][2 * i] = lo;
+        acc[j][2 * i + 1] = hi;
+        ow[i] = (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
+        float q, ql;
+        two_prod(lo, lo, q, ql);
+        dd_add(ss, ss_lo, q, ql);
+        two_prod(hi, hi, q, ql);
+        dd_add(ss, ss_lo, q, ql);
+      }
+      if (rout) __stcs(rout + c, make_uint4(ow[0], ow[1], ow[2], ow[3]));
+    }
+  }
+  // The normalised row n = acc * rstd * (1 + gamma) is rounded to f32 once,
+  // from an (almost) exact value: sum(acc^2) and rstd as double-floats, the
+  // products as error-free pairs.  An FP8 code
+  // that moved by one step would shift the whole token's projection, so the
+  // f32 n (and everything quantised from it) follows the definition exactly
+  // rather than one particular rounding order.
+  float rh, rl;
+  block_rstd_dd<NTHR>(ss, ss_lo, red2, H, p.eps, rh, rl);
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < MAXC; ++j) {
+    const int c = tid + NTHR * j;
+    if (c < nch) {
+      const uint32_t gw[4] = {gpre[j].x, gpre[j].y, gpre[j].z, gpre[j].w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float gam = bf16_to_f32(i & 1 ? gw[i >> 1] >> 16 : gw[i >> 1] & 0xffff);
+        // acc * (rh + rl) = p + e1 + e2, then (p + e) * (1 + gam)
+        float p1, e1, a1, a2, s1, s2;
+        two_prod(acc[j][i], rh, p1, e1);
+        const float e = __fadd_rn(e1, __fmul_rn(acc[j][i], rl));
+        two_prod(p1, gam, a1, a2);
+        two_sum(p1, a1, s1, s2);
+        const float tail = __fadd_rn(__fadd_rn(s2, a2), __fmaf_rn(e, gam, e));
+        acc[j][i] = __fadd_rn(s1, tail);
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(acc[j][e]));
+    }
+  }
+  uint2 *xq = reinterpret_cast<uint2 *>(p.xq + (int64_t)m * H);
+  if (WFMT == 0) {
+    const float tmax = block_max<NTHR>(amax, red);
+    const float s = tmax == 0.f ? 1.0f : __fdiv_rn(tmax, kFp8Max);
+#pragma unroll
+    for (int j = 0; j < MAXC; ++j) {
+      const int c = tid + NTHR * j;
+      if (c < nch) {
+        uint2 w;
+        w.x = e4m3x4(__fdiv_rn(acc[j][0], s), __fdiv_rn(acc[j][1], s), __fdiv_rn(acc[j][2], s),
+                     __fdiv_rn(acc[j][3], s));
+        w.y = e4m3x4(__fdiv_rn(acc[j][4], s), __fdiv_rn(acc[j][5], s), __fdiv_rn(acc[j][6], s),
+                     __fdiv_rn(acc[j][7], s));
+        xq[c] = w;
+      }
+    }
+    if (tid == 0) p.x_scale[m] = s;
+  } else {
+    // a 32-element block is 4 consecutive chunks, held by lanes 4i .. 4i + 3
+#pragma unroll
+    for (int j = 0; j < MAXC; ++j) {
+      const int c = tid + NTHR * j;
+      if (j * NTHR < nch) {  // warp-uniform: every lane reaches the shuffles
+        float bm = 0.f;
+        if (c < nch)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) bm = fmaxf(bm, fabsf(acc[j][e]));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+        if (c < nch) {
+          const int e = mx_exponent(bm);
+          const float inv = pow2_neg(e);
+          uint2 w;
+          w.x = e4m3x4(acc[j][0] * inv, acc[j][1] * inv, acc[j][2] * inv, acc[j][3] * inv);
+          w.y = e4m3x4(acc[j][4] * inv, acc[j][5] * inv, acc[j][6] * inv, acc[j][7] * inv);
+          xq[c] = w;
+          if ((c & 3) == 0) p.xsf[sf128x4_offset(m, c >> 2, ksf)] = (uint8_t)(e + 127);
+        }
+      }
+    }
+  }
+}
+
+}  // namespace pa

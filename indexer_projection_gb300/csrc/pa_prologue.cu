@@ -1,88 +1,20 @@
 // Prologue of the pre-attention step: one CTA per token row.
-//   acc = ar + res (f32), residual = bf16(acc)
-//   n = acc * rsqrt(mean(acc^2) + eps) * (1 + g_in)            (Gemma RMSNorm)
-//   per-channel format: s = amax(n) / 448 (1 if 0), xq = e4m3(n / s), a true
-//     f32 divide ("vllm.models.minimax_m3.amd.mono.kernels.pre_attn",
-//     emit_pre_attn / norm_quant)
-//   MXFP8 format: per 32-element block an E8M0 exponent e, the smallest with
-//     448 * 2^e >= amax(block), xq = e4m3(n * 2^-e); the codes go to the
-//     F8_128x4 layout the tensor-core path reads
-//     ("vllm.models.minimax_m3.nvidia.ops.qkv_index_fused_epilogue",
-//     prepare_SF).
+// residual add, Gemma RMSNorm and the activation quantiser (pa_norm.cuh),
+// used ahead of the tensor-core path and of the skinny path at large H.
 // HBM-bound: 16-byte coalesced loads and stores, the row held in registers,
 // warp-shuffle + shared-memory block reductions for sum(acc^2) and amax.
 #include "pa_device.cuh"
 #include "pa_launch.h"
+#include "pa_norm.cuh"
 
 namespace pa {
 
 constexpr int kProThreads = 256;
-constexpr int kProMaxChunks = 8;  // 8 chunks x 8 elements x 256 threads = H <= 16384
 
-__device__ __forceinline__ float block_max(float v, float *red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  __syncthreads();  // red may still be read by a previous reduction
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  float r = red[0];
-#pragma unroll
-  for (int w = 1; w < kProThreads / 32; ++w) r = fmaxf(r, red[w]);
-  return r;
-}
-
-// Error-free transformations (Knuth two-sum, FMA two-product): a + b = s + e
-// and a * b = p + e exactly.  Explicit _rn intrinsics keep the compiler from
-// contracting or reassociating them.
-__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
-  s = __fadd_rn(a, b);
-  const float bb = __fsub_rn(s, a);
-  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
-}
-__device__ __forceinline__ void two_prod(float a, float b, float &p, float &e) {
-  p = __fmul_rn(a, b);
-  e = __fmaf_rn(a, b, -p);
-}
-// (hi, lo) double-float accumulation of sum(acc^2): each square is exact as
-// a pair and the running sum carries its rounding error, so the total is
-// exact to about 2^-48 whatever the summation order.
-__device__ __forceinline__ void dd_add(float &hi, float &lo, float x, float xl) {
-  float s, e;
-  two_sum(hi, x, s, e);
-  hi = s;
-  lo = __fadd_rn(lo, __fadd_rn(e, xl));
-}
-__device__ __forceinline__ double block_sum_dd(float hi, float lo, float2 *red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float oh = __shfl_xor_sync(0xffffffffu, hi, o), ol = __shfl_xor_sync(0xffffffffu, lo, o);
-    dd_add(hi, lo, oh, ol);
-  }
-  if (lane == 0) red[warp] = make_float2(hi, lo);
-  __syncthreads();
-  double r = 0.0;
-#pragma unroll
-  for (int w = 0; w < kProThreads / 32; ++w) r += (double)red[w].x + (double)red[w].y;
-  return r;
-}
-
-// The smallest e with 448 * 2^e >= amax (amax > 0), clamped to [-127, 127];
-// exact, from the bits of amax: amax = (1 + f) 2^E and 448 = 1.75 * 2^8.
-__device__ __forceinline__ int mx_exponent(float amax) {
-  if (!(amax > 0.f)) return 0;
-  const uint32_t b = __float_as_uint(amax);
-  const int E = (int)((b >> 23) & 255);
-  if (E == 0) return -127;
-  const int e = (E - 127) - 8 + ((b & 0x7fffffu) > 0x600000u ? 1 : 0);
-  return e < -127 ? -127 : (e > 127 ? 127 : e);
-}
-__device__ __forceinline__ float pow2_neg(int e) {  // 2^-e, e in [-127, 127]
-  return e == 127 ? __uint_as_float(0x00400000u) : __uint_as_float((uint32_t)(127 - e) << 23);
-}
-
-template <int WFMT>
+// MAXC chunks of 8 elements per thread: H <= 2048 * MAXC.  The row stays in
+// registers, so MAXC is sized to H: fewer registers, more CTAs (and loads in
+// flight) per SM.
+template <int WFMT, int MAXC>
 __global__ void __launch_bounds__(kProThreads) prologue_kernel(Params p, int use_pdl) {
   __shared__ float red[kProThreads / 32];
   __shared__ float2 red2[kProThreads / 32];
@@ -91,115 +23,13 @@ __global__ void __launch_bounds__(kProThreads) prologue_kernel(Params p, int use
     pdl_wait();
   }
   const int m = blockIdx.x;
-  const int tid = threadIdx.x;
-  const int H = p.H, nch = H >> 3, ksf = H >> 5;
+  const int ksf = p.H >> 5;
   if (m >= p.M) {  // MXFP8 padding rows of the tensor-core path: scale 1, codes unused
     if (WFMT == 1)
-      for (int kb = tid; kb < ksf; kb += kProThreads) p.xsf[sf128x4_offset(m, kb, ksf)] = 127;
+      for (int kb = threadIdx.x; kb < ksf; kb += kProThreads) p.xsf[sf128x4_offset(m, kb, ksf)] = 127;
     return;
   }
-  const uint4 *ar = reinterpret_cast<const uint4 *>(p.ar + (int64_t)m * H);
-  const uint4 *res = reinterpret_cast<const uint4 *>(p.res + (int64_t)m * H);
-  uint4 *rout = p.residual ? reinterpret_cast<uint4 *>(p.residual + (int64_t)m * H) : nullptr;
-  float acc[kProMaxChunks][8];
-  float ss = 0.f, ss_lo = 0.f;
-#pragma unroll
-  for (int j = 0; j < kProMaxChunks; ++j) {
-    const int c = tid + kProThreads * j;
-    if (c < nch) {
-      const uint4 a = __ldcs(ar + c), r = __ldcs(res + c);
-      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, rw[4] = {r.x, r.y, r.z, r.w};
-      uint32_t ow[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float lo = bf16_to_f32(aw[i] & 0xffff) + bf16_to_f32(rw[i] & 0xffff);
-        float hi = bf16_to_f32(aw[i] >> 16) + bf16_to_f32(rw[i] >> 16);
-        acc[j][2 * i] = lo;
-        acc[j][2 * i + 1] = hi;
-        ow[i] = (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
-        float q, ql;
-        two_prod(lo, lo, q, ql);
-        dd_add(ss, ss_lo, q, ql);
-        two_prod(hi, hi, q, ql);
-        dd_add(ss, ss_lo, q, ql);
-      }
-      if (rout) __stcs(rout + c, make_uint4(ow[0], ow[1], ow[2], ow[3]));
-    }
-  }
-  // The normalised row n = acc * rstd * (1 + gamma) is rounded to f32 once,
-  // from an (almost) exact value: sum(acc^2) as a double-float, rstd in
-  // double (once per row), the products as error-free pairs.  An FP8 code
-  // that moved by one step would shift the whole token's projection, so the
-  // f32 n (and everything quantised from it) follows the definition exactly
-  // rather than one particular rounding order.
-  const double tot = block_sum_dd(ss, ss_lo, red2);
-  const double rstd_d = 1.0 / sqrt(tot / (double)H + (double)p.eps);
-  const float rh = (float)rstd_d, rl = (float)(rstd_d - (double)rh);
-  const uint4 *g4 = reinterpret_cast<const uint4 *>(p.g_in);
-  float amax = 0.f;
-#pragma unroll
-  for (int j = 0; j < kProMaxChunks; ++j) {
-    const int c = tid + kProThreads * j;
-    if (c < nch) {
-      const uint4 g = __ldg(g4 + c);
-      const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float gam = bf16_to_f32(i & 1 ? gw[i >> 1] >> 16 : gw[i >> 1] & 0xffff);
-        // acc * (rh + rl) = p + e1 + e2, then (p + e) * (1 + gam)
-        float p1, e1, a1, a2, s1, s2;
-        two_prod(acc[j][i], rh, p1, e1);
-        const float e = __fadd_rn(e1, __fmul_rn(acc[j][i], rl));
-        two_prod(p1, gam, a1, a2);
-        two_sum(p1, a1, s1, s2);
-        const float tail = __fadd_rn(__fadd_rn(s2, a2), __fmaf_rn(e, gam, e));
-        acc[j][i] = __fadd_rn(s1, tail);
-      }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(acc[j][e]));
-    }
-  }
-  uint2 *xq = reinterpret_cast<uint2 *>(p.xq + (int64_t)m * H);
-  if (WFMT == 0) {
-    const float tmax = block_max(amax, red);
-    const float s = tmax == 0.f ? 1.0f : __fdiv_rn(tmax, kFp8Max);
-#pragma unroll
-    for (int j = 0; j < kProMaxChunks; ++j) {
-      const int c = tid + kProThreads * j;
-      if (c < nch) {
-        uint2 w;
-        w.x = e4m3x4(__fdiv_rn(acc[j][0], s), __fdiv_rn(acc[j][1], s), __fdiv_rn(acc[j][2], s),
-                     __fdiv_rn(acc[j][3], s));
-        w.y = e4m3x4(__fdiv_rn(acc[j][4], s), __fdiv_rn(acc[j][5], s), __fdiv_rn(acc[j][6], s),
-                     __fdiv_rn(acc[j][7], s));
-        xq[c] = w;
-      }
-    }
-    if (tid == 0) p.x_scale[m] = s;
-  } else {
-    // a 32-element block is 4 consecutive chunks, held by lanes 4i .. 4i + 3
-#pragma unroll
-    for (int j = 0; j < kProMaxChunks; ++j) {
-      const int c = tid + kProThreads * j;
-      if (j * kProThreads < nch) {  // warp-uniform: every lane reaches the shuffles
-        float bm = 0.f;
-        if (c < nch)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) bm = fmaxf(bm, fabsf(acc[j][e]));
-        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
-        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
-        if (c < nch) {
-          const int e = mx_exponent(bm);
-          const float inv = pow2_neg(e);
-          uint2 w;
-          w.x = e4m3x4(acc[j][0] * inv, acc[j][1] * inv, acc[j][2] * inv, acc[j][3] * inv);
-          w.y = e4m3x4(acc[j][4] * inv, acc[j][5] * inv, acc[j][6] * inv, acc[j][7] * inv);
-          xq[c] = w;
-          if ((c & 3) == 0) p.xsf[sf128x4_offset(m, c >> 2, ksf)] = (uint8_t)(e + 127);
-        }
-      }
-    }
-  }
+  norm_quant_row<WFMT, kProThreads, MAXC>(p, m, red, red2);
 }
 
 __global__ void pack_scales_kernel(const uint8_t *src, uint8_t *dst, int rows, int ksf) {
@@ -224,8 +54,12 @@ cudaError_t launch_prologue(const Params &p, int grid, bool pdl, cudaStream_t st
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  if (p.weight_fmt == 0) return cudaLaunchKernelEx(&cfg, prologue_kernel<0>, p, (int)pdl);
-  return cudaLaunchKernelEx(&cfg, prologue_kernel<1>, p, (int)pdl);
+  const int maxc = (p.H + 8 * kProThreads - 1) / (8 * kProThreads);
+  const bool mx = p.weight_fmt == 1;
+  if (maxc <= 2) return cudaLaunchKernelEx(&cfg, mx ? prologue_kernel<1, 2> : prologue_kernel<0, 2>, p, (int)pdl);
+  if (maxc <= 3) return cudaLaunchKernelEx(&cfg, mx ? prologue_kernel<1, 3> : prologue_kernel<0, 3>, p, (int)pdl);
+  if (maxc <= 4) return cudaLaunchKernelEx(&cfg, mx ? prologue_kernel<1, 4> : prologue_kernel<0, 4>, p, (int)pdl);
+  return cudaLaunchKernelEx(&cfg, mx ? prologue_kernel<1, 8> : prologue_kernel<0, 8>, p, (int)pdl);
 }
 
 cudaError_t launch_pack_scales(const uint8_t *src, uint8_t *dst, int rows, int ksf, cudaStream_t stream) {

@@ -13,9 +13,14 @@ from tests import harness
 pytestmark = pytest.mark.gpu
 
 
-def _flags(force_gemm=True):
+def _flags(force_gemm=True, tiles=None):
     from indexer_projection_gb300 import binding as B
-    return B.PA_FLAG_FORCE_GEMM if force_gemm else 0
+    f = B.PA_FLAG_FORCE_GEMM if force_gemm else 0
+    if tiles == "single":
+        f |= B.PA_FLAG_GEMM_SINGLE
+    elif tiles == "pair":
+        f |= B.PA_FLAG_GEMM_PAIR
+    return f
 
 
 def check(wl, rows=None, flags=None, gemm_grid=0, nsample=48):
@@ -37,33 +42,50 @@ def small(name, M, fmt="ptpc", cache="fp8", nkv=1, H=512, seed=21, **kw):
     return workloads.Workload(name, H=H, nkv=nkv, M=M, weight_fmt=fmt, cache_fmt=cache, seed=seed, **base)
 
 
+TILES = ["single", "pair"]
+
+
+@pytest.mark.parametrize("tiles", TILES)
 @pytest.mark.parametrize("fmt", ["ptpc", "mx"])
 @pytest.mark.parametrize("cache", ["fp8", "nvfp4"])
-def test_small_ragged(fmt, cache):
-    check(small(f"g_{fmt}_{cache}", 200, fmt, cache, nkv=2, skip_rows=(3, 130)))
+def test_small_ragged(fmt, cache, tiles):
+    # nkv = 2: 39 heads, so the pair kernel's last tile has a zero-filled second head
+    check(small(f"g_{fmt}_{cache}_{tiles}", 200, fmt, cache, nkv=2, skip_rows=(3, 130)), flags=_flags(tiles=tiles))
 
 
-@pytest.mark.parametrize("M", [1, 5, 17, 127, 128, 129, 256])
-def test_token_counts(M):
-    check(small(f"g_m{M}", M, "mx", "nvfp4", H=1024, seed=M))
+@pytest.mark.parametrize("tiles", TILES)
+@pytest.mark.parametrize("M", [1, 5, 17, 127, 128, 129, 256, 300])
+def test_token_counts(M, tiles):
+    check(small(f"g_m{M}_{tiles}", M, "mx", "nvfp4", H=1024, seed=M), flags=_flags(tiles=tiles))
 
 
-@pytest.mark.parametrize("grid", [1, 3, 37])
-def test_persistent_grid_override(grid):
-    # fewer CTAs than tiles: every CTA walks many tiles through both TMEM buffers
-    check(small(f"g_grid{grid}", 300, "mx", "fp8", nkv=1, H=768, seed=grid), gemm_grid=grid)
+@pytest.mark.parametrize("tiles,grid", [("single", 1), ("single", 3), ("single", 37), ("pair", 2), ("pair", 6),
+                                        ("pair", 38)])
+def test_persistent_grid_override(tiles, grid):
+    # fewer CTAs than tiles: every CTA (pair) walks many tiles
+    check(small(f"g_grid{grid}_{tiles}", 600, "mx", "fp8", nkv=1, H=768, seed=grid), flags=_flags(tiles=tiles),
+          gemm_grid=grid)
 
 
-def test_long_k_and_outliers():
-    check(small("g_k6144", 136, "ptpc", "fp8", nkv=1, H=6144, seed=8, outlier_frac=0.05))
+@pytest.mark.parametrize("tiles", TILES)
+def test_per_channel_nvfp4_ragged_pair_rows(tiles):
+    check(small(f"g_pc_{tiles}", 389, "ptpc", "nvfp4", nkv=4, H=640, seed=3, page_pad=32, k_global=0.7,
+                v_global=1.3), flags=_flags(tiles=tiles))
+
+
+@pytest.mark.parametrize("tiles", TILES)
+def test_long_k_and_outliers(tiles):
+    check(small(f"g_k6144_{tiles}", 136, "ptpc", "fp8", nkv=1, H=6144, seed=8, outlier_frac=0.05),
+          flags=_flags(tiles=tiles))
 
 
 def test_spec_decode_config():
     check(workloads.spec_decode(), flags=0)
 
 
-def test_prefill_config():
-    check(workloads.prefill(), flags=0, nsample=40)
+@pytest.mark.parametrize("tiles", [None, "single"])
+def test_prefill_config(tiles):
+    check(workloads.prefill(), flags=_flags(force_gemm=False, tiles=tiles), nsample=40)
 
 
 @pytest.mark.parametrize("M", [64, 256, 1024, 4096, 16384])
