@@ -82,6 +82,7 @@ def step_flops(wl) -> int:
 
 
 KERNEL_SOURCES = {"gemv": ("pa_gemv.cu", "pa_device.cuh"), "gemm": ("pa_gemm.cu", "pa_device.cuh"),
+                  "gemm2": ("pa_gemm2.cu", "pa_device.cuh"),
                   "prologue": ("pa_prologue.cu", "pa_device.cuh")}
 
 
@@ -271,7 +272,8 @@ def run_ours(args, wl, rank, world, local_rank):
     l2 = props.L2_cache_size
     per_copy = step_bytes(wl)["weights"] + 2 * wl.M * wl.H * 2
     copies = max(2, min(64, math.ceil(2.5 * l2 / per_copy)))
-    dw = DeviceWorkload(wl, st, copies, dev)
+    flags = {"auto": 0, "single": B.PA_FLAG_GEMM_SINGLE, "pair": B.PA_FLAG_GEMM_PAIR}[args.gemm]
+    dw = DeviceWorkload(wl, st, copies, dev, flags=flags)
     stream = torch.cuda.Stream(dev)
     K, W = args.steps, args.warmup
 
@@ -323,19 +325,30 @@ def run_ours(args, wl, rank, world, local_rank):
     del graphs
 
     # main-kernel device time: events recorded around it on the launching
-    # stream, steps queued behind a GPU sleep so the host never starves the
-    # GPU between them (no programmatic overlap with the prologue here)
+    # stream, steps queued behind a GPU sleep long enough that the host never
+    # starves the GPU between them (else the events would time the host's
+    # launch calls); no programmatic overlap with the prologue here
     P = min(max(K, 50), 400)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(P)]
     for a, b in evs:  # torch creates its CUDA events on first record
         a.record(stream)
         b.record(stream)
     stream.synchronize()
-    with torch.cuda.stream(stream):
-        torch.cuda._sleep(int(1e5 * P))  # ~50 us of GPU time per queued step, ahead of the host
-        for i in range(P):
+
+    def profiled_steps(n):
+        for i in range(n):
             B.pre_attn_set_profile_events(dw.runner.handle, evs[i][0], evs[i][1])
             dw.step(i, stream)
+
+    with torch.cuda.stream(stream):
+        t_h = time.perf_counter()
+        profiled_steps(min(P, 20))
+        host_s = (time.perf_counter() - t_h) / min(P, 20)  # host time to queue one step
+    stream.synchronize()
+    sleep_cycles = int(3.0 * P * host_s * 2.1e9)  # three times the queueing time at <= 2.1 GHz
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(sleep_cycles)
+        profiled_steps(P)
     B.pre_attn_set_profile_events(dw.runner.handle, None, None)
     stream.synchronize()
     main_ms = statistics.median(a.elapsed_time(b) for a, b in evs[P // 4:])
@@ -395,21 +408,25 @@ def run_ours(args, wl, rank, world, local_rank):
     ms_step = ms / K
     tokens_s = world * wl.M / (ms_step * 1e-3)
     nb = step_bytes(wl)
-    gemm = not (wl.M <= 16)
-    kname = "gemm" if gemm else "gemv"
+    path = B.pre_attn_path(dw.runner.handle, wl.M)
+    gemm = path != B.PA_PATH_GEMV
+    kname = {B.PA_PATH_GEMV: "gemv", B.PA_PATH_GEMM_SINGLE: "gemm", B.PA_PATH_GEMM_PAIR: "gemm2"}[path]
+    kdesc = {"gemv": "pa::gemv_kernel (FP8 GEMV, one cluster per head)",
+             "gemm": "pa::gemm_kernel (tcgen05, 128x128 tiles)",
+             "gemm2": "pa::g2::gemm2_kernel (tcgen05 cta_group::2, 256x256 tiles)"}[kname]
     if gemm:
         achieved = step_flops(wl) / (main_ms * 1e-3) / 1e12
         peak = peaks["bf16_tflops"] * FP8_OVER_BF16
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "traffic": ncu_traffic(kname, args.workload),
-                "kernel": f"pa::gemm_kernel (tcgen05), {main_ms * 1e3:.2f} us/launch",
+                "kernel": f"{kdesc}, {main_ms * 1e3:.2f} us/launch",
                 "peak_source": f"{peak_src} bf16 x nominal FP8/BF16 ratio 2"}
     else:
         achieved = nb["main"] / (main_ms * 1e-3) / 1e9
         peak = peaks["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": ncu_traffic(kname, args.workload),
-                "kernel": f"pa::gemv_kernel, {main_ms * 1e3:.2f} us/launch, {nb['main']} algorithmic bytes",
+                "kernel": f"{kdesc}, {main_ms * 1e3:.2f} us/launch, {nb['main']} algorithmic bytes",
                 "peak_source": f"{peak_src} hbm_gbs"}
     step_roof = (nb["step"] / (ms_step * 1e-3) / 1e9) / peaks["hbm_gbs"]
     line = {
@@ -418,7 +435,7 @@ def run_ours(args, wl, rank, world, local_rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 x e4m3 -> f32 (bf16 in/out)", "data": "synthetic (seeded, configs' shapes; random-init weights)",
         "config": {"workload": args.workload, "hidden": wl.H, "nkv": wl.nkv, "M": wl.M, "N": wl.N,
-                   "weight": wl.weight_fmt, "cache": wl.cache_fmt, "path": "tcgen05 GEMM" if gemm else "skinny GEMV",
+                   "weight": wl.weight_fmt, "cache": wl.cache_fmt, "path": kdesc,
                    "l2": f"{copies} rotating weight+input copies ({copies * per_copy / 1e6:.0f} MB > 2x L2)",
                    "timing": "CUDA graph of K steps, PDL chained", "parallelism": f"replicas x{world}"},
         "roofline": roof,
@@ -496,6 +513,8 @@ def main():
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--gemm", default="auto", choices=["auto", "single", "pair"],
+                    help="tensor-core path tiling (auto: chosen per shape)")
     args = ap.parse_args()
     wl = get_workload(args.workload)
     rank = int(os.environ.get("RANK", 0))

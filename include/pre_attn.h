@@ -195,13 +195,13 @@ const char *pre_attn_strerror(int status);
 int pre_attn_out_features(const pa_handle *h);
 
 /* Bytes of device workspace pre_attn_run needs for up to M rows (M <= the
- * handle's max_tokens), including a status word and the skinny path's
- * per-head arrival counters.  Returns 0 for an invalid handle or M. */
+ * handle's max_tokens): a status word and the quantised activations with
+ * their scales.  Returns 0 for an invalid handle or M. */
 size_t pre_attn_workspace_bytes(const pa_handle *h, int M);
 
 /* Zero a freshly allocated workspace (cudaMemsetAsync on `stream`).  Must be
- * called once before the workspace's first pre_attn_run; the kernels keep
- * it valid afterwards.  Errors: PA_ERR_NULL, PA_ERR_CUDA. */
+ * called once before the workspace's first pre_attn_run (the status word
+ * starts clear).  Errors: PA_ERR_NULL, PA_ERR_CUDA. */
 int pre_attn_workspace_init(void *workspace, size_t bytes, void *stream);
 
 /* Bytes of the F8_128x4 layout for an [rows, hidden/32] E8M0 grid
@@ -252,7 +252,7 @@ int pre_attn_set_profile_events(pa_handle *h, void *before_main, void *after_mai
  * after start-up fails.
  * It runs the same step as pre_attn_run (same arguments minus the workspace)
  * for 0 <= M <= 16 token rows, with the kernels' scratch (status word,
- * per-head counters, quantised activations, f32 projection rows) in a fixed
+ * quantised activations and their scales) in a fixed
  * 2 MiB array inside this library; every GPU that loads the library holds
  * that array until the process exits.  It calls no cudaMalloc, cudaFree or
  * allocating library routine.
@@ -267,6 +267,20 @@ int pre_attn_set_profile_events(pa_handle *h, void *before_main, void *after_mai
  * handle's max_tokens, or pre_attn_workspace_bytes(h, M) exceeds 2 MiB. */
 int pre_attn_run_noalloc(pa_handle *h, int M, const pa_step_inputs *in, const pa_weights *wt,
                          const pa_caches *caches, const pa_outputs *out, void *stream);
+
+/* Main kernels a call can run (pre_attn_path). */
+enum {
+  PA_PATH_GEMV = 0,         /* skinny path: FP8 GEMV on one cluster per head (M <= 16) */
+  PA_PATH_GEMM_SINGLE = 1,  /* tensor-core path, 128 x 128 tiles on single SMs */
+  PA_PATH_GEMM_PAIR = 2     /* tensor-core path, 256 x 256 tiles on SM pairs */
+};
+
+/* Which main kernel pre_attn_run(h, M, ...) launches on the current device
+ * (PA_PATH_*; the choice depends on M, the handle's flags and the device's
+ * SM count).  Returns a negative PA_ERR_* value for a NULL handle
+ * (-PA_ERR_NULL), an M outside [1, max_tokens] or one the flags exclude
+ * (-PA_ERR_SHAPE), or a failed device query (-PA_ERR_CUDA). */
+int pre_attn_path(pa_handle *h, int M);
 
 /* The last CUDA error string seen by this thread's calls ("" if none). */
 const char *pre_attn_last_cuda_error(void);

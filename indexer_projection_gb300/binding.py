@@ -27,6 +27,7 @@ PA_WEIGHT_FP8_PER_CHANNEL, PA_WEIGHT_MXFP8 = 0, 1
 PA_CACHE_FP8, PA_CACHE_NVFP4 = 0, 1
 PA_FLAG_STATIC_KV_SCALE, PA_FLAG_FORCE_GEMV, PA_FLAG_FORCE_GEMM, PA_FLAG_NO_PDL = 1, 2, 4, 8
 PA_FLAG_GEMM_SINGLE, PA_FLAG_GEMM_PAIR = 16, 32
+PA_PATH_GEMV, PA_PATH_GEMM_SINGLE, PA_PATH_GEMM_PAIR = 0, 1, 2
 
 _vp = ctypes.c_void_p
 
@@ -95,6 +96,7 @@ def load(path: str = LIB_PATH):
                              ctypes.POINTER(pa_caches), ctypes.POINTER(pa_outputs), _vp, sz, _vp]),
         "pre_attn_device_status": (i, [_vp, u32p, _vp]),
         "pre_attn_last_cuda_error": (ctypes.c_char_p, []),
+        "pre_attn_path": (i, [H, i]),
         "pre_attn_set_profile_events": (i, [H, _vp, _vp]),
         "pre_attn_run_noalloc": (i, [H, i, ctypes.POINTER(pa_step_inputs), ctypes.POINTER(pa_weights),
                                      ctypes.POINTER(pa_caches), ctypes.POINTER(pa_outputs), _vp]),
@@ -152,6 +154,14 @@ def pre_attn_destroy(h) -> None:
 
 def pre_attn_out_features(h) -> int:
     return load().pre_attn_out_features(h)
+
+
+def pre_attn_path(h, M: int) -> int:
+    """PA_PATH_* of the main kernel a call with M rows launches."""
+    st = load().pre_attn_path(h, int(M))
+    if st < 0:
+        raise PreAttnError(-st, "pre_attn_path")
+    return st
 
 
 def pre_attn_workspace_bytes(h, M: int) -> int:

@@ -32,12 +32,11 @@ int cuda_fail(cudaError_t e) {
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Workspace layout for M rows.  The first 256 bytes hold the status word
-// (offset 0), the fused skinny path's finished-CTA counter (8) and its 16
-// row flags (128); the per-head counters follow at 256.  These carry state
-// between calls (each call leaves them zero); the rest is scratch.
+// Workspace layout for M rows.  The status word sits at offset 0 and carries
+// state between calls (PA_DEV_* bits, sticky until read); the rest is
+// scratch: the prologue's quantised activations and their scales.
 struct WsLayout {
-  size_t status, cnt, x_scale, xsf, xq, y, total;
+  size_t status, x_scale, xsf, xq, total;
   int m_pad;
 };
 
@@ -46,19 +45,51 @@ WsLayout ws_layout(const pa_handle *h, int M) {
   const size_t H = (size_t)h->cfg.hidden;
   L.m_pad = (M + 127) / 128 * 128;
   L.status = 0;
-  L.cnt = 256;
-  size_t off = align_up(L.cnt + sizeof(int) * (size_t)h->n_heads, 256);
+  size_t off = 256;
   L.x_scale = off;
   off = align_up(off + sizeof(float) * (size_t)(M > 0 ? M : 1), 256);
   L.xsf = off;
-  off = align_up(off + (size_t)(L.m_pad > 0 ? L.m_pad : 128) * (H / 32), 256);
+  if (h->cfg.weight_format == PA_WEIGHT_MXFP8)  // the MXFP8 activation scales
+    off = align_up(off + (size_t)(L.m_pad > 0 ? L.m_pad : 128) * (H / 32), 256);
   L.xq = off;
   off = align_up(off + (size_t)M * H, 256);
-  L.y = off;
-  const int my = M < 16 ? M : 16;  // the skinny path's f32 projection rows
-  off = align_up(off + sizeof(float) * (size_t)my * (size_t)h->N, 256);
   L.total = off;
   return L;
+}
+
+// The device's SM count, queried once per device.
+cudaError_t query_sms(pa_handle *h) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (h->device != dev) {
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    h->num_sms = sms;
+    h->device = dev;
+  }
+  return cudaSuccess;
+}
+
+bool uses_gemv(const pa_config &c, int M) {
+  return (c.flags & PA_FLAG_FORCE_GEMV) ? true : (c.flags & PA_FLAG_FORCE_GEMM) ? false : M <= 16;
+}
+
+// Main kernel for M rows (h->num_sms known).  256 x 256 pair tiles cost
+// about 1.5x a 128 x 128 tile on one SM: the pairs are used unless wave
+// quantisation favours the finer tiles.
+int choose_path(const pa_handle *h, int M) {
+  const pa_config &c = h->cfg;
+  if (uses_gemv(c, M)) return PA_PATH_GEMV;
+  if (c.flags & PA_FLAG_GEMM_SINGLE) return PA_PATH_GEMM_SINGLE;
+  if (c.flags & PA_FLAG_GEMM_PAIR) return PA_PATH_GEMM_PAIR;
+  const int sms = h->num_sms > 1 ? h->num_sms : 2;
+  const int64_t t1 = (int64_t)((M + 127) / 128) * (h->N / 128);
+  const int64_t t2 = (int64_t)((M + 255) / 256) * ((h->N + 255) / 256);
+  const int64_t w1 = (t1 + sms - 1) / sms;
+  const int64_t w2 = (t2 + sms / 2 - 1) / (sms / 2);
+  return 3 * w2 <= 2 * w1 ? PA_PATH_GEMM_PAIR : PA_PATH_GEMM_SINGLE;
 }
 
 bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb) {
@@ -88,6 +119,15 @@ const char *pre_attn_strerror(int s) {
 }
 
 const char *pre_attn_last_cuda_error(void) { return g_cuda_err; }
+
+int pre_attn_path(pa_handle *h, int M) {
+  if (!h) return -PA_ERR_NULL;
+  if (M < 1 || M > h->cfg.max_tokens) return -PA_ERR_SHAPE;
+  if (uses_gemv(h->cfg, M) && M > 16) return -PA_ERR_SHAPE;
+  const cudaError_t e = query_sms(h);
+  if (e != cudaSuccess) return -cuda_fail(e);
+  return choose_path(h, M);
+}
 
 int pre_attn_init(const pa_config *cfg, pa_handle **out) {
   if (!cfg || !out) return PA_ERR_NULL;
@@ -219,21 +259,13 @@ int pre_attn_run(pa_handle *h, int M, const pa_step_inputs *in, const pa_weights
     for (const void *src : {in->ar, in->res})
       if (out->residual != src && ranges_overlap(out->residual, act_bytes, src, act_bytes)) return PA_ERR_ALIAS;
   }
-  const bool gemv = (c.flags & PA_FLAG_FORCE_GEMV) ? true : (c.flags & PA_FLAG_FORCE_GEMM) ? false : M <= 16;
+  const bool gemv = uses_gemv(c, M);
   if (gemv && M > 16) return PA_ERR_SHAPE;
   if (M == 0) return PA_OK;
 
-  // the device's SM count, queried once per device
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = query_sms(h);
   if (e != cudaSuccess) return cuda_fail(e);
-  if (h->device != dev) {
-    int sms = 0;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return cuda_fail(e);
-    h->num_sms = sms;
-    h->device = dev;
-  }
+  const int path = choose_path(h, M);
 
   pa::Params p;
   memset(&p, 0, sizeof(p));
@@ -295,39 +327,22 @@ int pre_attn_run(pa_handle *h, int M, const pa_step_inputs *in, const pa_weights
   p.q_fp8_inv = out->q_fp8 ? 1.0f / out->q_fp8_scale : 1.0f;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   p.status = reinterpret_cast<uint32_t *>(ws + L.status);
-  p.head_cnt = reinterpret_cast<int *>(ws + L.cnt);
   p.x_scale = reinterpret_cast<float *>(ws + L.x_scale);
   p.xsf = ws + L.xsf;
   p.xq = ws + L.xq;
-  p.y = reinterpret_cast<float *>(ws + L.y);
-  p.done_cnt = reinterpret_cast<int *>(ws + L.status + 8);
-  p.row_flag = reinterpret_cast<int *>(ws + L.status + 128);
   p.m_pad = L.m_pad;
 
   const bool pdl = !(c.flags & PA_FLAG_NO_PDL);
   cudaStream_t s = (cudaStream_t)stream;
-  // the skinny path normalises the rows inside its own launch when it can
-  const bool fused = gemv && pa::gemv_fuses_prologue(p);
-  if (!fused) {
-    const int pro_grid = (!gemv && c.weight_format == PA_WEIGHT_MXFP8) ? L.m_pad : M;
-    e = pa::launch_prologue(p, pro_grid, pdl, s);
-    if (e != cudaSuccess) return cuda_fail(e);
-  }
+  const int pro_grid = (!gemv && c.weight_format == PA_WEIGHT_MXFP8) ? L.m_pad : M;
+  e = pa::launch_prologue(p, pro_grid, pdl, s);
+  if (e != cudaSuccess) return cuda_fail(e);
   if (h->prof_before && (e = cudaEventRecord(h->prof_before, s)) != cudaSuccess) return cuda_fail(e);
   if (gemv) {
-    e = pa::launch_gemv(p, h->num_sms, pdl, fused, s);
+    e = pa::launch_gemv(p, pdl, s);
   } else {
-    // 256 x 256 pair tiles cost about 1.5x a 128 x 128 tile on one SM: use the
-    // pairs unless wave quantisation favours the finer tiles
-    const int64_t t1 = (int64_t)((M + 127) / 128) * (h->N / 128);
-    const int64_t t2 = (int64_t)((M + 255) / 256) * ((h->N + 255) / 256);
-    const int64_t w1 = (t1 + h->num_sms - 1) / h->num_sms;
-    const int64_t w2 = (t2 + h->num_sms / 2 - 1) / (h->num_sms / 2);
-    bool pair = 3 * w2 <= 2 * w1;
-    if (c.flags & PA_FLAG_GEMM_SINGLE) pair = false;
-    if (c.flags & PA_FLAG_GEMM_PAIR) pair = true;
-    e = pair ? pa::launch_gemm_pair(p, h->num_sms, c.gemm_grid, pdl, s)
-             : pa::launch_gemm(p, h->num_sms, c.gemm_grid, pdl, s);
+    e = path == PA_PATH_GEMM_PAIR ? pa::launch_gemm_pair(p, h->num_sms, c.gemm_grid, pdl, s)
+                                  : pa::launch_gemm(p, h->num_sms, c.gemm_grid, pdl, s);
   }
   if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return cuda_fail(e);

@@ -55,13 +55,9 @@ struct Params {
   float q_fp8_inv;           // 1 / q_fp8_scale (f32 reciprocal)
   // workspace
   uint32_t *status;
-  int *head_cnt;             // [n_heads] arrival counters (skinny path)
   uint8_t *xq;               // [M, H] e4m3 activations
   float *x_scale;            // [M] per-token scales (per-channel format)
   uint8_t *xsf;              // MXFP8 activation scales, F8_128x4 of [Mpad, H/32]
-  float *y;                  // [M, N] f32 projection rows (skinny path only)
-  int *row_flag;             // [16] fused skinny path: row m's activations are published
-  int *done_cnt;             // fused skinny path: CTAs finished (the last one resets the flags)
   int m_pad;                 // M rounded up to 128 (MXFP8 scale rows)
 };
 
@@ -164,6 +160,83 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
   const uint64_t t0 = globaltimer();
   while (true) {
     if (mbar_try_wait(a, parity)) return true;
+    if (globaltimer() - t0 > 1000000000ull) {
+      set_status(status, kDevWaitTimeout);
+      return false;
+    }
+  }
+}
+
+// ------------------------------------------- asynchronous global -> shared
+// (cp.async: no registers held while the copy is in flight; .cg bypasses L1,
+// so data written by the previous kernel is read from L2)
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(void *dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's committed groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ------------------------------------------------------ thread-block clusters
+__device__ __forceinline__ uint32_t cta_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// This CTA's shared address `saddr` as seen in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+// Arrive (release at cluster scope) on an mbarrier given by its cluster address.
+__device__ __forceinline__ void arrive_remote(uint32_t caddr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t caddr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(caddr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
+// Asynchronous store of 16 bytes into the shared memory of a CTA of the
+// cluster; its completion counts 16 bytes on that CTA's mbarrier `cbar`
+// (both addresses in the destination CTA, as given by mapa).
+__device__ __forceinline__ void st_async_v4(uint32_t caddr, float4 v, uint32_t cbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1,%2,%3,%4}, [%5];" ::"r"(caddr),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(cbar)
+               : "memory");
+}
+// Wait for phase `parity` of a local mbarrier whose arrivals come from other
+// CTAs of the cluster (acquire at cluster scope), giving up after about a
+// second (PA_DEV_WAIT_TIMEOUT).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, uint32_t *status) {
+  const uint32_t a = smem_u32(bar);
+  auto try_wait = [&]() {
+    uint32_t ok;
+    asm volatile(
+        "{.reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p;}"
+        : "=r"(ok) : "r"(a), "r"(parity) : "memory");
+    return ok != 0;
+  };
+  if (try_wait()) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    if (try_wait()) return true;
     if (globaltimer() - t0 > 1000000000ull) {
       set_status(status, kDevWaitTimeout);
       return false;

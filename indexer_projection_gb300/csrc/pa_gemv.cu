@@ -1,439 +1,375 @@
 // Skinny-M path of the pre-attention projection (M <= 16 token rows, the
 // decode shapes): an HBM-bound FP8 GEMV over the fused [q|k|v|index_q|index_k]
-// weight with the per-head epilogue fused behind it.
+// weight on the tcgen05 tensor cores, one thread-block cluster per 128-channel
+// head, with the head's epilogue fused behind it.
 //
-// Work split: CTA c of G owns output channels [c*N/G, (c+1)*N/G) (balanced to
-// one row) over all of K.  A producer warp streams the CTA's weight rows
-// through a shared-memory ring with 1-D bulk copies (cp.async.bulk, one copy
-// a row a stage, 512-1536 K bytes), issued before the kernel waits on the
-// prologue (programmatic dependent launch), so the weight stream overlaps the
-// prologue and the previous kernel's tail; at the decode shape the whole
-// weight slice is in flight at once.  Eight consumer warps own contiguous K
-// ranges of each stage; their activation fragments are loaded into registers
-// once, right after the wait, so the K loop never waits on L2.  The inner
-// products are e4m3 m16n8k32 warp MMAs with the tokens on the B columns (the
-// pre_attn page's GEMV tasks put the token on the MFMA B column the same
-// way): a few hundred per CTA, far below the weight stream's time, so the
-// legacy MMA is ample here; the dense prefill contraction uses tcgen05.
+// Work split.  The C CTAs of head h's cluster (C = 16, or 8 where the device
+// cannot co-schedule clusters of 16) each own the head's 128 weight rows over
+// one K range of kc = ceil(K / C) bytes rounded up to 128 (384 at K = 6144).
+// Every thread copies its share of the range's weight rows from HBM straight
+// into shared memory with 16-byte cp.async (no registers held), in the
+// 128-byte-swizzled K-major layout the tensor core reads, all issued before
+// the kernel waits on the prologue (programmatic dependent launch), so the
+// weight stream overlaps the prologue.  After the wait the CTA stages the
+// range's activations the same way and one thread issues the MMAs:
+// tcgen05.mma m128 n16 k32 per 32 bytes of K, weights as A (128 rows),
+// tokens as B (16 columns, the absent ones zero), f32 accumulator in tensor
+// memory (kind::f8f6f4; for MXFP8 kind::mxf8f6f4.block_scale with the
+// F8_128x4 scale atoms of both operands moved to tensor memory by
+// tcgen05.cp).  A K range longer than the 3 staged 128-byte chunks is
+// streamed in batches.  The pre_attn page's GEMV tasks put the token on the
+// MFMA B column the same way.
 //
-// Per 32-element K block the MXFP8 format rescales each MMA result by
-// 2^(e_w + e_x) before accumulating ([EPI] MXFP8 projection), with both
-// operands' block scales staged in shared memory; the per-channel format
-// scales once at the end by x_scale * w_scale
+// Per 32-element K block the MXFP8 format scales each product by
+// 2^(e_w + e_x) inside the MMA ([EPI] MXFP8 projection); the per-channel
+// format scales the summed rows by x_scale * w_scale
 // ("vllm.models.minimax_m3.amd.mono.kernels.pre_attn", GEMV tasks).
 //
-// The projection rows go to an f32 scratch in the workspace; the CTA whose
-// arrival completes a head's 128 channels (an atomic counter per head, no
-// waiting) runs that head's epilogue for every token: one warp per token,
-// 4 dims per lane, as the pre_attn page's head tasks.  The tokens' positions,
-// slots and cos/sin rows and the head gammas are staged in shared memory
-// while the weights stream, so the finishing CTA waits only on its rows.
+// Reduction and epilogue, inside the cluster: warps 0-3 read the 128 x 16
+// accumulator (thread = weight row) and store each token m's partial rows
+// into the shared memory of cluster CTA m % C with asynchronous
+// distributed-shared-memory stores that count their bytes on that CTA's
+// mbarrier (no fences, no arrivals).  CTA m % C, once all C x 512 bytes of
+// the token's partials are in, sums the C K-range partials of the head's 128
+// channels and runs the head epilogue for token m, one warp, 4 dims a lane,
+// as the pre_attn page's head tasks.  Nothing goes through global memory
+// between the MMAs and the outputs.
+//
+// The weight, its scales, the head's gamma and w_scale are read before the
+// wait on the previous kernel: they must not be written by work still in
+// flight on the stream (they are model constants).  Everything else is read
+// after the wait.  Every mbarrier wait is bounded (about a second; then
+// PA_DEV_WAIT_TIMEOUT), and the tensor memory is freed on every path.
 #include "pa_device.cuh"
 #include "pa_launch.h"
-#include "pa_norm.cuh"
+#include "pa_tc.cuh"
 
 namespace pa {
 
-constexpr int kGvConsumers = 8;
-constexpr int kGvThreads = (kGvConsumers + 1) * 32;
-constexpr int kSlice = 64;               // K bytes of one MMA pair (two 32-element blocks)
-constexpr int kMaxMT = 5;                // up to 80 weight rows per CTA
-constexpr int kMaxRows = 16 * kMaxMT;
-constexpr int kRingBudget = 108 * 1024;  // two CTAs fit on an SM (overlap of consecutive steps)
-constexpr int kBRegSlices = 12;          // activation slices a warp keeps in registers (K <= 6144)
+constexpr int kGvThreads = 256;
+constexpr int kChunk = 128;        // K bytes of one swizzle atom column (4 MMAs)
+constexpr int kStageChunks = 3;    // weight chunks staged at once (48 KB)
+constexpr int kWChunkBytes = kHeadDim * kChunk;  // 16 KB: 128 rows x 128 B
+constexpr int kXChunkBytes = 16 * kChunk;        // 2 KB: 16 token rows x 128 B
+constexpr int kSfAtom = 512;       // F8_128x4: 128 rows x 4 K-blocks
 constexpr int kMaxTok = 16;
+constexpr int kTmemCols = 32;      // accumulator 16 columns, scale factors at 16 and 20
+constexpr int kSfaCol = 16, kSfbCol = 20;
+constexpr uint32_t kIdescF8 = idesc_f8(128, 16);
+constexpr uint32_t kIdescMx = idesc_mx(128, 16);
 
-constexpr int kFusedMaxChunks = 4;       // fused row normalisation: H <= 8 * 288 * 4 = 9216
-constexpr int kFusedMaxH = 8 * kGvThreads * kFusedMaxChunks;
+// Byte offsets of the dynamic shared memory from its 1024-aligned base.
+struct GvLayout {
+  int w;     // [kStageChunks] weight chunks, 128 rows x 128 B, 128B-swizzled
+  int x;     // [nchunks] activation chunks, 16 rows x 128 B, 128B-swizzled
+  int sfa;   // MXFP8 [kStageChunks] weight scale atoms
+  int sfb;   // MXFP8 [nchunks] activation scale atoms
+  int recv;  // [TS][C][128] f32 partial rows received from the cluster
+  int total;
+};
+__host__ __device__ inline GvLayout gv_layout(int C, int kc, int mx) {
+  GvLayout L;
+  const int nch = kc / kChunk;
+  const int ts = (kMaxTok + C - 1) / C;
+  L.w = 0;
+  L.x = L.w + kStageChunks * kWChunkBytes;
+  L.sfa = L.x + nch * kXChunkBytes;
+  L.sfb = L.sfa + (mx ? kStageChunks * kSfAtom : 0);
+  L.recv = L.sfb + (mx ? nch * kSfAtom : 0);
+  L.total = L.recv + ts * C * kHeadDim * 4;
+  return L;
+}
 
+// Small per-CTA state (static shared memory).
 struct GvStatic {
-  int64_t slot[kMaxTok], islot[kMaxTok];
-  __nv_bfloat16 cs[kMaxTok][kRotDim];
-  __nv_bfloat16 gam[4][kHeadDim];
-  float red[kGvThreads / 32];
-  float2 red2[kGvThreads / 32];
-  int fin[8];
-  int nfin;
+  float wsc[kHeadDim];           // per-channel weight scales of the head
+  __nv_bfloat16 gam[kHeadDim];   // the head role's gamma
+  __nv_bfloat16 cs[2][kRotDim];  // cos / sin rows of the tokens finished here
+  float xs[kMaxTok];             // per-token activation scales
+  int64_t slot[2], islot[2];
+  uint64_t mma_bar;              // the MMAs of a batch have completed
+  uint64_t recv_bar;             // partial rows received (transaction bytes)
+  uint32_t tmem;
+  int ok;
 };
 
-// FUSED: the step in one launch.  CTAs 0 .. M-1 first normalise and quantise
-// token row blockIdx.x (the prologue, pa_norm.cuh) and publish it with a
-// release flag; every CTA has its weight stream in flight before that and
-// waits (bounded) on the flags of all M rows before its MMAs.  The last CTA
-// to finish clears the flags for the next launch.
-template <int WFMT, int NT, bool BREG, bool FUSED>
-__global__ void __launch_bounds__(kGvThreads, NT == 1 ? 2 : 1)
-    gemv_kernel(Params p, int G, int rmax, int S, int chunk, int use_pdl) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ GvStatic sm;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int N = p.N, K = p.H, M = p.M;
-  const int r0 = (int)((int64_t)blockIdx.x * N / G), r1 = (int)((int64_t)(blockIdx.x + 1) * N / G);
-  const int R = r1 - r0;
-  const int MT = (R + 15) >> 4;
-  const int nchunks = (K + chunk - 1) / chunk;
-  const int jw = chunk / (kSlice * kGvConsumers);  // slices per warp per chunk
-  const int pitch = chunk + 32;                    // rows 32 B apart modulo 128: conflict-free 8-byte reads
-  const int ksf = K >> 5;
-  const int stage_bytes = rmax * pitch;
-  const int ring_bytes = S * stage_bytes;
-  const int red_bytes = kGvConsumers * rmax * kMaxTok * 4;
-  const int ring_or_red = ring_bytes > red_bytes ? ring_bytes : red_bytes;
-  uint8_t *xsf_s = smem + ring_or_red;                  // MXFP8: [M][ksf] token scales
-  uint8_t *wsf_s = xsf_s + (WFMT == 1 ? kMaxTok * ksf : 0);  // MXFP8: [R][ksf] weight scales
-  uint64_t *full = reinterpret_cast<uint64_t *>(wsf_s + (WFMT == 1 ? ((rmax * ksf + 15) & ~15) : 0));
-  uint64_t *empty = full + S;
-  float *red = reinterpret_cast<float *>(smem);
+// 128B swizzle: 16-byte chunk c of row r of an 8-row, 1024-byte atom.
+__device__ __forceinline__ int swz(int r, int c) { return (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4); }
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kGvConsumers);
-    }
-    sm.nfin = 0;
+__device__ __forceinline__ void st_async_b32(uint32_t caddr, float v, uint32_t cbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(caddr),
+               "r"(__float_as_uint(v)), "r"(cbar)
+               : "memory");
+}
+
+template <int WFMT, int C>
+__global__ void __launch_bounds__(kGvThreads, 3) gemv_kernel(Params p, int kc, int use_pdl) {
+  constexpr int TS = (kMaxTok + C - 1) / C;
+  extern __shared__ uint8_t dsm_raw[];
+  uint8_t *dsm = dsm_raw + ((1024 - (smem_u32(dsm_raw) & 1023)) & 1023);
+  __shared__ GvStatic ss;
+  const GvLayout L = gv_layout(C, kc, WFMT);
+  uint8_t *w_s = dsm + L.w, *x_s = dsm + L.x, *sfa_s = dsm + L.sfa, *sfb_s = dsm + L.sfb;
+  float *recv = reinterpret_cast<float *>(dsm + L.recv);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int K = p.H, M = p.M, ksf = K >> 5;
+  const int ks = (int)cta_rank();  // this CTA's K range
+  const int h = blockIdx.x / C;
+  const int k0 = ks * kc, k1 = k0 + kc < K ? k0 + kc : K;
+  const int nch = k1 > k0 ? (k1 - k0) / kChunk : 0;
+  const uint8_t *wrow = p.w + (int64_t)h * kHeadDim * K + k0;  // row 0 of the head, this range
+
+  if (tid == 0) {
+    int ntok = 0;  // tokens rank + C * j < M finished here; 512 bytes from each CTA for each
+    for (int j = 0; j < TS; ++j) ntok += ks + C * j < M;
+    mbar_init(&ss.mma_bar, 1);
+    mbar_init(&ss.recv_bar, 1);
+    if (ntok) mbar_expect_tx(&ss.recv_bar, (uint32_t)(ntok * C * kHeadDim * 4));
+    else mbar_arrive(&ss.recv_bar);
+    ss.ok = 1;
     fence_mbar_init();
   }
-  // static per-layer data may be read before the wait on the previous kernel
-  for (int i = threadIdx.x; i < 4 * kHeadDim / 8; i += kGvThreads) {
-    const int r = i / (kHeadDim / 8), c = i % (kHeadDim / 8);
-    const __nv_bfloat16 *g = r == 0 ? p.g_q : r == 1 ? p.g_k : r == 2 ? p.g_iq : p.g_ik;
-    reinterpret_cast<uint4 *>(sm.gam[r])[c] = __ldg(reinterpret_cast<const uint4 *>(g) + c);
-  }
-  if (WFMT == 1) {  // this CTA's weight-row block scales, F8_128x4 -> [row][kb]
-    for (int i = threadIdx.x; i < R * (ksf >> 2); i += kGvThreads) {
-      const int row = i / (ksf >> 2), kq = i - row * (ksf >> 2);
-      *reinterpret_cast<uint32_t *>(wsf_s + row * ksf + 4 * kq) =
-          __ldg(reinterpret_cast<const uint32_t *>(p.wsf + sf128x4_offset(r0 + row, 4 * kq, ksf)));
+  if (warp == 4) tc_alloc(&ss.tmem, kTmemCols);
+  cluster_arrive_relaxed();  // matched by cluster_wait() before the first remote store
+
+  // ------------------------------- the weight stream (batch 0), before the wait
+  auto issue_weights = [&](int c0) {
+    const int n = nch - c0 < kStageChunks ? nch - c0 : kStageChunks;
+    for (int i = tid; i < n * kHeadDim * 8; i += kGvThreads) {
+      const int j = i / (kHeadDim * 8), rc = i - j * (kHeadDim * 8), r = rc >> 3, c = rc & 7;
+      cp_async16(w_s + j * kWChunkBytes + swz(r, c), wrow + (int64_t)r * K + (c0 + j) * kChunk + 16 * c);
     }
-  }
-  __syncthreads();
-  if (use_pdl) pdl_trigger();
-
-  float acc[kMaxMT][NT][4];
-#pragma unroll
-  for (int mt = 0; mt < kMaxMT; ++mt)
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
-
-  // weights (static) stream before the wait on the previous kernel
-  auto issue = [&](const int ch) {
-    const int s = ch % S;
-    const int kb0 = ch * chunk;
-    const int bytes = K - kb0 < chunk ? K - kb0 : chunk;
-    if (lane == 0) mbar_expect_tx(&full[s], (uint32_t)(bytes * R));
-    __syncwarp();
-    uint8_t *dst = smem + s * stage_bytes;
-    for (int r = lane; r < R; r += 32)
-      bulk_g2s(dst + r * pitch, p.w + (int64_t)(r0 + r) * K + kb0, (uint32_t)bytes, &full[s]);
+    if (WFMT == 1)
+      for (int i = tid; i < n * (kSfAtom / 16); i += kGvThreads) {
+        const int j = i / (kSfAtom / 16), c = i - j * (kSfAtom / 16);
+        cp_async16(sfa_s + j * kSfAtom + 16 * c,
+                   p.wsf + ((int64_t)h * (ksf >> 2) + (k0 / kChunk) + c0 + j) * kSfAtom + 16 * c);
+      }
+    cp_async_commit();
   };
-  const int first = S < nchunks ? S : nchunks;
-  if (warp == kGvConsumers)
-    for (int ch = 0; ch < first; ++ch) issue(ch);
-  if (use_pdl) pdl_wait();
-  if (FUSED) {
-    if (blockIdx.x < M) {  // this CTA normalises token row blockIdx.x
-      norm_quant_row<WFMT, kGvThreads, kFusedMaxChunks>(p, blockIdx.x, sm.red, sm.red2);
+  issue_weights(0);
+  const bool is_v = h >= p.v0 && h < p.iq0;
+  if (tid < 32) {
+    if (WFMT == 0)
+      reinterpret_cast<float4 *>(ss.wsc)[tid] = __ldg(reinterpret_cast<const float4 *>(p.w_scale + h * kHeadDim) + tid);
+  } else if (tid < 48) {
+    if (!is_v) {
+      const __nv_bfloat16 *gsrc = h < p.k0 ? p.g_q : h < p.v0 ? p.g_k : h < p.ik0 ? p.g_iq : p.g_ik;
+      reinterpret_cast<uint4 *>(ss.gam)[tid - 32] = __ldg(reinterpret_cast<const uint4 *>(gsrc) + (tid - 32));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ss.tmem;
+  if (use_pdl) {
+    pdl_trigger();
+    pdl_wait();
+  }
+  // ------------------------------------------ activations and per-token data
+  for (int i = tid; i < nch * 16 * 8; i += kGvThreads) {
+    const int j = i >> 7, rc = i & 127, r = rc >> 3, c = rc & 7;
+    uint8_t *dst = x_s + j * kXChunkBytes + swz(r, c);
+    if (r < M) cp_async16(dst, p.xq + (int64_t)r * K + k0 + j * kChunk + 16 * c);
+    else *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (WFMT == 1)
+    for (int i = tid; i < nch * (kSfAtom / 16); i += kGvThreads) {
+      const int j = i / (kSfAtom / 16), c = i - j * (kSfAtom / 16);
+      cp_async16(sfb_s + j * kSfAtom + 16 * c, p.xsf + ((int64_t)(k0 / kChunk) + j) * kSfAtom + 16 * c);
+    }
+  if (WFMT == 0 && tid < M) cp_async4(&ss.xs[tid], p.x_scale + tid);
+  // tokens finished here: ks + C * j, j < TS
+  const bool cs_lane = warp == 7 && lane < 8 * TS && ks + C * (lane >> 3) < M;
+  int64_t pos = 0;
+  if (cs_lane) pos = ld_i64(p.pos + ks + C * (lane >> 3));
+  if (warp == 7 && lane < TS && ks + C * lane < M) {
+    cp_async8(&ss.slot[lane], p.slot + ks + C * lane);
+    cp_async8(&ss.islot[lane], p.islot + ks + C * lane);
+  }
+  cp_async_commit();
+  if (cs_lane) {  // the cos / sin rows wait on the positions: their own group
+    if (pos < 0 || pos >= p.max_pos) {
+      set_status(p.status, kDevPosRange);
+      pos = pos < 0 ? 0 : p.max_pos - 1;
+    }
+    cp_async16(&ss.cs[lane >> 3][8 * (lane & 7)], p.cos_sin + pos * kRotDim + 8 * (lane & 7));
+  }
+  cp_async_commit();
+  cp_async_wait<1>();  // weights of batch 0 and the activations
+  fence_proxy_async_smem();
+  __syncthreads();
+
+  // ------------------------------------------------------------- the MMAs
+  for (int c0 = 0, bi = 0; c0 < nch; c0 += kStageChunks, ++bi) {
+    if (c0 > 0) {  // a longer K range: the next batch into the freed stages
+      issue_weights(c0);
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
       __syncthreads();
-      if (threadIdx.x == 0) {
-        __threadfence();
-        st_release(p.row_flag + blockIdx.x, 1);
-      }
     }
-  }
-  // per-step data the epilogue needs, staged while the weights stream
-  if (warp == 0 && lane < M) {
-    const int64_t pos = load_pos(p, lane);
-    sm.slot[lane] = ld_i64(p.slot + lane);
-    sm.islot[lane] = ld_i64(p.islot + lane);
-    const uint4 *src = reinterpret_cast<const uint4 *>(p.cos_sin + pos * kRotDim);
-#pragma unroll
-    for (int c = 0; c < kRotDim / 8; ++c) reinterpret_cast<uint4 *>(sm.cs[lane])[c] = __ldg(src + c);
-  }
-  if (FUSED) {  // every row's activations published
-    if (threadIdx.x < M) {
-      const int *f = p.row_flag + threadIdx.x;
-      if (ld_acquire(f) != 1) {
-        const uint64_t t0 = globaltimer();
-        while (ld_acquire(f) != 1) {
-          if (globaltimer() - t0 > 1000000000ull) {
-            set_status(p.status, kDevWaitTimeout);
-            break;
-          }
-          __nanosleep(64);
-        }
-      }
-    }
-    __syncthreads();
-  }
-  if (WFMT == 1) {  // the tokens' block scales, F8_128x4 -> [tok][kb]
-    for (int i = threadIdx.x; i < M * (ksf >> 2); i += kGvThreads) {
-      const int tok = i / (ksf >> 2), kq = i - tok * (ksf >> 2);
-      *reinterpret_cast<uint32_t *>(xsf_s + tok * ksf + 4 * kq) =
-          __ldcg(reinterpret_cast<const uint32_t *>(p.xsf + sf128x4_offset(tok, 4 * kq, ksf)));
-    }
-    __syncthreads();
-  }
-
-  if (warp == kGvConsumers) {
-    // ------------------------------------------------ producer warp: refills
-    for (int ch = first; ch < nchunks; ++ch) {
-      if (!mbar_wait(&empty[ch % S], ((ch / S) - 1) & 1, p.status)) break;
-      issue(ch);
-    }
-  } else {
-    // -------------------------------------------------------- consumer warps
-    const int g = lane >> 2, t = lane & 3;
-    // activation fragments of every slice of this warp: token nt*8+g, block b
-    // of the slice: bytes kw + 32b + 8t .. + 8
-    uint2 bpre[BREG ? kBRegSlices : 1][NT][2];
-    if (BREG) {
-#pragma unroll
-      for (int sl = 0; sl < kBRegSlices; ++sl) {
-        const int ch = sl / jw, i = sl - ch * jw;
-        const int kw = ch * chunk + warp * (chunk / kGvConsumers) + kSlice * i;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const int tok = nt * 8 + g;
-#pragma unroll
-          for (int b = 0; b < 2; ++b)
-            bpre[sl][nt][b] = (sl < nchunks * jw && kw < K && tok < M)
-                                  ? __ldcg(reinterpret_cast<const uint2 *>(p.xq + (int64_t)tok * K + kw + 32 * b + 8 * t))
-                                  : make_uint2(0u, 0u);
-        }
-      }
-    }
-    // one pass over this warp's slices; slice sl sits in chunk sl / jw
-    const int nsl = nchunks * jw;
-    bool alive = true;
-    auto slice = [&](const int sl, const uint2 (&bf)[NT][2]) {
-      const int ch = sl / jw, i = sl - ch * jw, s = ch % S;
-      if (i == 0 && alive) alive = mbar_wait(&full[s], (ch / S) & 1, p.status);
-      const int kw = ch * chunk + warp * (chunk / kGvConsumers) + kSlice * i;
-      if (alive && kw < K) {
-        float xs[NT][2][2];  // MXFP8: 2^e_x of tokens nt*8+2t(+1), block b
+    if (warp == 4 && lane == 0) {
+      tc_fence_after();
+      const int n = nch - c0 < kStageChunks ? nch - c0 : kStageChunks;
+      for (int j = 0; j < n; ++j) {
+        const uint64_t ad = sdesc_sw128(smem_u32(w_s + j * kWChunkBytes));
+        const uint64_t bd = sdesc_sw128(smem_u32(x_s + (c0 + j) * kXChunkBytes));
         if (WFMT == 1) {
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              int tk = nt * 8 + 2 * t + j;
-              tk = tk < M ? tk : M - 1;
-              const uint32_t w2 = *reinterpret_cast<const unsigned short *>(xsf_s + tk * ksf + (kw >> 5));
-              xs[nt][0][j] = e8m0_to_f32(w2 & 0xff);
-              xs[nt][1][j] = e8m0_to_f32(w2 >> 8);
-            }
+          tc_cp_sf(tmem + kSfaCol, sdesc_sf(smem_u32(sfa_s + j * kSfAtom)));
+          tc_cp_sf(tmem + kSfbCol, sdesc_sf(smem_u32(sfb_s + (c0 + j) * kSfAtom)));
         }
-        const uint8_t *st = smem + s * stage_bytes + (kw - ch * chunk) + 8 * t;
 #pragma unroll
-        for (int mt = 0; mt < kMaxMT; ++mt) {
-          if (mt < MT) {
-            const int ra = mt * 16 + g, rb = ra + 8;
-            uint2 alo[2], ahi[2];
-#pragma unroll
-            for (int b = 0; b < 2; ++b) {
-              alo[b] = ra < R ? *reinterpret_cast<const uint2 *>(st + ra * pitch + 32 * b) : make_uint2(0u, 0u);
-              ahi[b] = rb < R ? *reinterpret_cast<const uint2 *>(st + rb * pitch + 32 * b) : make_uint2(0u, 0u);
-            }
-            float ws[2][2];  // MXFP8: 2^e_w of rows ra, rb for block b
-            if (WFMT == 1) {
-              const int ca = ra < R ? ra : R - 1, cb = rb < R ? rb : R - 1;
-              const uint32_t wa = *reinterpret_cast<const unsigned short *>(wsf_s + ca * ksf + (kw >> 5));
-              const uint32_t wb = *reinterpret_cast<const unsigned short *>(wsf_s + cb * ksf + (kw >> 5));
-              ws[0][0] = e8m0_to_f32(wa & 0xff);
-              ws[1][0] = e8m0_to_f32(wa >> 8);
-              ws[0][1] = e8m0_to_f32(wb & 0xff);
-              ws[1][1] = e8m0_to_f32(wb >> 8);
-            }
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-              for (int b = 0; b < 2; ++b) {
-                if (WFMT == 0) {
-                  mma_e4m3_16832(acc[mt][nt], alo[b].x, ahi[b].x, alo[b].y, ahi[b].y, bf[nt][b].x, bf[nt][b].y);
-                } else {
-                  float c[4] = {0.f, 0.f, 0.f, 0.f};
-                  mma_e4m3_16832(c, alo[b].x, ahi[b].x, alo[b].y, ahi[b].y, bf[nt][b].x, bf[nt][b].y);
-                  acc[mt][nt][0] = fmaf(c[0], ws[b][0] * xs[nt][b][0], acc[mt][nt][0]);
-                  acc[mt][nt][1] = fmaf(c[1], ws[b][0] * xs[nt][b][1], acc[mt][nt][1]);
-                  acc[mt][nt][2] = fmaf(c[2], ws[b][1] * xs[nt][b][0], acc[mt][nt][2]);
-                  acc[mt][nt][3] = fmaf(c[3], ws[b][1] * xs[nt][b][1], acc[mt][nt][3]);
-                }
-              }
-          }
+        for (int k = 0; k < kChunk / 32; ++k) {
+          const uint32_t acc = (c0 + j) > 0 || k > 0;
+          // +32 bytes along K inside the swizzle atom: +2 in the 16-byte address field
+          if (WFMT == 0) mma_f8(tmem, ad + 2 * k, bd + 2 * k, kIdescF8, acc);
+          else mma_mx(tmem, ad + 2 * k, bd + 2 * k, kIdescMx | ((uint32_t)k << 4) | ((uint32_t)k << 29),
+                      tmem + kSfaCol, tmem + kSfbCol, acc);
         }
       }
-      if (i == jw - 1 || sl == nsl - 1) {  // the warp is done with this stage
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-      }
-    };
-    if (BREG) {
-#pragma unroll
-      for (int sl = 0; sl < kBRegSlices; ++sl)
-        if (sl < nsl) slice(sl, bpre[sl]);
-    } else {
-      for (int sl = 0; sl < nsl; ++sl) {
-        const int ch = sl / jw, i = sl - ch * jw;
-        const int kw = ch * chunk + warp * (chunk / kGvConsumers) + kSlice * i;
-        uint2 bf[NT][2];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const int tok = nt * 8 + g;
-#pragma unroll
-          for (int b = 0; b < 2; ++b)
-            bf[nt][b] = (tok < M && kw < K)
-                            ? __ldcg(reinterpret_cast<const uint2 *>(p.xq + (int64_t)tok * K + kw + 32 * b + 8 * t))
-                            : make_uint2(0u, 0u);
-        }
-        slice(sl, bf);
-      }
+      tc_commit(&ss.mma_bar);
     }
-  }
-  __syncthreads();  // every stage consumed: the ring is free for the reduction
-
-  // --------------------------------------------- cross-warp reduction -> y
-  if (warp < kGvConsumers) {
-    const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-    for (int mt = 0; mt < kMaxMT; ++mt)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int row = mt * 16 + g + 8 * (e >> 1), tok = nt * 8 + 2 * t + (e & 1);
-          if (mt < MT && row < R) red[(warp * rmax + row) * kMaxTok + tok] = acc[mt][nt][e];
-        }
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < R * M; i += kGvThreads) {
-    const int tok = i / R, row = i - tok * R;
-    float v = 0.f;
-#pragma unroll
-    for (int w = 0; w < kGvConsumers; ++w) v += red[(w * rmax + row) * kMaxTok + tok];
-    if (WFMT == 0) v = v * __ldcg(p.x_scale + tok) * __ldg(p.w_scale + r0 + row);
-    __stcg(p.y + (int64_t)tok * N + r0 + row, v);
-  }
-  __threadfence();  // release this thread's rows before the CTA's arrival is counted
-
-  // ------------------------------------- arrival; the last CTA of a head runs it
-  __syncthreads();
-  const int h0 = r0 >> 7, nh = ((r1 - 1) >> 7) - h0 + 1;
-  if (threadIdx.x < nh) {
-    const int h = h0 + threadIdx.x;
-    const int lo = r0 > (h << 7) ? r0 : (h << 7);
-    const int hi = r1 < ((h + 1) << 7) ? r1 : ((h + 1) << 7);
-    const int cnt = hi - lo;
-    const int old = atomicAdd(p.head_cnt + h, cnt);
-    if (old + cnt == kHeadDim) {
-      sm.fin[atomicAdd(&sm.nfin, 1)] = h;
-      p.head_cnt[h] = 0;  // every arrival of this launch is in: reset for the next
-      __threadfence();    // acquire the other CTAs' rows
-    }
-  }
-  __syncthreads();
-  const int nf = sm.nfin;
-  for (int f = 0; f < nf; ++f) {
-    const int h = sm.fin[f];
-    for (int m = warp; m < M; m += kGvConsumers + 1) {
-      HeadCtx hc;
-      hc.m = m;
-      hc.head = h;
-      hc.slot = sm.slot[m];
-      hc.islot = sm.islot[m];
-      hc.cs_row = sm.cs[m];
-      hc.g_q = sm.gam[0];
-      hc.g_k = sm.gam[1];
-      hc.g_iq = sm.gam[2];
-      hc.g_ik = sm.gam[3];
-      const float4 y4 = __ldcg(reinterpret_cast<const float4 *>(p.y + (int64_t)m * N + h * kHeadDim + 4 * lane));
-      float v[4] = {y4.x, y4.y, y4.z, y4.w};
-      head_epilogue<4>(p, hc, v, 4 * lane);
-    }
-  }
-  if (FUSED) {  // the last CTA out clears the row flags for the next launch
+    // every thread: the batch's MMAs are done (its stages may be refilled)
+    if (!mbar_wait(&ss.mma_bar, bi & 1, p.status)) ss.ok = 0;
     __syncthreads();
-    if (threadIdx.x == 0) {
-      __threadfence();
-      if (atomicAdd(p.done_cnt, 1) == G - 1) {
-        for (int m = 0; m < M; ++m) p.row_flag[m] = 0;
-        *p.done_cnt = 0;
-        __threadfence();
+    if (!ss.ok) break;
+  }
+  tc_fence_after();
+  // ---------------------------------- accumulator -> partial rows of the cluster
+  float v[16];
+  if (warp < 4) {
+    if (nch > 0 && ss.ok) {
+      tc_ld16(tmem + ((uint32_t)(warp * 32) << 16), v);
+      tc_wait_ld();
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = 0.f;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tc_dealloc(tmem, kTmemCols);
+  }
+  cluster_wait();  // every CTA of the cluster has initialised its barriers
+  if (warp < 4) {
+    const int r = warp * 32 + lane;  // weight row of the head
+#pragma unroll
+    for (int m = 0; m < kMaxTok; ++m) {
+      if (m < M) {
+        float *dst = recv + ((m / C) * C + ks) * kHeadDim + r;
+        st_async_b32(mapa(smem_u32(dst), m % C), v[m], mapa(smem_u32(&ss.recv_bar), m % C));
       }
     }
   }
-}
-
-struct GemvPlan {
-  int G, rmax, S, chunk, smem;
-  bool breg;
-};
-
-static GemvPlan plan_gemv(const Params &p, int num_sms) {
-  GemvPlan g;
-  int G = num_sms;
-  const int need = (p.N + kMaxRows - 1) / kMaxRows;
-  if (G < need) G = need;
-  if (G > p.N) G = p.N;
-  g.G = G;
-  g.rmax = (p.N + G - 1) / G;
-  // the largest stage (1536, 1024 or 512 K bytes a row) whose ring holds at
-  // least min(4, stages) stages in the budget
-  g.chunk = 512;
-  g.S = 1;
-  for (int j = 3; j >= 1; --j) {
-    const int chunk = 512 * j;
-    const int nchunks = (p.H + chunk - 1) / chunk;
-    int S = kRingBudget / (g.rmax * (chunk + 32));
-    if (S > nchunks) S = nchunks;
-    if (S >= (nchunks < 4 ? nchunks : 4) || j == 1) {
-      g.chunk = chunk;
-      g.S = S < 1 ? 1 : S;
-      break;
-    }
+  // ------------------------------------------- head epilogue of token m
+  if (warp >= TS) return;
+  const int m = ks + C * warp;
+  if (m >= M) return;
+  if (!mbar_wait_cluster(&ss.recv_bar, 0, p.status)) return;
+  const int d0 = 4 * lane;
+  float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int q = 0; q < C; ++q) {
+    const float4 u = *reinterpret_cast<const float4 *>(recv + (warp * C + q) * kHeadDim + d0);
+    y[0] += u.x;
+    y[1] += u.y;
+    y[2] += u.z;
+    y[3] += u.w;
   }
-  g.breg = p.H / 512 <= kBRegSlices;
-  const int ring = g.S * g.rmax * (g.chunk + 32), red = kGvConsumers * g.rmax * kMaxTok * 4;
-  const int ksf = p.H / 32;
-  const int scales = p.weight_fmt == 1 ? kMaxTok * ksf + ((g.rmax * ksf + 15) & ~15) : 0;
-  g.smem = (ring > red ? ring : red) + scales + 2 * g.S * 8;
-  return g;
+  if (WFMT == 0) {
+    const float xs = ss.xs[m];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) y[i] = y[i] * xs * ss.wsc[d0 + i];
+  }
+  HeadCtx hc;
+  hc.m = m;
+  hc.head = h;
+  hc.slot = ss.slot[warp];
+  hc.islot = ss.islot[warp];
+  hc.cs_row = ss.cs[warp];
+  hc.g_q = hc.g_k = hc.g_iq = hc.g_ik = ss.gam;
+  head_epilogue<4>(p, hc, y, d0);
 }
 
-template <int WFMT, int NT, bool BREG, bool FUSED>
-static cudaError_t launch_gemv_t(const Params &p, const GemvPlan &g, bool pdl, cudaStream_t stream) {
-  auto kern = gemv_kernel<WFMT, NT, BREG, FUSED>;
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), g.smem);
+namespace {
+
+int gv_kc(int H, int C) { return ((H + C - 1) / C + kChunk - 1) / kChunk * kChunk; }
+int gv_smem(int C, int kc, int mx) { return gv_layout(C, kc, mx).total + 1024; }  // + alignment slack
+
+// Cluster size usable on the current device: 16 where clusters of 16 CTAs
+// with `smem16` bytes of dynamic shared memory can be co-scheduled, else 8.
+// Queried once per (kernel, device) and again only for a larger
+// shared-memory size; the attributes it sets stay set.
+template <int WFMT>
+int pick_cluster(int smem16) {
+  struct Entry {
+    int c, smem;
+  };
+  static Entry cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
+  if (cached[dev].c && cached[dev].smem >= smem16) return cached[dev].c;
+  int c = 8;
+  const void *k16 = reinterpret_cast<const void *>(gemv_kernel<WFMT, 16>);
+  bool failed = cudaFuncSetAttribute(k16, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess;
+  if (!failed) failed = ensure_smem_attr(k16, smem16) != cudaSuccess;
+  if (!failed) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(16 * 64);
+    cfg.blockDim = dim3(kGvThreads);
+    cfg.dynamicSmemBytes = smem16;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 16;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    failed = cudaOccupancyMaxActiveClusters(&n, k16, &cfg) != cudaSuccess;
+    if (!failed && n >= 1) c = 16;
+  }
+  if (failed) cudaGetLastError();  // a refused attribute or query only means: clusters of 8
+  cached[dev] = Entry{c, smem16};
+  return c;
+}
+
+template <int WFMT, int C>
+cudaError_t launch_c(const Params &p, bool pdl, cudaStream_t stream) {
+  const int kc = gv_kc(p.H, C);
+  const int smem = gv_smem(C, kc, WFMT);
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemv_kernel<WFMT, C>), smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  cfg.gridDim = dim3(g.G);
+  cudaLaunchAttribute attr[2];
+  cfg.gridDim = dim3(p.n_heads * C);
   cfg.blockDim = dim3(kGvThreads);
-  cfg.dynamicSmemBytes = g.smem;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, p, g.G, g.rmax, g.S, g.chunk, (int)pdl);
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, gemv_kernel<WFMT, C>, p, kc, (int)pdl);
 }
 
-template <int WFMT, int NT>
-static cudaError_t launch_gemv_b(const Params &p, const GemvPlan &g, bool pdl, bool fused, cudaStream_t stream) {
-  if (fused)  // fused implies H <= 9216, so the activations fit in registers
-    return launch_gemv_t<WFMT, NT, true, true>(p, g, pdl, stream);
-  return g.breg ? launch_gemv_t<WFMT, NT, true, false>(p, g, pdl, stream)
-                : launch_gemv_t<WFMT, NT, false, false>(p, g, pdl, stream);
+template <int WFMT>
+cudaError_t launch_t(const Params &p, bool pdl, cudaStream_t stream) {
+  if (pick_cluster<WFMT>(gv_smem(16, gv_kc(p.H, 16), WFMT)) == 16) return launch_c<WFMT, 16>(p, pdl, stream);
+  return launch_c<WFMT, 8>(p, pdl, stream);
 }
 
-bool gemv_fuses_prologue(const Params &p) { return p.M <= kMaxTok && p.H <= kFusedMaxH && p.H <= 512 * kBRegSlices; }
+}  // namespace
 
-cudaError_t launch_gemv(const Params &p, int num_sms, bool pdl, bool fused, cudaStream_t stream) {
-  const GemvPlan g = plan_gemv(p, num_sms);
-  if (p.M <= 8)
-    return p.weight_fmt == 0 ? launch_gemv_b<0, 1>(p, g, pdl, fused, stream) : launch_gemv_b<1, 1>(p, g, pdl, fused, stream);
-  return p.weight_fmt == 0 ? launch_gemv_b<0, 2>(p, g, pdl, fused, stream) : launch_gemv_b<1, 2>(p, g, pdl, fused, stream);
+cudaError_t launch_gemv(const Params &p, bool pdl, cudaStream_t stream) {
+  return p.weight_fmt == 0 ? launch_t<0>(p, pdl, stream) : launch_t<1>(p, pdl, stream);
 }
 
 }  // namespace pa

@@ -33,11 +33,9 @@ cudaError_t launch_prologue(const Params &p, int grid, bool pdl, cudaStream_t st
 // Row-major [rows, ksf] E8M0 -> F8_128x4 layout.
 cudaError_t launch_pack_scales(const uint8_t *src, uint8_t *dst, int rows, int ksf, cudaStream_t stream);
 
-// Skinny-M path (M <= 16): weight-streaming FP8 GEMV with the per-head
-// epilogue run by the last CTA to finish each head; `fused` folds the
-// prologue into the same launch (when gemv_fuses_prologue(p)).
-bool gemv_fuses_prologue(const Params &p);
-cudaError_t launch_gemv(const Params &p, int num_sms, bool pdl, bool fused, cudaStream_t stream);
+// Skinny-M path (M <= 16): FP8 GEMV on one thread-block cluster per head,
+// the head epilogue fused behind the in-cluster reduction.
+cudaError_t launch_gemv(const Params &p, bool pdl, cudaStream_t stream);
 
 // Tensor-core path: persistent tcgen05 GEMM with the fused head epilogue,
 // on single CTAs (128 x 128 tiles) or on CTA pairs (cta_group::2, 256 x 256).

@@ -6,9 +6,8 @@
 // memory through its own pool and hands out none, or a process whose device
 // memory is capped so that any cudaMalloc after start-up fails.  This entry
 // point runs the same prologue and skinny-GEMV kernels as pre_attn_run, with
-// the kernels' scratch (status word, per-head arrival counters, the
-// quantised activations and the f32 projection rows) in a fixed array that
-// lives in this file.  It allocates nothing: no cudaMalloc, no cudaFree, no
+// the kernels' scratch (the status word and the quantised activations with
+// their scales) in a fixed array that lives in this file.  It allocates nothing: no cudaMalloc, no cudaFree, no
 // allocating library call.
 #include <cstdint>
 #include <mutex>
@@ -60,8 +59,7 @@ int pre_attn_run_noalloc(pa_handle *h, int M, const pa_step_inputs *in, const pa
   const int st = scratch_for_current_device(&scratch);
   if (st != PA_OK) return st;
   // Every call reuses the array and finds the previous call's contents; the
-  // status word and the per-head arrival counters must start at zero, so the
-  // part this call uses is cleared first.
+  // part this call uses is cleared first (the status word must start at zero).
   if (cudaMemsetAsync(scratch, 0, need, (cudaStream_t)stream) != cudaSuccess) return PA_ERR_CUDA;
   return pre_attn_run(h, M, in, wt, caches, out, scratch, kScratchBytes, stream);
 }

@@ -1,5 +1,4 @@
-// Row normalisation of the pre-attention step, shared by the prologue kernel
-// and the fused skinny-M kernel:
+// Row normalisation of the pre-attention step (the prologue kernel):
 //   acc = ar + res (f32), residual = bf16(acc)
 //   n = acc * rsqrt(mean(acc^2) + eps) * (1 + g_in)            (Gemma RMSNorm)
 //   per-channel format: s = amax(n) / 448 (1 if 0), xq = e4m3(n / s), a true
@@ -42,13 +41,16 @@ __device__ __forceinline__ void dd_add(float &hi, float &lo, float x, float xl) 
 }
 // rstd = 1 / sqrt(sum / H + eps) from the block's (hi, lo) partial sums, as
 // an unevaluated f32 pair rh + rl accurate to about 2^-44 relative (no FP64:
-// it is slow on this part).  sum / H and + eps are carried as double-floats;
-// rsqrtf gives r0, and one Newton step with its second-order term,
-// r = r0 (1 - t/2 + 3t^2/8) with t = x r0^2 - 1 evaluated with FMAs, gives
-// the rest.  Every thread ends with the same pair.
+// it is slow on this part).  The warps' partials are combined by every warp
+// with the same shuffle tree (no second barrier, no serial loop over the
+// warps).  sum / H and + eps are carried as double-floats; rsqrtf gives r0,
+// and one Newton step with its second-order term, r = r0 (1 - t/2 + 3t^2/8)
+// with t = x r0^2 - 1 evaluated with FMAs, gives the rest.  Every thread ends
+// with the same pair.
 template <int NTHR>
 __device__ __forceinline__ void block_rstd_dd(float hi, float lo, float2 *red, int H, float eps, float &rh,
                                               float &rl) {
+  static_assert(NTHR / 32 <= 32 && (NTHR & (NTHR - 1)) == 0, "one warp combines the warps' partials");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -57,9 +59,18 @@ __device__ __forceinline__ void block_rstd_dd(float hi, float lo, float2 *red, i
   }
   if (lane == 0) red[warp] = make_float2(hi, lo);
   __syncthreads();
-  float sh = red[0].x, sl = red[0].y;
+  constexpr int W = NTHR / 32;
+  float2 w = lane < W ? red[lane] : make_float2(0.f, 0.f);
+  float sh = w.x, sl = w.y;
 #pragma unroll
-  for (int w = 1; w < NTHR / 32; ++w) dd_add(sh, sl, red[w].x, red[w].y);
+  for (int o = 16; o > 0; o >>= 1) {
+    if (o < W) {
+      const float oh = __shfl_xor_sync(0xffffffffu, sh, o), ol = __shfl_xor_sync(0xffffffffu, sl, o);
+      dd_add(sh, sl, oh, ol);
+    }
+  }
+  sh = __shfl_sync(0xffffffffu, sh, 0);  // lanes >= W summed only zeros
+  sl = __shfl_sync(0xffffffffu, sl, 0);
   // x = sum / H + eps
   const float fh = (float)H;
   const float qh = __fdiv_rn(sh, fh);
@@ -100,10 +111,12 @@ __device__ __forceinline__ float block_max(float v, float *red) {
   __syncthreads();  // red may still be read by a previous reduction
   if (lane == 0) red[warp] = v;
   __syncthreads();
-  float r = red[0];
+  constexpr int W = NTHR / 32;
+  float r = lane < W ? red[lane] : 0.f;
 #pragma unroll
-  for (int w = 1; w < NTHR / 32; ++w) r = fmaxf(r, red[w]);
-  return r;
+  for (int o = 16; o > 0; o >>= 1)
+    if (o < W) r = fmaxf(r, __shfl_xor_sync(0xffffffffu, r, o));
+  return __shfl_sync(0xffffffffu, r, 0);  // lanes >= W saw only zeros
 }
 
 // Normalise and quantise token row m with the NTHR threads of the block

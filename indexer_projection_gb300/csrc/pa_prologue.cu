@@ -9,15 +9,16 @@
 
 namespace pa {
 
-constexpr int kProThreads = 256;
-
-// MAXC chunks of 8 elements per thread: H <= 2048 * MAXC.  The row stays in
-// registers, so MAXC is sized to H: fewer registers, more CTAs (and loads in
-// flight) per SM.
-template <int WFMT, int MAXC>
-__global__ void __launch_bounds__(kProThreads) prologue_kernel(Params p, int use_pdl) {
-  __shared__ float red[kProThreads / 32];
-  __shared__ float2 red2[kProThreads / 32];
+// NTHR threads a row, MAXC chunks of 8 elements per thread: H <= 8 * NTHR *
+// MAXC.  The row stays in registers, so MAXC is sized to H.  Many rows (the
+// tensor-core path): 256 threads a row, more rows resident per SM.  A few
+// rows (the skinny path, which waits on this kernel): 1024 threads a row, so
+// the per-element work of the correctly rounded norm is spread 4x wider and
+// the row is done sooner.
+template <int WFMT, int NTHR, int MAXC>
+__global__ void __launch_bounds__(NTHR) prologue_kernel(Params p, int use_pdl) {
+  __shared__ float red[NTHR / 32];
+  __shared__ float2 red2[NTHR / 32];
   if (use_pdl) {
     pdl_trigger();
     pdl_wait();
@@ -26,10 +27,10 @@ __global__ void __launch_bounds__(kProThreads) prologue_kernel(Params p, int use
   const int ksf = p.H >> 5;
   if (m >= p.M) {  // MXFP8 padding rows of the tensor-core path: scale 1, codes unused
     if (WFMT == 1)
-      for (int kb = threadIdx.x; kb < ksf; kb += kProThreads) p.xsf[sf128x4_offset(m, kb, ksf)] = 127;
+      for (int kb = threadIdx.x; kb < ksf; kb += NTHR) p.xsf[sf128x4_offset(m, kb, ksf)] = 127;
     return;
   }
-  norm_quant_row<WFMT, kProThreads, MAXC>(p, m, red, red2);
+  norm_quant_row<WFMT, NTHR, MAXC>(p, m, red, red2);
 }
 
 __global__ void pack_scales_kernel(const uint8_t *src, uint8_t *dst, int rows, int ksf) {
@@ -43,23 +44,38 @@ __global__ void pack_scales_kernel(const uint8_t *src, uint8_t *dst, int rows, i
   }
 }
 
+namespace {
+// H <= 16384: 1024 threads need at most 2 chunks, 256 threads at most 8
+cudaError_t launch_1024(const Params &p, cudaLaunchConfig_t &cfg, bool pdl) {
+  cfg.blockDim = dim3(1024);
+  const bool mx = p.weight_fmt == 1;
+  if (mx) return cudaLaunchKernelEx(&cfg, prologue_kernel<1, 1024, 2>, p, (int)pdl);  // (one chunk spills)
+  if (p.H <= 8 * 1024) return cudaLaunchKernelEx(&cfg, prologue_kernel<0, 1024, 1>, p, (int)pdl);
+  return cudaLaunchKernelEx(&cfg, prologue_kernel<0, 1024, 2>, p, (int)pdl);
+}
+cudaError_t launch_256(const Params &p, cudaLaunchConfig_t &cfg, bool pdl) {
+  cfg.blockDim = dim3(256);
+  const int maxc = (p.H + 8 * 256 - 1) / (8 * 256);
+  const bool mx = p.weight_fmt == 1;
+  if (maxc <= 2) return cudaLaunchKernelEx(&cfg, mx ? prologue_kernel<1, 256, 2> : prologue_kernel<0, 256, 2>, p, (int)pdl);
+  if (maxc <= 3) return cudaLaunchKernelEx(&cfg, mx ? prologue_kernel<1, 256, 3> : prologue_kernel<0, 256, 3>, p, (int)pdl);
+  if (maxc <= 4) return cudaLaunchKernelEx(&cfg, mx ? prologue_kernel<1, 256, 4> : prologue_kernel<0, 256, 4>, p, (int)pdl);
+  return cudaLaunchKernelEx(&cfg, mx ? prologue_kernel<1, 256, 8> : prologue_kernel<0, 256, 8>, p, (int)pdl);
+}
+}  // namespace
+
 cudaError_t launch_prologue(const Params &p, int grid, bool pdl, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kProThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  const int maxc = (p.H + 8 * kProThreads - 1) / (8 * kProThreads);
-  const bool mx = p.weight_fmt == 1;
-  if (maxc <= 2) return cudaLaunchKernelEx(&cfg, mx ? prologue_kernel<1, 2> : prologue_kernel<0, 2>, p, (int)pdl);
-  if (maxc <= 3) return cudaLaunchKernelEx(&cfg, mx ? prologue_kernel<1, 3> : prologue_kernel<0, 3>, p, (int)pdl);
-  if (maxc <= 4) return cudaLaunchKernelEx(&cfg, mx ? prologue_kernel<1, 4> : prologue_kernel<0, 4>, p, (int)pdl);
-  return cudaLaunchKernelEx(&cfg, mx ? prologue_kernel<1, 8> : prologue_kernel<0, 8>, p, (int)pdl);
+  // fewer rows than a fraction of the SMs: the row latency is the step's
+  return grid <= 64 ? launch_1024(p, cfg, pdl) : launch_256(p, cfg, pdl);
 }
 
 cudaError_t launch_pack_scales(const uint8_t *src, uint8_t *dst, int rows, int ksf, cudaStream_t stream) {

@@ -72,6 +72,28 @@ def test_init_shapes_and_workspace(B):
     assert B.pre_attn_packed_scale_bytes(0, 512) == 0
 
 
+def test_path_query_rejects_before_touching_the_device(B):
+    L = B.load()
+    assert L.pre_attn_path(None, 8) == -B.PA_ERR_NULL
+    h = B.pre_attn_init(_cfg(B, hidden=6144, n_kv_heads=1, max_tokens=64))
+    assert L.pre_attn_path(h, 0) == -B.PA_ERR_SHAPE
+    assert L.pre_attn_path(h, 65) == -B.PA_ERR_SHAPE
+    B.pre_attn_destroy(h)
+    h = B.pre_attn_init(_cfg(B, hidden=6144, n_kv_heads=1, max_tokens=64, flags=B.PA_FLAG_FORCE_GEMV))
+    assert L.pre_attn_path(h, 17) == -B.PA_ERR_SHAPE  # the skinny path stops at 16 rows
+    B.pre_attn_destroy(h)
+
+
+def test_workspace_sizes(B):
+    # status word + quantised activations and their scales, nothing per N
+    h = B.pre_attn_init(_cfg(B, hidden=6144, n_kv_heads=1, max_tokens=64))
+    assert 8 * 6144 < B.pre_attn_workspace_bytes(h, 8) < 8 * 6144 + 8192
+    B.pre_attn_destroy(h)
+    h = B.pre_attn_init(_cfg(B, hidden=6144, n_kv_heads=4, max_tokens=64, weight_format=1))
+    assert B.pre_attn_workspace_bytes(h, 8) < 8 * 6144 + 128 * 192 + 8192  # MXFP8: 128 scale rows
+    B.pre_attn_destroy(h)
+
+
 def _run_args(B, M=4, **over):
     """Fake but aligned device addresses: validation fails before any use."""
     base = 1 << 32

@@ -91,3 +91,20 @@ def test_prefill_config(tiles):
 @pytest.mark.parametrize("M", [64, 256, 1024, 4096, 16384])
 def test_sweep_config_tensor_core_points(M):
     check(workloads.sweep(M), flags=0, nsample=24)
+
+
+def test_path_choice():
+    from indexer_projection_gb300 import binding as B
+    from indexer_projection_gb300.runner import PreAttn
+
+    def path(M, flags=0, nkv=4):
+        r = PreAttn(6144, nkv, weight_format=B.PA_WEIGHT_MXFP8, cache_format=B.PA_CACHE_FP8, max_tokens=16384,
+                    flags=flags)
+        return B.pre_attn_path(r.handle, M)
+
+    assert path(8) == B.PA_PATH_GEMV and path(16) == B.PA_PATH_GEMV
+    assert path(8, B.PA_FLAG_FORCE_GEMM) != B.PA_PATH_GEMV
+    assert path(8192) == B.PA_PATH_GEMM_PAIR  # 1312 pair tiles vs 5184 single tiles
+    assert path(8192, B.PA_FLAG_GEMM_SINGLE) == B.PA_PATH_GEMM_SINGLE
+    assert path(64, B.PA_FLAG_GEMM_PAIR) == B.PA_PATH_GEMM_PAIR
+    assert path(17) in (B.PA_PATH_GEMM_SINGLE, B.PA_PATH_GEMM_PAIR)

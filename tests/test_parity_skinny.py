@@ -109,3 +109,14 @@ def test_out_of_range_slots_and_positions_are_flagged_not_written():
 @pytest.mark.parametrize("M", [1, 2, 4, 8, 16])
 def test_sweep_config_skinny_points(M):
     check(workloads.sweep(M), flags=0)
+
+
+@pytest.mark.parametrize("H", [128, 2048, 2176, 4352, 16384])
+@pytest.mark.parametrize("fmt", ["ptpc", "mx"])
+def test_k_ranges(H, fmt):
+    # each head's cluster splits K into 8 ranges of ceil(H / 8) rounded up to
+    # 64 bytes: empty ranges (H = 128), a ragged last range (2176, 4352) and
+    # ranges longer than the registers hold (16384: the units are refilled)
+    check(workloads.Workload(f"ks{H}", H=H, nkv=1, M=11 if fmt == "mx" else 5, weight_fmt=fmt, cache_fmt="fp8",
+                             seed=H + (fmt == "mx"), positions="uniform", max_pos=500, pool_pages16=64,
+                             q_fp8=True, iq_fp8=True))

@@ -46,7 +46,7 @@ def test_noalloc_matches_pre_attn_run_on_two_calls_in_a_row():
         harness.compare(wl, got, reference, range(wl.M), where=" noalloc vs pre_attn_run")
 
 
-def test_noalloc_rejects_sizes_beyond_its_scratch():
+def test_noalloc_rejects_rows_it_cannot_take():
     from indexer_projection_gb300 import binding as B
     from indexer_projection_gb300.runner import PreAttn
 
@@ -58,9 +58,12 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     # M beyond the 16 rows of the skinny path
     assert B.pre_attn_run_noalloc(g.runner.handle, 17, ins, g.weights, g.caches, g.outputs, check=False) \
         == B.PA_ERR_SHAPE
-    # a shape whose scratch need exceeds 2 MiB (H = 16384, 16 rows, 264 heads)
-    big = PreAttn(16384, 4, weight_format=B.PA_WEIGHT_FP8_PER_CHANNEL, cache_format=B.PA_CACHE_FP8,
-                  max_tokens=16, n_q_heads=250, n_iq_heads=5)
-    assert B.pre_attn_workspace_bytes(big.handle, 16) > (2 << 20)
-    assert B.pre_attn_run_noalloc(big.handle, 16, ins, g.weights, g.caches, g.outputs, check=False) \
+    # beyond the handle's max_tokens
+    small = PreAttn(512, 1, weight_format=B.PA_WEIGHT_FP8_PER_CHANNEL, cache_format=B.PA_CACHE_FP8, max_tokens=4)
+    assert B.pre_attn_run_noalloc(small.handle, 5, ins, g.weights, g.caches, g.outputs, check=False) \
         == B.PA_ERR_SHAPE
+    # the largest skinny request the handles accept (H = 16384, MXFP8, 16 rows)
+    # needs well under the 2 MiB: the scratch holds only the activations
+    big = PreAttn(16384, 4, weight_format=B.PA_WEIGHT_MXFP8, cache_format=B.PA_CACHE_FP8,
+                  max_tokens=16, n_q_heads=250, n_iq_heads=5)
+    assert 0 < B.pre_attn_workspace_bytes(big.handle, 16) <= (2 << 20)
