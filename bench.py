@@ -81,7 +81,7 @@ def step_flops(wl) -> int:
     return 2 * wl.M * wl.N * wl.H
 
 
-KERNEL_SOURCES = {"gemv": ("pa_gemv.cu", "pa_device.cuh"), "gemm": ("pa_gemm.cu", "pa_device.cuh"),
+KERNEL_SOURCES = {"gemv": ("pa_gemv.cu", "pa_device.cuh"), "gemv_fused": ("pa_gemv.cu", "pa_norm.cuh", "pa_device.cuh"), "gemm": ("pa_gemm.cu", "pa_device.cuh"),
                   "gemm2": ("pa_gemm2.cu", "pa_device.cuh"),
                   "prologue": ("pa_prologue.cu", "pa_device.cuh")}
 
@@ -273,6 +273,8 @@ def run_ours(args, wl, rank, world, local_rank):
     per_copy = step_bytes(wl)["weights"] + 2 * wl.M * wl.H * 2
     copies = max(2, min(64, math.ceil(2.5 * l2 / per_copy)))
     flags = {"auto": 0, "single": B.PA_FLAG_GEMM_SINGLE, "pair": B.PA_FLAG_GEMM_PAIR}[args.gemm]
+    if args.fuse:
+        flags |= B.PA_FLAG_FUSE
     dw = DeviceWorkload(wl, st, copies, dev, flags=flags)
     stream = torch.cuda.Stream(dev)
     K, W = args.steps, args.warmup
@@ -409,11 +411,14 @@ def run_ours(args, wl, rank, world, local_rank):
     tokens_s = world * wl.M / (ms_step * 1e-3)
     nb = step_bytes(wl)
     path = B.pre_attn_path(dw.runner.handle, wl.M)
-    gemm = path != B.PA_PATH_GEMV
-    kname = {B.PA_PATH_GEMV: "gemv", B.PA_PATH_GEMM_SINGLE: "gemm", B.PA_PATH_GEMM_PAIR: "gemm2"}[path]
-    kdesc = {"gemv": "pa::gemv_kernel (FP8 GEMV, one cluster per head)",
+    gemm = path in (B.PA_PATH_GEMM_SINGLE, B.PA_PATH_GEMM_PAIR)
+    kname = {B.PA_PATH_GEMV: "gemv", B.PA_PATH_GEMV_FUSED: "gemv_fused", B.PA_PATH_GEMM_SINGLE: "gemm",
+             B.PA_PATH_GEMM_PAIR: "gemm2"}[path]
+    kdesc = {"gemv": "pa::gemv_kernel<.., false> (tcgen05 GEMV, one cluster per head, after the prologue)",
+             "gemv_fused": "pa::gemv_kernel<.., true> (prologue + tcgen05 GEMV in one kernel, one cluster per head)",
              "gemm": "pa::gemm_kernel (tcgen05, 128x128 tiles)",
              "gemm2": "pa::g2::gemm2_kernel (tcgen05 cta_group::2, 256x256 tiles)"}[kname]
+    launches_per_step = 1 if path == B.PA_PATH_GEMV_FUSED else 2
     if gemm:
         achieved = step_flops(wl) / (main_ms * 1e-3) / 1e12
         peak = peaks["bf16_tflops"] * FP8_OVER_BF16
@@ -440,7 +445,7 @@ def run_ours(args, wl, rank, world, local_rank):
                    "timing": "CUDA graph of K steps, PDL chained", "parallelism": f"replicas x{world}"},
         "roofline": roof,
         "step_hbm_frac": round(step_roof, 4),
-        "gpu_launches": 2 * K,
+        "gpu_launches": launches_per_step * K,
         "e2e": {"value": round(world * wl.M / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E,
                 "how": "pinned host inputs -> device, pre_attn_run, outputs -> pinned host, every step; "
@@ -515,6 +520,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--gemm", default="auto", choices=["auto", "single", "pair"],
                     help="tensor-core path tiling (auto: chosen per shape)")
+    ap.add_argument("--fuse", action="store_true",
+                    help="skinny path in one kernel (row normalisation inside the GEMV) where the shape allows")
     args = ap.parse_args()
     wl = get_workload(args.workload)
     rank = int(os.environ.get("RANK", 0))

@@ -106,7 +106,10 @@ enum pa_flags {
   PA_FLAG_FORCE_GEMM = 1 << 2,      /* testing: the tensor-core GEMM path for any M */
   PA_FLAG_NO_PDL = 1 << 3,          /* launch without programmatic dependent launch */
   PA_FLAG_GEMM_SINGLE = 1 << 4,     /* testing: tensor-core path on single CTAs (128 x 128 tiles) */
-  PA_FLAG_GEMM_PAIR = 1 << 5        /* testing: tensor-core path on CTA pairs (256 x 256 tiles) */
+  PA_FLAG_GEMM_PAIR = 1 << 5,       /* testing: tensor-core path on CTA pairs (256 x 256 tiles) */
+  PA_FLAG_FUSE = 1 << 6             /* skinny path in one kernel (the row normalisation inside the
+                                       GEMV's clusters) where the shape allows; measured slower than
+                                       prologue + GEMV at the decode shape, so not the default */
 };
 
 /* ----------------------------------------------------------- config */
@@ -270,9 +273,10 @@ int pre_attn_run_noalloc(pa_handle *h, int M, const pa_step_inputs *in, const pa
 
 /* Main kernels a call can run (pre_attn_path). */
 enum {
-  PA_PATH_GEMV = 0,         /* skinny path: FP8 GEMV on one cluster per head (M <= 16) */
+  PA_PATH_GEMV = 0,         /* skinny path: prologue, then the FP8 GEMV on one cluster per head */
   PA_PATH_GEMM_SINGLE = 1,  /* tensor-core path, 128 x 128 tiles on single SMs */
-  PA_PATH_GEMM_PAIR = 2     /* tensor-core path, 256 x 256 tiles on SM pairs */
+  PA_PATH_GEMM_PAIR = 2,    /* tensor-core path, 256 x 256 tiles on SM pairs */
+  PA_PATH_GEMV_FUSED = 3    /* skinny path in one kernel (PA_FLAG_FUSE) */
 };
 
 /* Which main kernel pre_attn_run(h, M, ...) launches on the current device

@@ -76,12 +76,15 @@ bool uses_gemv(const pa_config &c, int M) {
   return (c.flags & PA_FLAG_FORCE_GEMV) ? true : (c.flags & PA_FLAG_FORCE_GEMM) ? false : M <= 16;
 }
 
-// Main kernel for M rows (h->num_sms known).  256 x 256 pair tiles cost
+// Main kernel for M rows (h->num_sms known; the skinny path's fusion
+// check queries the device once).  256 x 256 pair tiles cost
 // about 1.5x a 128 x 128 tile on one SM: the pairs are used unless wave
 // quantisation favours the finer tiles.
 int choose_path(const pa_handle *h, int M) {
   const pa_config &c = h->cfg;
-  if (uses_gemv(c, M)) return PA_PATH_GEMV;
+  if (uses_gemv(c, M))
+    return (c.flags & PA_FLAG_FUSE) && pa::gemv_fuses_prologue(c.hidden, c.weight_format) ? PA_PATH_GEMV_FUSED
+                                                                                         : PA_PATH_GEMV;
   if (c.flags & PA_FLAG_GEMM_SINGLE) return PA_PATH_GEMM_SINGLE;
   if (c.flags & PA_FLAG_GEMM_PAIR) return PA_PATH_GEMM_PAIR;
   const int sms = h->num_sms > 1 ? h->num_sms : 2;
@@ -334,12 +337,16 @@ int pre_attn_run(pa_handle *h, int M, const pa_step_inputs *in, const pa_weights
 
   const bool pdl = !(c.flags & PA_FLAG_NO_PDL);
   cudaStream_t s = (cudaStream_t)stream;
-  const int pro_grid = (!gemv && c.weight_format == PA_WEIGHT_MXFP8) ? L.m_pad : M;
-  e = pa::launch_prologue(p, pro_grid, pdl, s);
-  if (e != cudaSuccess) return cuda_fail(e);
+  // the skinny path normalises the rows inside its own launch when it can
+  const bool fused = path == PA_PATH_GEMV_FUSED;
+  if (!fused) {
+    const int pro_grid = (!gemv && c.weight_format == PA_WEIGHT_MXFP8) ? L.m_pad : M;
+    e = pa::launch_prologue(p, pro_grid, pdl, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
   if (h->prof_before && (e = cudaEventRecord(h->prof_before, s)) != cudaSuccess) return cuda_fail(e);
   if (gemv) {
-    e = pa::launch_gemv(p, pdl, s);
+    e = pa::launch_gemv(p, fused, pdl, s);
   } else {
     e = path == PA_PATH_GEMM_PAIR ? pa::launch_gemm_pair(p, h->num_sms, c.gemm_grid, pdl, s)
                                   : pa::launch_gemm(p, h->num_sms, c.gemm_grid, pdl, s);

@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], kBM);
+      mbar_init(&tempty[b], kBM / 32);  // one arrival per epilogue warp
     }
     fence_mbar_init();
   }
@@ -225,7 +225,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       tc_wait_ld();
       tc_fence_before();
-      mbar_arrive(&tempty[abuf]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[abuf]);
       if (++abuf == 2) {
         abuf = 0;
         aphase ^= 1;

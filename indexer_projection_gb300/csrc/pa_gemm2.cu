@@ -19,7 +19,8 @@
 //             the F8_128x4 atoms (512 B) by TMA, SFA for the CTA's own rows,
 //             SFB for both halves of N (each CTA needs all 256 columns'
 //             scales; no multicast).  Every load of both CTAs completes on
-//             CTA 0's stage barrier (TMA .cta_group::2).
+//             CTA 0's stage barrier (TMA .cta_group::2), which CTA 0 alone
+//             arms with both CTAs' byte count.
 //   odd head count: the last N tile's second head is zero-filled by TMA and
 //             never stored.
 // Every mbarrier wait is bounded (about a second); a timeout raises
@@ -57,10 +58,6 @@ struct Smem {  // offsets from the 1024-aligned base
 constexpr int kSmemBytes = Smem::total + 1024;
 
 // ------------------------------------------------------------- cluster PTX
-__device__ __forceinline__ void expect_tx_remote(uint32_t caddr, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(caddr), "r"(bytes)
-               : "memory");
-}
 // 2-D TMA load into this CTA's shared memory, completing on a barrier that
 // may sit in the peer CTA (cta_group::2).
 __device__ __forceinline__ void tma_2d_pair(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t cbar) {
@@ -151,11 +148,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 2);   // one expect_tx arrival per CTA of the pair
+      mbar_init(&full[s], 1);   // CTA 0's expect_tx arrival, for both CTAs' bytes
       mbar_init(&empty[s], 1);  // the MMA's commit
     }
     mbar_init(tfull, 1);
-    mbar_init(tempty, 2 * kEpiThreads);
+    mbar_init(tempty, 4);  // one arrival per epilogue warpgroup of each CTA
     fence_mbar_init();
   }
   if (warp == 8 && lane == 0) {
@@ -196,7 +193,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t fb = full0 + stage * 8;
-          expect_tx_remote(fb, tx);
+          // CTA 0 expects both CTAs' bytes on its own barrier (a local
+          // arrival); CTA 1's loads just complete their bytes there.  A
+          // remote arrival per stage would put a cluster-scope release on
+          // CTA 1's load path every k-step.
+          if (rank == 0) mbar_expect_tx(&full[stage], 2 * tx);
           tma_2d_pair(smem_u32(smem + Smem::a + stage * kTile), &tmA, ks * kBK, m_tile * kBM, fb);
           tma_2d_pair(smem_u32(smem + Smem::b + stage * kTile), &tmB, ks * kBK, nt * kBN + (int)rank * 128, fb);
           if (WFMT == 1) {
@@ -283,7 +284,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       tc_wait_ld();
       tc_fence_before();
-      arrive_remote(tempty0);  // the accumulator is in registers: CTA 0 may overwrite it
+      // the warpgroup's accumulator columns are in registers: one arrival
+      // tells CTA 0's MMA issuer it may overwrite them (one remote arrival per
+      // thread would serialise hundreds of them on one barrier)
+      named_bar_sync(2 + wg, 128);
+      if ((warp & 3) == 0 && lane == 0) arrive_remote(tempty0);
       aphase ^= 1;
       const int m = (2 * mp + (int)rank) * kBM + row;
       if (m >= M || head >= p.n_heads) continue;

@@ -35,6 +35,18 @@
 // as the pre_attn page's head tasks.  Nothing goes through global memory
 // between the MMAs and the outputs.
 //
+// Fused variant (clusters of 16, K <= 16 x 384): the kernel also does the
+// prologue's work, so the decode step is one launch.  The 16 threads of
+// token group m of every CTA add ar + res over the CTA's K range (the
+// residual is written by head 0's cluster), reduce sum(acc^2) as a
+// double-float and exchange the 16 K-range partials across the cluster
+// (st.async, byte-counted); every CTA then sums them in the same order, so
+// all agree bit for bit on rstd.  The correctly rounded n (pa_norm.cuh) and,
+// for the per-channel format, a second exchange of the K-range amax give the
+// FP8 codes, written straight into the MMA's B operand (and the MXFP8 scale
+// atoms into their tcgen05.cp source): nothing goes through global memory
+// between the inputs and the outputs.
+//
 // The weight, its scales, the head's gamma and w_scale are read before the
 // wait on the previous kernel: they must not be written by work still in
 // flight on the stream (they are model constants).  Everything else is read
@@ -42,6 +54,7 @@
 // PA_DEV_WAIT_TIMEOUT), and the tensor memory is freed on every path.
 #include "pa_device.cuh"
 #include "pa_launch.h"
+#include "pa_norm.cuh"
 #include "pa_tc.cuh"
 
 namespace pa {
@@ -57,6 +70,7 @@ constexpr int kTmemCols = 32;      // accumulator 16 columns, scale factors at 1
 constexpr int kSfaCol = 16, kSfbCol = 20;
 constexpr uint32_t kIdescF8 = idesc_f8(128, 16);
 constexpr uint32_t kIdescMx = idesc_mx(128, 16);
+constexpr int kFusedMaxKc = 384;   // fused variant: 3 chunks of 8 elements a thread
 
 // Byte offsets of the dynamic shared memory from its 1024-aligned base.
 struct GvLayout {
@@ -65,6 +79,9 @@ struct GvLayout {
   int sfa;   // MXFP8 [kStageChunks] weight scale atoms
   int sfb;   // MXFP8 [nchunks] activation scale atoms
   int recv;  // [TS][C][128] f32 partial rows received from the cluster
+  int ex1;   // fused: [16 K ranges][16 tokens] float2 sum(acc^2) partials
+  int ex2;   // fused: [16 K ranges][16 tokens] f32 amax partials
+  int gin;   // fused: the K range's input-norm gamma (bf16)
   int total;
 };
 __host__ __device__ inline GvLayout gv_layout(int C, int kc, int mx) {
@@ -76,7 +93,10 @@ __host__ __device__ inline GvLayout gv_layout(int C, int kc, int mx) {
   L.sfa = L.x + nch * kXChunkBytes;
   L.sfb = L.sfa + (mx ? kStageChunks * kSfAtom : 0);
   L.recv = L.sfb + (mx ? nch * kSfAtom : 0);
-  L.total = L.recv + ts * C * kHeadDim * 4;
+  L.ex1 = L.recv + ts * C * kHeadDim * 4;
+  L.ex2 = L.ex1 + 16 * kMaxTok * 8;
+  L.gin = L.ex2 + 16 * kMaxTok * 4;
+  L.total = L.gin + kc * 2;
   return L;
 }
 
@@ -89,6 +109,7 @@ struct GvStatic {
   int64_t slot[2], islot[2];
   uint64_t mma_bar;              // the MMAs of a batch have completed
   uint64_t recv_bar;             // partial rows received (transaction bytes)
+  uint64_t ex1_bar, ex2_bar;     // fused: the cluster's norm partials received
   uint32_t tmem;
   int ok;
 };
@@ -102,8 +123,117 @@ __device__ __forceinline__ void st_async_b32(uint32_t caddr, float v, uint32_t c
                : "memory");
 }
 
-template <int WFMT, int C>
+// The fused variant's row normalisation for the CTA's K range [k0, k1) of
+// every token (16 threads a token: thread (m, sub) holds chunks sub + 16j of
+// 8 elements), written as the MMA's B operand.  Exchanges with the 16 CTAs
+// of the cluster; leaves the per-token scales in xs (per-channel format).
+template <int WFMT>
+__device__ __forceinline__ void fused_norm_quant(const Params &p, int tid, int ks, int k0, int k1, int h,
+                                                 uint8_t *x_s, uint8_t *sfb_s, float2 *ex1, float *ex2,
+                                                 const uint4 *gin_s, float *xs, uint64_t *ex1_bar,
+                                                 uint64_t *ex2_bar) {
+  constexpr int kJ = kFusedMaxKc / 8 / 16;  // chunks a thread
+  const int M = p.M, K = p.H;
+  const int m = tid >> 4, sub = tid & 15;
+  const int cpt = (k1 - k0) / 8;  // chunks of 8 elements a token in the range
+  const bool active = m < M;
+  float acc[kJ][8];
+  float sh = 0.f, sl = 0.f;
+  if (active) {
+    const uint4 *ar = reinterpret_cast<const uint4 *>(p.ar + (int64_t)m * K + k0);
+    const uint4 *res = reinterpret_cast<const uint4 *>(p.res + (int64_t)m * K + k0);
+    uint4 *rout = (h == 0 && p.residual) ? reinterpret_cast<uint4 *>(p.residual + (int64_t)m * K + k0) : nullptr;
+#pragma unroll
+    for (int j = 0; j < kJ; ++j) {
+      const int c = sub + 16 * j;
+      if (c < cpt) {
+        uint4 rb;
+        acc8(__ldcs(ar + c), __ldcs(res + c), acc[j], rb, sh, sl);
+        if (rout) __stcs(rout + c, rb);
+      }
+    }
+  }
+  // the token's sum over this K range, in all 16 lanes of the group
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) {
+    const float oh = __shfl_xor_sync(0xffffffffu, sh, o), ol = __shfl_xor_sync(0xffffffffu, sl, o);
+    dd_add(sh, sl, oh, ol);
+  }
+  cluster_wait();  // every CTA of the cluster has initialised its barriers
+  // lane sub of token m's group sends this range's partial to cluster CTA sub
+  if (active) {
+    float2 *dst = ex1 + ks * kMaxTok + m;
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+                     mapa(smem_u32(dst), sub)),
+                 "f"(sh), "f"(sl), "r"(mapa(smem_u32(ex1_bar), sub))
+                 : "memory");
+  }
+  const bool ok1 = mbar_wait_cluster(ex1_bar, 0, p.status);
+  float rh = 0.f, rl = 0.f;
+  float amax = 0.f;
+  if (active && ok1) {
+    float th = ex1[m].x, tl = ex1[m].y;  // the 16 K ranges in order: the same sum in every CTA
+#pragma unroll
+    for (int q = 1; q < 16; ++q) dd_add(th, tl, ex1[q * kMaxTok + m].x, ex1[q * kMaxTok + m].y);
+    rstd_from_dd(th, tl, K, p.eps, rh, rl);
+#pragma unroll
+    for (int j = 0; j < kJ; ++j) {
+      const int c = sub + 16 * j;
+      if (c < cpt) {
+        norm8(acc[j], gin_s[c], rh, rl);
+        amax = fmaxf(amax, amax8(acc[j]));
+      }
+    }
+  }
+  // quantise into the B operand: chunk c of token m is K bytes 8c .. 8c + 7 of
+  // the range: 128-byte chunk c / 16, 16-byte piece (c % 16) / 2, half c % 2
+  auto put = [&](int c, uint2 w) {
+    *reinterpret_cast<uint2 *>(x_s + (c >> 4) * kXChunkBytes + swz(m, (c & 15) >> 1) + 8 * (c & 1)) = w;
+  };
+  if (WFMT == 0) {
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (active) {
+      float *dst = ex2 + ks * kMaxTok + m;
+      asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+                       mapa(smem_u32(dst), sub)),
+                   "r"(__float_as_uint(amax)), "r"(mapa(smem_u32(ex2_bar), sub))
+                   : "memory");
+    }
+    const bool ok2 = mbar_wait_cluster(ex2_bar, 0, p.status);
+    if (active && ok1 && ok2) {
+      float tmax = 0.f;
+#pragma unroll
+      for (int q = 0; q < 16; ++q) tmax = fmaxf(tmax, ex2[q * kMaxTok + m]);
+      const float s = tmax == 0.f ? 1.0f : __fdiv_rn(tmax, kFp8Max);
+#pragma unroll
+      for (int j = 0; j < kJ; ++j) {
+        const int c = sub + 16 * j;
+        if (c < cpt) put(c, quant8_ptpc(acc[j], s));
+      }
+      if (sub == 0) xs[m] = s;
+    }
+  } else {
+    // a 32-element block is 4 consecutive chunks: lanes sub .. sub + 3 of the group
+#pragma unroll
+    for (int j = 0; j < kJ; ++j) {
+      const int c = sub + 16 * j;
+      float bm = (active && ok1 && c < cpt) ? amax8(acc[j]) : 0.f;
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+      if (active && ok1 && c < cpt) {
+        const int e = mx_exponent(bm);
+        put(c, quant8_mx(acc[j], pow2_neg(e)));
+        // F8_128x4 atom of 128-byte chunk c / 16: row m, K-block (c / 4) % 4
+        if ((c & 3) == 0) sfb_s[(c >> 4) * kSfAtom + m * 16 + ((c >> 2) & 3)] = (uint8_t)(e + 127);
+      }
+    }
+  }
+}
+
+template <int WFMT, int C, bool FUSED>
 __global__ void __launch_bounds__(kGvThreads, 3) gemv_kernel(Params p, int kc, int use_pdl) {
+  static_assert(!FUSED || C == 16, "the fused variant exchanges norm partials among 16 K ranges");
   constexpr int TS = (kMaxTok + C - 1) / C;
   extern __shared__ uint8_t dsm_raw[];
   uint8_t *dsm = dsm_raw + ((1024 - (smem_u32(dsm_raw) & 1023)) & 1023);
@@ -111,6 +241,9 @@ __global__ void __launch_bounds__(kGvThreads, 3) gemv_kernel(Params p, int kc, i
   const GvLayout L = gv_layout(C, kc, WFMT);
   uint8_t *w_s = dsm + L.w, *x_s = dsm + L.x, *sfa_s = dsm + L.sfa, *sfb_s = dsm + L.sfb;
   float *recv = reinterpret_cast<float *>(dsm + L.recv);
+  float2 *ex1 = reinterpret_cast<float2 *>(dsm + L.ex1);
+  float *ex2 = reinterpret_cast<float *>(dsm + L.ex2);
+  uint4 *gin_s = reinterpret_cast<uint4 *>(dsm + L.gin);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int K = p.H, M = p.M, ksf = K >> 5;
@@ -127,6 +260,13 @@ __global__ void __launch_bounds__(kGvThreads, 3) gemv_kernel(Params p, int kc, i
     mbar_init(&ss.recv_bar, 1);
     if (ntok) mbar_expect_tx(&ss.recv_bar, (uint32_t)(ntok * C * kHeadDim * 4));
     else mbar_arrive(&ss.recv_bar);
+    if (FUSED) {  // every CTA sends 8 (then 4) bytes per token to every CTA
+      mbar_init(&ss.ex1_bar, 1);
+      mbar_expect_tx(&ss.ex1_bar, (uint32_t)(16 * M * 8));
+      mbar_init(&ss.ex2_bar, 1);
+      if (WFMT == 0) mbar_expect_tx(&ss.ex2_bar, (uint32_t)(16 * M * 4));
+      else mbar_arrive(&ss.ex2_bar);
+    }
     ss.ok = 1;
     fence_mbar_init();
   }
@@ -148,7 +288,18 @@ __global__ void __launch_bounds__(kGvThreads, 3) gemv_kernel(Params p, int kc, i
       }
     cp_async_commit();
   };
+  if (FUSED) {  // the K range's input-norm gamma (a model constant), its own group
+    for (int i = tid; i < (k1 - k0) / 8; i += kGvThreads) cp_async16(gin_s + i, p.g_in + k0 + 8 * i);
+    cp_async_commit();
+  }
   issue_weights(0);
+  if (FUSED) {  // token rows >= M of the B operand are zero; their scales 2^0
+    for (int i = tid; i < nch * kXChunkBytes / 16; i += kGvThreads)
+      reinterpret_cast<uint4 *>(x_s)[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (WFMT == 1)
+      for (int i = tid; i < nch * kSfAtom / 16; i += kGvThreads)
+        reinterpret_cast<uint4 *>(sfb_s)[i] = make_uint4(0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu);
+  }
   const bool is_v = h >= p.v0 && h < p.iq0;
   if (tid < 32) {
     if (WFMT == 0)
@@ -159,6 +310,7 @@ __global__ void __launch_bounds__(kGvThreads, 3) gemv_kernel(Params p, int kc, i
       reinterpret_cast<uint4 *>(ss.gam)[tid - 32] = __ldg(reinterpret_cast<const uint4 *>(gsrc) + (tid - 32));
     }
   }
+  if (FUSED) cp_async_wait<1>();  // the gamma (the weights stay in flight)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -168,18 +320,20 @@ __global__ void __launch_bounds__(kGvThreads, 3) gemv_kernel(Params p, int kc, i
     pdl_wait();
   }
   // ------------------------------------------ activations and per-token data
-  for (int i = tid; i < nch * 16 * 8; i += kGvThreads) {
-    const int j = i >> 7, rc = i & 127, r = rc >> 3, c = rc & 7;
-    uint8_t *dst = x_s + j * kXChunkBytes + swz(r, c);
-    if (r < M) cp_async16(dst, p.xq + (int64_t)r * K + k0 + j * kChunk + 16 * c);
-    else *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
-  }
-  if (WFMT == 1)
-    for (int i = tid; i < nch * (kSfAtom / 16); i += kGvThreads) {
-      const int j = i / (kSfAtom / 16), c = i - j * (kSfAtom / 16);
-      cp_async16(sfb_s + j * kSfAtom + 16 * c, p.xsf + ((int64_t)(k0 / kChunk) + j) * kSfAtom + 16 * c);
+  if (!FUSED) {
+    for (int i = tid; i < nch * 16 * 8; i += kGvThreads) {
+      const int j = i >> 7, rc = i & 127, r = rc >> 3, c = rc & 7;
+      uint8_t *dst = x_s + j * kXChunkBytes + swz(r, c);
+      if (r < M) cp_async16(dst, p.xq + (int64_t)r * K + k0 + j * kChunk + 16 * c);
+      else *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
     }
-  if (WFMT == 0 && tid < M) cp_async4(&ss.xs[tid], p.x_scale + tid);
+    if (WFMT == 1)
+      for (int i = tid; i < nch * (kSfAtom / 16); i += kGvThreads) {
+        const int j = i / (kSfAtom / 16), c = i - j * (kSfAtom / 16);
+        cp_async16(sfb_s + j * kSfAtom + 16 * c, p.xsf + ((int64_t)(k0 / kChunk) + j) * kSfAtom + 16 * c);
+      }
+    if (WFMT == 0 && tid < M) cp_async4(&ss.xs[tid], p.x_scale + tid);
+  }
   // tokens finished here: ks + C * j, j < TS
   const bool cs_lane = warp == 7 && lane < 8 * TS && ks + C * (lane >> 3) < M;
   int64_t pos = 0;
@@ -197,6 +351,7 @@ __global__ void __launch_bounds__(kGvThreads, 3) gemv_kernel(Params p, int kc, i
     cp_async16(&ss.cs[lane >> 3][8 * (lane & 7)], p.cos_sin + pos * kRotDim + 8 * (lane & 7));
   }
   cp_async_commit();
+  if (FUSED) fused_norm_quant<WFMT>(p, tid, ks, k0, k1, h, x_s, sfb_s, ex1, ex2, gin_s, ss.xs, &ss.ex1_bar, &ss.ex2_bar);
   cp_async_wait<1>();  // weights of batch 0 and the activations
   fence_proxy_async_smem();
   __syncthreads();
@@ -253,7 +408,7 @@ __global__ void __launch_bounds__(kGvThreads, 3) gemv_kernel(Params p, int kc, i
     tc_fence_after();
     tc_dealloc(tmem, kTmemCols);
   }
-  cluster_wait();  // every CTA of the cluster has initialised its barriers
+  if (!FUSED) cluster_wait();  // every CTA of the cluster has initialised its barriers
   if (warp < 4) {
     const int r = warp * 32 + lane;  // weight row of the head
 #pragma unroll
@@ -301,8 +456,8 @@ int gv_smem(int C, int kc, int mx) { return gv_layout(C, kc, mx).total + 1024; }
 
 // Cluster size usable on the current device: 16 where clusters of 16 CTAs
 // with `smem16` bytes of dynamic shared memory can be co-scheduled, else 8.
-// Queried once per (kernel, device) and again only for a larger
-// shared-memory size; the attributes it sets stay set.
+// Queried once per device and again only for a larger shared-memory size;
+// the attributes it sets stay set.
 template <int WFMT>
 int pick_cluster(int smem16) {
   struct Entry {
@@ -313,9 +468,13 @@ int pick_cluster(int smem16) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
   if (cached[dev].c && cached[dev].smem >= smem16) return cached[dev].c;
   int c = 8;
-  const void *k16 = reinterpret_cast<const void *>(gemv_kernel<WFMT, 16>);
-  bool failed = cudaFuncSetAttribute(k16, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess;
-  if (!failed) failed = ensure_smem_attr(k16, smem16) != cudaSuccess;
+  const void *k16[2] = {reinterpret_cast<const void *>(gemv_kernel<WFMT, 16, false>),
+                        reinterpret_cast<const void *>(gemv_kernel<WFMT, 16, true>)};
+  bool failed = false;
+  for (const void *k : k16) {
+    if (!failed) failed = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess;
+    if (!failed) failed = ensure_smem_attr(k, smem16) != cudaSuccess;
+  }
   if (!failed) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -329,7 +488,7 @@ int pick_cluster(int smem16) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    failed = cudaOccupancyMaxActiveClusters(&n, k16, &cfg) != cudaSuccess;
+    failed = cudaOccupancyMaxActiveClusters(&n, k16[1], &cfg) != cudaSuccess;
     if (!failed && n >= 1) c = 16;
   }
   if (failed) cudaGetLastError();  // a refused attribute or query only means: clusters of 8
@@ -337,11 +496,11 @@ int pick_cluster(int smem16) {
   return c;
 }
 
-template <int WFMT, int C>
+template <int WFMT, int C, bool FUSED>
 cudaError_t launch_c(const Params &p, bool pdl, cudaStream_t stream) {
   const int kc = gv_kc(p.H, C);
   const int smem = gv_smem(C, kc, WFMT);
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemv_kernel<WFMT, C>), smem);
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemv_kernel<WFMT, C, FUSED>), smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
@@ -357,19 +516,27 @@ cudaError_t launch_c(const Params &p, bool pdl, cudaStream_t stream) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, gemv_kernel<WFMT, C>, p, kc, (int)pdl);
+  return cudaLaunchKernelEx(&cfg, gemv_kernel<WFMT, C, FUSED>, p, kc, (int)pdl);
 }
 
 template <int WFMT>
-cudaError_t launch_t(const Params &p, bool pdl, cudaStream_t stream) {
-  if (pick_cluster<WFMT>(gv_smem(16, gv_kc(p.H, 16), WFMT)) == 16) return launch_c<WFMT, 16>(p, pdl, stream);
-  return launch_c<WFMT, 8>(p, pdl, stream);
+bool fused_ok(int H) {
+  return gv_kc(H, 16) <= kFusedMaxKc && pick_cluster<WFMT>(gv_smem(16, gv_kc(H, 16), WFMT)) == 16;
+}
+
+template <int WFMT>
+cudaError_t launch_t(const Params &p, bool fused, bool pdl, cudaStream_t stream) {
+  if (fused) return launch_c<WFMT, 16, true>(p, pdl, stream);
+  if (pick_cluster<WFMT>(gv_smem(16, gv_kc(p.H, 16), WFMT)) == 16) return launch_c<WFMT, 16, false>(p, pdl, stream);
+  return launch_c<WFMT, 8, false>(p, pdl, stream);
 }
 
 }  // namespace
 
-cudaError_t launch_gemv(const Params &p, bool pdl, cudaStream_t stream) {
-  return p.weight_fmt == 0 ? launch_t<0>(p, pdl, stream) : launch_t<1>(p, pdl, stream);
+bool gemv_fuses_prologue(int H, int weight_fmt) { return weight_fmt == 0 ? fused_ok<0>(H) : fused_ok<1>(H); }
+
+cudaError_t launch_gemv(const Params &p, bool fused, bool pdl, cudaStream_t stream) {
+  return p.weight_fmt == 0 ? launch_t<0>(p, fused, pdl, stream) : launch_t<1>(p, fused, pdl, stream);
 }
 
 }  // namespace pa

@@ -34,8 +34,11 @@ cudaError_t launch_prologue(const Params &p, int grid, bool pdl, cudaStream_t st
 cudaError_t launch_pack_scales(const uint8_t *src, uint8_t *dst, int rows, int ksf, cudaStream_t stream);
 
 // Skinny-M path (M <= 16): FP8 GEMV on one thread-block cluster per head,
-// the head epilogue fused behind the in-cluster reduction.
-cudaError_t launch_gemv(const Params &p, bool pdl, cudaStream_t stream);
+// the head epilogue fused behind the in-cluster reduction.  With `fused`
+// (allowed when gemv_fuses_prologue(H, weight format)) the kernel also does
+// the prologue's work and no prologue is launched.
+bool gemv_fuses_prologue(int H, int weight_fmt);
+cudaError_t launch_gemv(const Params &p, bool fused, bool pdl, cudaStream_t stream);
 
 // Tensor-core path: persistent tcgen05 GEMM with the fused head epilogue,
 // on single CTAs (128 x 128 tiles) or on CTA pairs (cta_group::2, 256 x 256).

@@ -47,6 +47,26 @@ __device__ __forceinline__ void dd_add(float &hi, float &lo, float x, float xl) 
 // and one Newton step with its second-order term, r = r0 (1 - t/2 + 3t^2/8)
 // with t = x r0^2 - 1 evaluated with FMAs, gives the rest.  Every thread ends
 // with the same pair.
+// The rstd pair from the row's sum of squares (sh, sl), as described below.
+__device__ __forceinline__ void rstd_from_dd(float sh, float sl, int H, float eps, float &rh, float &rl) {
+  // x = sum / H + eps
+  const float fh = (float)H;
+  const float qh = __fdiv_rn(sh, fh);
+  const float rem = __fmaf_rn(-qh, fh, sh);  // exact: sh - qh * H
+  const float ql = __fdiv_rn(__fadd_rn(rem, sl), fh);
+  float xh, xe;
+  two_sum(qh, eps, xh, xe);
+  const float xl = __fadd_rn(ql, xe);
+  const float r0 = rsqrtf(xh);
+  float p, pe;
+  two_prod(r0, r0, p, pe);
+  float t = __fmaf_rn(xh, p, -1.0f);
+  t = __fmaf_rn(xh, pe, t);
+  t = __fmaf_rn(xl, p, t);
+  rh = r0;
+  rl = __fmul_rn(__fmul_rn(r0, t), __fmaf_rn(0.375f, t, -0.5f));
+}
+
 template <int NTHR>
 __device__ __forceinline__ void block_rstd_dd(float hi, float lo, float2 *red, int H, float eps, float &rh,
                                               float &rl) {
@@ -71,22 +91,7 @@ __device__ __forceinline__ void block_rstd_dd(float hi, float lo, float2 *red, i
   }
   sh = __shfl_sync(0xffffffffu, sh, 0);  // lanes >= W summed only zeros
   sl = __shfl_sync(0xffffffffu, sl, 0);
-  // x = sum / H + eps
-  const float fh = (float)H;
-  const float qh = __fdiv_rn(sh, fh);
-  const float rem = __fmaf_rn(-qh, fh, sh);  // exact: sh - qh * H
-  const float ql = __fdiv_rn(__fadd_rn(rem, sl), fh);
-  float xh, xe;
-  two_sum(qh, eps, xh, xe);
-  const float xl = __fadd_rn(ql, xe);
-  const float r0 = rsqrtf(xh);
-  float p, pe;
-  two_prod(r0, r0, p, pe);
-  float t = __fmaf_rn(xh, p, -1.0f);
-  t = __fmaf_rn(xh, pe, t);
-  t = __fmaf_rn(xl, p, t);
-  rh = r0;
-  rl = __fmul_rn(__fmul_rn(r0, t), __fmaf_rn(0.375f, t, -0.5f));
+  rstd_from_dd(sh, sl, H, eps, rh, rl);
 }
 
 // The smallest e with 448 * 2^e >= amax (amax > 0), clamped to [-127, 127];
@@ -119,6 +124,70 @@ __device__ __forceinline__ float block_max(float v, float *red) {
   return __shfl_sync(0xffffffffu, r, 0);  // lanes >= W saw only zeros
 }
 
+// 8 elements of a row: acc = ar + res in f32, their bf16 residual bits, and
+// the (hi, lo) running sum of acc^2.
+__device__ __forceinline__ void acc8(uint4 a, uint4 r, float (&acc)[8], uint4 &resid, float &ss, float &ss_lo) {
+  const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, rw[4] = {r.x, r.y, r.z, r.w};
+  uint32_t ow[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float lo = bf16_to_f32(aw[i] & 0xffff) + bf16_to_f32(rw[i] & 0xffff);
+    float hi = bf16_to_f32(aw[i] >> 16) + bf16_to_f32(rw[i] >> 16);
+    acc[2 * i] = lo;
+    acc[2 * i + 1] = hi;
+    ow[i] = (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
+    float q, ql;
+    two_prod(lo, lo, q, ql);
+    dd_add(ss, ss_lo, q, ql);
+    two_prod(hi, hi, q, ql);
+    dd_add(ss, ss_lo, q, ql);
+  }
+  resid = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+}
+
+// The normalised row n = acc * rstd * (1 + gamma), rounded to f32 once from
+// an (almost) exact value: rstd as the pair rh + rl, the products as
+// error-free pairs.  An FP8 code that moved by one step would shift the whole
+// token's projection, so the f32 n (and everything quantised from it)
+// follows the definition exactly rather than one particular rounding order.
+// In place on 8 elements; gw4 holds their 8 bf16 gammas.
+__device__ __forceinline__ void norm8(float (&acc)[8], uint4 gw4, float rh, float rl) {
+  const uint32_t gw[4] = {gw4.x, gw4.y, gw4.z, gw4.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float gam = bf16_to_f32(i & 1 ? gw[i >> 1] >> 16 : gw[i >> 1] & 0xffff);
+    // acc * (rh + rl) = p + e1 + e2, then (p + e) * (1 + gam)
+    float p1, e1, a1, a2, s1, s2;
+    two_prod(acc[i], rh, p1, e1);
+    const float e = __fadd_rn(e1, __fmul_rn(acc[i], rl));
+    two_prod(p1, gam, a1, a2);
+    two_sum(p1, a1, s1, s2);
+    const float tail = __fadd_rn(__fadd_rn(s2, a2), __fmaf_rn(e, gam, e));
+    acc[i] = __fadd_rn(s1, tail);
+  }
+}
+
+// Per-token FP8: e4m3(n / s), a true f32 divide.
+__device__ __forceinline__ uint2 quant8_ptpc(const float (&n)[8], float s) {
+  uint2 w;
+  w.x = e4m3x4(__fdiv_rn(n[0], s), __fdiv_rn(n[1], s), __fdiv_rn(n[2], s), __fdiv_rn(n[3], s));
+  w.y = e4m3x4(__fdiv_rn(n[4], s), __fdiv_rn(n[5], s), __fdiv_rn(n[6], s), __fdiv_rn(n[7], s));
+  return w;
+}
+// MXFP8: e4m3(n * 2^-e), an exact scaling by a power of two.
+__device__ __forceinline__ uint2 quant8_mx(const float (&n)[8], float inv) {
+  uint2 w;
+  w.x = e4m3x4(n[0] * inv, n[1] * inv, n[2] * inv, n[3] * inv);
+  w.y = e4m3x4(n[4] * inv, n[5] * inv, n[6] * inv, n[7] * inv);
+  return w;
+}
+__device__ __forceinline__ float amax8(const float (&n)[8]) {
+  float a = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(n[e]));
+  return a;
+}
+
 // Normalise and quantise token row m with the NTHR threads of the block
 // (every thread must call it).  Chunks of 8 elements: thread tid holds chunks
 // tid + NTHR * j, j < MAXC, so H <= 8 * NTHR * MAXC; NTHR % 4 == 0 keeps the
@@ -144,31 +213,11 @@ __device__ __forceinline__ void norm_quant_row(const Params &p, const int m, flo
   for (int j = 0; j < MAXC; ++j) {
     const int c = tid + NTHR * j;
     if (c < nch) {
-      const uint4 a = __ldcs(ar + c), r = __ldcs(res + c);
-      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, rw[4] = {r.x, r.y, r.z, r.w};
-      uint32_t ow[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float lo = bf16_to_f32(aw[i] & 0xffff) + bf16_to_f32(rw[i] & 0xffff);
-        float hi = bf16_to_f32(aw[i] >> 16) + bf16_to_f32(rw[i] >> 16);
-        acc[j][2 * i] = lo;
-        acc[j][2 * i + 1] = hi;
-        ow[i] = (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
-        float q, ql;
-        two_prod(lo, lo, q, ql);
-        dd_add(ss, ss_lo, q, ql);
-        two_prod(hi, hi, q, ql);
-        dd_add(ss, ss_lo, q, ql);
-      }
-      if (rout) __stcs(rout + c, make_uint4(ow[0], ow[1], ow[2], ow[3]));
+      uint4 rb;
+      acc8(__ldcs(ar + c), __ldcs(res + c), acc[j], rb, ss, ss_lo);
+      if (rout) __stcs(rout + c, rb);
     }
   }
-  // The normalised row n = acc * rstd * (1 + gamma) is rounded to f32 once,
-  // from an (almost) exact value: sum(acc^2) and rstd as double-floats, the
-  // products as error-free pairs.  An FP8 code
-  // that moved by one step would shift the whole token's projection, so the
-  // f32 n (and everything quantised from it) follows the definition exactly
-  // rather than one particular rounding order.
   float rh, rl;
   block_rstd_dd<NTHR>(ss, ss_lo, red2, H, p.eps, rh, rl);
   float amax = 0.f;
@@ -176,21 +225,8 @@ __device__ __forceinline__ void norm_quant_row(const Params &p, const int m, flo
   for (int j = 0; j < MAXC; ++j) {
     const int c = tid + NTHR * j;
     if (c < nch) {
-      const uint32_t gw[4] = {gpre[j].x, gpre[j].y, gpre[j].z, gpre[j].w};
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float gam = bf16_to_f32(i & 1 ? gw[i >> 1] >> 16 : gw[i >> 1] & 0xffff);
-        // acc * (rh + rl) = p + e1 + e2, then (p + e) * (1 + gam)
-        float p1, e1, a1, a2, s1, s2;
-        two_prod(acc[j][i], rh, p1, e1);
-        const float e = __fadd_rn(e1, __fmul_rn(acc[j][i], rl));
-        two_prod(p1, gam, a1, a2);
-        two_sum(p1, a1, s1, s2);
-        const float tail = __fadd_rn(__fadd_rn(s2, a2), __fmaf_rn(e, gam, e));
-        acc[j][i] = __fadd_rn(s1, tail);
-      }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(acc[j][e]));
+      norm8(acc[j], gpre[j], rh, rl);
+      amax = fmaxf(amax, amax8(acc[j]));
     }
   }
   uint2 *xq = reinterpret_cast<uint2 *>(p.xq + (int64_t)m * H);
@@ -200,14 +236,7 @@ __device__ __forceinline__ void norm_quant_row(const Params &p, const int m, flo
 #pragma unroll
     for (int j = 0; j < MAXC; ++j) {
       const int c = tid + NTHR * j;
-      if (c < nch) {
-        uint2 w;
-        w.x = e4m3x4(__fdiv_rn(acc[j][0], s), __fdiv_rn(acc[j][1], s), __fdiv_rn(acc[j][2], s),
-                     __fdiv_rn(acc[j][3], s));
-        w.y = e4m3x4(__fdiv_rn(acc[j][4], s), __fdiv_rn(acc[j][5], s), __fdiv_rn(acc[j][6], s),
-                     __fdiv_rn(acc[j][7], s));
-        xq[c] = w;
-      }
+      if (c < nch) xq[c] = quant8_ptpc(acc[j], s);
     }
     if (tid == 0) p.x_scale[m] = s;
   } else {
@@ -216,19 +245,12 @@ __device__ __forceinline__ void norm_quant_row(const Params &p, const int m, flo
     for (int j = 0; j < MAXC; ++j) {
       const int c = tid + NTHR * j;
       if (j * NTHR < nch) {  // warp-uniform: every lane reaches the shuffles
-        float bm = 0.f;
-        if (c < nch)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) bm = fmaxf(bm, fabsf(acc[j][e]));
+        float bm = c < nch ? amax8(acc[j]) : 0.f;
         bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
         bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
         if (c < nch) {
           const int e = mx_exponent(bm);
-          const float inv = pow2_neg(e);
-          uint2 w;
-          w.x = e4m3x4(acc[j][0] * inv, acc[j][1] * inv, acc[j][2] * inv, acc[j][3] * inv);
-          w.y = e4m3x4(acc[j][4] * inv, acc[j][5] * inv, acc[j][6] * inv, acc[j][7] * inv);
-          xq[c] = w;
+          xq[c] = quant8_mx(acc[j], pow2_neg(e));
           if ((c & 3) == 0) p.xsf[sf128x4_offset(m, c >> 2, ksf)] = (uint8_t)(e + 127);
         }
       }

@@ -102,8 +102,10 @@ def test_path_choice():
                     flags=flags)
         return B.pre_attn_path(r.handle, M)
 
-    assert path(8) == B.PA_PATH_GEMV and path(16) == B.PA_PATH_GEMV
-    assert path(8, B.PA_FLAG_FORCE_GEMM) != B.PA_PATH_GEMV
+    skinny = (B.PA_PATH_GEMV, B.PA_PATH_GEMV_FUSED)
+    assert path(8) in skinny and path(16) in skinny
+    assert path(8) == B.PA_PATH_GEMV and path(8, B.PA_FLAG_FUSE) == B.PA_PATH_GEMV_FUSED
+    assert path(8, B.PA_FLAG_FORCE_GEMM) in (B.PA_PATH_GEMM_SINGLE, B.PA_PATH_GEMM_PAIR)
     assert path(8192) == B.PA_PATH_GEMM_PAIR  # 1312 pair tiles vs 5184 single tiles
     assert path(8192, B.PA_FLAG_GEMM_SINGLE) == B.PA_PATH_GEMM_SINGLE
     assert path(64, B.PA_FLAG_GEMM_PAIR) == B.PA_PATH_GEMM_PAIR

@@ -120,3 +120,18 @@ def test_k_ranges(H, fmt):
     check(workloads.Workload(f"ks{H}", H=H, nkv=1, M=11 if fmt == "mx" else 5, weight_fmt=fmt, cache_fmt="fp8",
                              seed=H + (fmt == "mx"), positions="uniform", max_pos=500, pool_pages16=64,
                              q_fp8=True, iq_fp8=True))
+
+
+@pytest.mark.parametrize("fmt", ["ptpc", "mx"])
+def test_fused_single_kernel(fmt):
+    # the skinny path in one kernel: the row normalisation runs inside the
+    # GEMV's clusters (norm partials exchanged among the 16 K ranges)
+    from indexer_projection_gb300 import binding as B
+    flags = B.PA_FLAG_FORCE_GEMV | B.PA_FLAG_FUSE
+    check(workloads.decode().replace(weight_fmt=fmt, q_fp8=True, iq_fp8=True), flags=flags)
+    check(workloads.tiny().replace(M=13, nkv=2, n_q=0, n_iq=0, weight_fmt=fmt, iq_fp8=True), flags=flags)
+    check(workloads.Workload("fz_ragged", H=4352, nkv=1, M=16, weight_fmt=fmt, cache_fmt="nvfp4", seed=91,
+                             positions="uniform", max_pos=500, pool_pages=64, q_fp8=True, iq_fp8=True,
+                             outlier_frac=0.2), flags=flags)
+    check(workloads.Workload("fz_one", H=6144, nkv=2, M=1, weight_fmt=fmt, cache_fmt="fp8", seed=92,
+                             positions="uniform", max_pos=500, pool_pages16=64), flags=flags)
