@@ -339,9 +339,11 @@ int pre_attn_run(pa_handle *h, int M, const pa_step_inputs *in, const pa_weights
   cudaStream_t s = (cudaStream_t)stream;
   // the skinny path normalises the rows inside its own launch when it can
   const bool fused = path == PA_PATH_GEMV_FUSED;
-  if (!fused) {
-    const int pro_grid = (!gemv && c.weight_format == PA_WEIGHT_MXFP8) ? L.m_pad : M;
-    e = pa::launch_prologue(p, pro_grid, pdl, s);
+  if (gemv && !fused) {
+    e = pa::launch_prologue_rows(p, pdl, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  } else if (!gemv) {
+    e = pa::launch_prologue(p, c.weight_format == PA_WEIGHT_MXFP8 ? L.m_pad : M, pdl, s);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   if (h->prof_before && (e = cudaEventRecord(h->prof_before, s)) != cudaSuccess) return cuda_fail(e);

@@ -13,8 +13,8 @@
 // weight stream overlaps the prologue.  After the wait the CTA stages the
 // range's activations the same way and one thread issues the MMAs:
 // tcgen05.mma m128 n16 k32 per 32 bytes of K, weights as A (128 rows),
-// tokens as B (16 columns, the absent ones zero), f32 accumulator in tensor
-// memory (kind::f8f6f4; for MXFP8 kind::mxf8f6f4.block_scale with the
+// tokens as B (16 columns, the absent ones zero), f32 accumulators in tensor
+// memory (one per staged chunk, so the MMA chains overlap) (kind::f8f6f4; for MXFP8 kind::mxf8f6f4.block_scale with the
 // F8_128x4 scale atoms of both operands moved to tensor memory by
 // tcgen05.cp).  A K range longer than the 3 staged 128-byte chunks is
 // streamed in batches.  The pre_attn page's GEMV tasks put the token on the
@@ -66,8 +66,10 @@ constexpr int kWChunkBytes = kHeadDim * kChunk;  // 16 KB: 128 rows x 128 B
 constexpr int kXChunkBytes = 16 * kChunk;        // 2 KB: 16 token rows x 128 B
 constexpr int kSfAtom = 512;       // F8_128x4: 128 rows x 4 K-blocks
 constexpr int kMaxTok = 16;
-constexpr int kTmemCols = 32;      // accumulator 16 columns, scale factors at 16 and 20
-constexpr int kSfaCol = 16, kSfbCol = 20;
+// One 16-column accumulator per staged chunk (independent MMA chains that
+// the tensor core can overlap; summed when read back), scale factors after.
+constexpr int kTmemCols = 64;
+constexpr int kSfaCol = 16 * kStageChunks, kSfbCol = kSfaCol + 4;
 constexpr uint32_t kIdescF8 = idesc_f8(128, 16);
 constexpr uint32_t kIdescMx = idesc_mx(128, 16);
 constexpr int kFusedMaxKc = 384;   // fused variant: 3 chunks of 8 elements a thread
@@ -376,10 +378,11 @@ __global__ void __launch_bounds__(kGvThreads, 3) gemv_kernel(Params p, int kc, i
         }
 #pragma unroll
         for (int k = 0; k < kChunk / 32; ++k) {
-          const uint32_t acc = (c0 + j) > 0 || k > 0;
+          const uint32_t acc = c0 > 0 || k > 0;
+          const uint32_t d = tmem + 16 * j;  // chunk j's accumulator
           // +32 bytes along K inside the swizzle atom: +2 in the 16-byte address field
-          if (WFMT == 0) mma_f8(tmem, ad + 2 * k, bd + 2 * k, kIdescF8, acc);
-          else mma_mx(tmem, ad + 2 * k, bd + 2 * k, kIdescMx | ((uint32_t)k << 4) | ((uint32_t)k << 29),
+          if (WFMT == 0) mma_f8(d, ad + 2 * k, bd + 2 * k, kIdescF8, acc);
+          else mma_mx(d, ad + 2 * k, bd + 2 * k, kIdescMx | ((uint32_t)k << 4) | ((uint32_t)k << 29),
                       tmem + kSfaCol, tmem + kSfbCol, acc);
         }
       }
@@ -394,12 +397,19 @@ __global__ void __launch_bounds__(kGvThreads, 3) gemv_kernel(Params p, int kc, i
   // ---------------------------------- accumulator -> partial rows of the cluster
   float v[16];
   if (warp < 4) {
-    if (nch > 0 && ss.ok) {
-      tc_ld16(tmem + ((uint32_t)(warp * 32) << 16), v);
-      tc_wait_ld();
-    } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = 0.f;
+    for (int i = 0; i < 16; ++i) v[i] = 0.f;
+    if (ss.ok) {
+#pragma unroll
+      for (int j = 0; j < kStageChunks; ++j) {
+        if (j < nch) {  // accumulator j holds chunks j, j + 3, ...
+          float u[16];
+          tc_ld16(tmem + ((uint32_t)(warp * 32) << 16) + 16 * j, u);
+          tc_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] += u[i];
+        }
+      }
     }
   }
   tc_fence_before();

@@ -30,6 +30,8 @@ inline cudaError_t ensure_smem_attr(const void *kern, int bytes) {
 
 // Prologue over `grid` CTAs (M rows, plus padding rows of the MXFP8 scale grid).
 cudaError_t launch_prologue(const Params &p, int grid, bool pdl, cudaStream_t stream);
+// Prologue of the skinny path: one thread-block cluster per row (M <= 16).
+cudaError_t launch_prologue_rows(const Params &p, bool pdl, cudaStream_t stream);
 // Row-major [rows, ksf] E8M0 -> F8_128x4 layout.
 cudaError_t launch_pack_scales(const uint8_t *src, uint8_t *dst, int rows, int ksf, cudaStream_t stream);
 

@@ -1,8 +1,14 @@
-// Prologue of the pre-attention step: one CTA per token row.
-// residual add, Gemma RMSNorm and the activation quantiser (pa_norm.cuh),
-// used ahead of the tensor-core path and of the skinny path at large H.
-// HBM-bound: 16-byte coalesced loads and stores, the row held in registers,
-// warp-shuffle + shared-memory block reductions for sum(acc^2) and amax.
+// Prologue of the pre-attention step: residual add, Gemma RMSNorm and the
+// activation quantiser (pa_norm.cuh).
+//   prologue_kernel       one CTA per token row: the tensor-core path's many
+//                         rows (HBM-bound: 16-byte coalesced loads and stores,
+//                         the row in registers, block reductions)
+//   prologue_rows_kernel  one thread-block cluster per token row, a K slice
+//                         per CTA: the skinny path's few rows, whose latency
+//                         the step waits on; the correctly rounded norm costs
+//                         ~50 instructions an element, too much for a few
+//                         SMs, so each row is spread over C SMs and the row
+//                         sums are exchanged through distributed shared memory
 #include "pa_device.cuh"
 #include "pa_launch.h"
 #include "pa_norm.cuh"
@@ -31,6 +37,113 @@ __global__ void __launch_bounds__(NTHR) prologue_kernel(Params p, int use_pdl) {
     return;
   }
   norm_quant_row<WFMT, NTHR, MAXC>(p, m, red, red2);
+}
+
+// One cluster of C CTAs per token row (blockIdx.x / C); CTA r takes the
+// row's elements [r * kc, (r + 1) * kc), kc a multiple of 32 (one 8-element
+// chunk a thread; the four chunks of an MXFP8 block in lanes 4i .. 4i + 3).
+// The CTAs' double-float partial sums of acc^2, and for the per-channel
+// format the partial amax, are sent to every CTA of the cluster with
+// byte-counted st.async; each CTA combines the C partials in the same order,
+// so all agree bit for bit on rstd and on the scale.
+template <int WFMT, int C>
+__global__ void __launch_bounds__(128 * 16 / C) prologue_rows_kernel(Params p, int kc, int use_pdl) {
+  constexpr int NTHR = 128 * 16 / C;
+  constexpr int W = NTHR / 32;
+  __shared__ float2 ex1[C];          // the C partial sums of acc^2
+  __shared__ float ex2[C];           // the C partial amax (per-channel format)
+  __shared__ float2 wred[W];
+  __shared__ float wmax[W];
+  __shared__ __align__(8) uint64_t bar1, bar2;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int m = blockIdx.x / C, r = (int)cta_rank();
+  const int H = p.H, ksf = H >> 5;
+  const int k0 = r * kc, k1 = k0 + kc < H ? k0 + kc : H;
+  const int c = (k0 >> 3) + tid;  // this thread's chunk of the row
+  const bool act = k0 + 8 * tid < k1;
+  if (tid == 0) {
+    mbar_init(&bar1, 1);
+    mbar_expect_tx(&bar1, C * 8);
+    mbar_init(&bar2, 1);
+    if (WFMT == 0) mbar_expect_tx(&bar2, C * 4);
+    else mbar_arrive(&bar2);
+    fence_mbar_init();
+  }
+  cluster_arrive_relaxed();
+  uint4 gw = make_uint4(0u, 0u, 0u, 0u);
+  if (act) gw = __ldg(reinterpret_cast<const uint4 *>(p.g_in) + c);  // a model constant
+  if (use_pdl) {
+    pdl_trigger();
+    pdl_wait();
+  }
+  float acc[8];
+  float sh = 0.f, sl = 0.f;
+  if (act) {
+    uint4 rb;
+    acc8(__ldcs(reinterpret_cast<const uint4 *>(p.ar + (int64_t)m * H) + c),
+         __ldcs(reinterpret_cast<const uint4 *>(p.res + (int64_t)m * H) + c), acc, rb, sh, sl);
+    if (p.residual) __stcs(reinterpret_cast<uint4 *>(p.residual + (int64_t)m * H) + c, rb);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float oh = __shfl_xor_sync(0xffffffffu, sh, o), ol = __shfl_xor_sync(0xffffffffu, sl, o);
+    dd_add(sh, sl, oh, ol);
+  }
+  if (lane == 0) wred[warp] = make_float2(sh, sl);
+  __syncthreads();
+  cluster_wait();  // every CTA of the cluster has initialised its barriers
+  if (tid < C) {   // the CTA's partial, to CTA tid
+    float th = wred[0].x, tl = wred[0].y;
+#pragma unroll
+    for (int w = 1; w < W; ++w) dd_add(th, tl, wred[w].x, wred[w].y);
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+                     mapa(smem_u32(&ex1[r]), tid)),
+                 "f"(th), "f"(tl), "r"(mapa(smem_u32(&bar1), tid))
+                 : "memory");
+  }
+  const bool ok1 = mbar_wait_cluster(&bar1, 0, p.status);
+  float th = ex1[0].x, tl = ex1[0].y;  // the C partials in order: the same sum in every CTA
+#pragma unroll
+  for (int q = 1; q < C; ++q) dd_add(th, tl, ex1[q].x, ex1[q].y);
+  float rh, rl;
+  rstd_from_dd(th, tl, H, p.eps, rh, rl);
+  float amax = 0.f;
+  if (act && ok1) {
+    norm8(acc, gw, rh, rl);
+    amax = amax8(acc);
+  }
+  uint2 *xq = reinterpret_cast<uint2 *>(p.xq + (int64_t)m * H);
+  if (WFMT == 0) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (lane == 0) wmax[warp] = amax;
+    __syncthreads();
+    if (tid < C) {
+      float t = wmax[0];
+#pragma unroll
+      for (int w = 1; w < W; ++w) t = fmaxf(t, wmax[w]);
+      asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+                       mapa(smem_u32(&ex2[r]), tid)),
+                   "r"(__float_as_uint(t)), "r"(mapa(smem_u32(&bar2), tid))
+                   : "memory");
+    }
+    const bool ok2 = mbar_wait_cluster(&bar2, 0, p.status);
+    float tmax = ex2[0];
+#pragma unroll
+    for (int q = 1; q < C; ++q) tmax = fmaxf(tmax, ex2[q]);
+    const float s = tmax == 0.f ? 1.0f : __fdiv_rn(tmax, kFp8Max);
+    if (act && ok1 && ok2) xq[c] = quant8_ptpc(acc, s);
+    if (r == 0 && tid == 0) p.x_scale[m] = s;
+  } else {
+    float bm = act ? amax : 0.f;
+    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+    if (act && ok1) {
+      const int e = mx_exponent(bm);
+      xq[c] = quant8_mx(acc, pow2_neg(e));
+      if ((c & 3) == 0) p.xsf[sf128x4_offset(m, c >> 2, ksf)] = (uint8_t)(e + 127);
+    }
+  }
 }
 
 __global__ void pack_scales_kernel(const uint8_t *src, uint8_t *dst, int rows, int ksf) {
@@ -76,6 +189,64 @@ cudaError_t launch_prologue(const Params &p, int grid, bool pdl, cudaStream_t st
   cfg.numAttrs = pdl ? 1 : 0;
   // fewer rows than a fraction of the SMs: the row latency is the step's
   return grid <= 64 ? launch_1024(p, cfg, pdl) : launch_256(p, cfg, pdl);
+}
+
+namespace {
+template <int WFMT, int C>
+cudaError_t launch_rows(const Params &p, bool pdl, cudaStream_t stream) {
+  const int kc = ((p.H + C - 1) / C + 31) / 32 * 32;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  cfg.gridDim = dim3(p.M * C);
+  cfg.blockDim = dim3(128 * 16 / C);
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, prologue_rows_kernel<WFMT, C>, p, kc, (int)pdl);
+}
+
+// Clusters of 16 where the device co-schedules them (queried once a device),
+// else 8.
+template <int WFMT>
+int rows_cluster() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
+  if (cached[dev]) return cached[dev];
+  int c = 8;
+  const void *k = reinterpret_cast<const void *>(prologue_rows_kernel<WFMT, 16>);
+  bool failed = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess;
+  if (!failed) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(16 * 16);
+    cfg.blockDim = dim3(128);
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 16;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    failed = cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess;
+    if (!failed && n >= 1) c = 16;
+  }
+  if (failed) cudaGetLastError();  // only means: clusters of 8
+  cached[dev] = c;
+  return c;
+}
+}  // namespace
+
+cudaError_t launch_prologue_rows(const Params &p, bool pdl, cudaStream_t stream) {
+  if (p.weight_fmt == 0)
+    return rows_cluster<0>() == 16 ? launch_rows<0, 16>(p, pdl, stream) : launch_rows<0, 8>(p, pdl, stream);
+  return rows_cluster<1>() == 16 ? launch_rows<1, 16>(p, pdl, stream) : launch_rows<1, 8>(p, pdl, stream);
 }
 
 cudaError_t launch_pack_scales(const uint8_t *src, uint8_t *dst, int rows, int ksf, cudaStream_t stream) {
