@@ -431,21 +431,36 @@ __device__ __forceinline__ void head_epilogue(const Params &p, const HeadCtx &hc
     uint8_t *of = is_q ? p.q_fp8 : p.iq_fp8;
     const float sc = is_q ? p.q_fp8_inv : 1.0f;
     const int64_t base = (int64_t)m * nh * kHeadDim + (int64_t)j * kHeadDim + d0;
+    // a thread holding a whole row (E >= 16) stores 16 bytes at a time (a
+    // quarter of the store transactions of 4-byte pieces); a warp holding a
+    // row (E = 4) already writes it contiguously
     if (ob) {
+      auto bf2 = [&](int i) {
+        return (uint32_t)f32_to_bf16_bits(v[i]) | ((uint32_t)f32_to_bf16_bits(v[i + 1]) << 16);
+      };
+      if constexpr (E >= 8) {
 #pragma unroll
-      for (int q = 0; q < E / 4; ++q) {
-        uint2 w;
-        w.x = (uint32_t)f32_to_bf16_bits(v[4 * q]) | ((uint32_t)f32_to_bf16_bits(v[4 * q + 1]) << 16);
-        w.y = (uint32_t)f32_to_bf16_bits(v[4 * q + 2]) | ((uint32_t)f32_to_bf16_bits(v[4 * q + 3]) << 16);
-        *reinterpret_cast<uint2 *>(ob + base + 4 * q) = w;
+        for (int q = 0; q < E / 8; ++q)
+          *reinterpret_cast<uint4 *>(ob + base + 8 * q) =
+              make_uint4(bf2(8 * q), bf2(8 * q + 2), bf2(8 * q + 4), bf2(8 * q + 6));
+      } else {
+#pragma unroll
+        for (int q = 0; q < E / 4; ++q) *reinterpret_cast<uint2 *>(ob + base + 4 * q) = make_uint2(bf2(4 * q), bf2(4 * q + 2));
       }
     }
     if (of) {
+      auto f8x4 = [&](int i) {
+        return is_q ? e4m3x4(v[i] * sc, v[i + 1] * sc, v[i + 2] * sc, v[i + 3] * sc)
+                    : e4m3x4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+      };
+      if constexpr (E >= 16) {
 #pragma unroll
-      for (int q = 0; q < E / 4; ++q) {
-        uint32_t w = is_q ? e4m3x4(v[4 * q] * sc, v[4 * q + 1] * sc, v[4 * q + 2] * sc, v[4 * q + 3] * sc)
-                          : e4m3x4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        *reinterpret_cast<uint32_t *>(of + base + 4 * q) = w;
+        for (int q = 0; q < E / 16; ++q)
+          *reinterpret_cast<uint4 *>(of + base + 16 * q) =
+              make_uint4(f8x4(16 * q), f8x4(16 * q + 4), f8x4(16 * q + 8), f8x4(16 * q + 12));
+      } else {
+#pragma unroll
+        for (int q = 0; q < E / 4; ++q) *reinterpret_cast<uint32_t *>(of + base + 4 * q) = f8x4(4 * q);
       }
     }
     return;
@@ -461,10 +476,17 @@ __device__ __forceinline__ void head_epilogue(const Params &p, const HeadCtx &hc
         return;
       }
       uint8_t *dst = p.index_cache + slot * kHeadDim + d0;
+      auto ik4 = [&](int i) {
+        return e4m3x4(bf16_round(v[i]), bf16_round(v[i + 1]), bf16_round(v[i + 2]), bf16_round(v[i + 3]));
+      };
+      if constexpr (E >= 16) {
 #pragma unroll
-      for (int q = 0; q < E / 4; ++q)
-        *reinterpret_cast<uint32_t *>(dst + 4 * q) = e4m3x4(bf16_round(v[4 * q]), bf16_round(v[4 * q + 1]),
-                                                            bf16_round(v[4 * q + 2]), bf16_round(v[4 * q + 3]));
+        for (int q = 0; q < E / 16; ++q)
+          *reinterpret_cast<uint4 *>(dst + 16 * q) = make_uint4(ik4(16 * q), ik4(16 * q + 4), ik4(16 * q + 8), ik4(16 * q + 12));
+      } else {
+#pragma unroll
+        for (int q = 0; q < E / 4; ++q) *reinterpret_cast<uint32_t *>(dst + 4 * q) = ik4(4 * q);
+      }
       return;
     }
     const int kvh = is_k ? h - p.k0 : h - p.v0;
@@ -481,12 +503,23 @@ __device__ __forceinline__ void head_epilogue(const Params &p, const HeadCtx &hc
     const float s = p.static_kv ? 1.0f : (amax == 0.f ? 1.0f : __fdiv_rn(amax, kFp8Max));
     const int64_t page = (p16 * p.n_kv + kvh) * 2048;
     if (is_k) {
+      auto k4 = [&](int i) {
+        return e4m3x4(__fdiv_rn(bf16_round(v[i]), s), __fdiv_rn(bf16_round(v[i + 1]), s),
+                      __fdiv_rn(bf16_round(v[i + 2]), s), __fdiv_rn(bf16_round(v[i + 3]), s));
+      };
+      if constexpr (E >= 16) {  // 16 dims: one 16-byte row of the page's 16 x 16 block
 #pragma unroll
-      for (int q = 0; q < E / 4; ++q) {
-        const int d = d0 + 4 * q;
-        uint32_t w = e4m3x4(__fdiv_rn(bf16_round(v[4 * q]), s), __fdiv_rn(bf16_round(v[4 * q + 1]), s),
-                            __fdiv_rn(bf16_round(v[4 * q + 2]), s), __fdiv_rn(bf16_round(v[4 * q + 3]), s));
-        *reinterpret_cast<uint32_t *>(p.k_cache + page + (d >> 4) * 256 + t * 16 + (d & 15)) = w;
+        for (int q = 0; q < E / 16; ++q) {
+          const int d = d0 + 16 * q;
+          *reinterpret_cast<uint4 *>(p.k_cache + page + (d >> 4) * 256 + t * 16) =
+              make_uint4(k4(16 * q), k4(16 * q + 4), k4(16 * q + 8), k4(16 * q + 12));
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < E / 4; ++q) {
+          const int d = d0 + 4 * q;
+          *reinterpret_cast<uint32_t *>(p.k_cache + page + (d >> 4) * 256 + t * 16 + (d & 15)) = k4(4 * q);
+        }
       }
       if (d0 == 0) p.k_scale[(p16 * p.n_kv + kvh) * 16 + t] = s;
     } else {
@@ -538,11 +571,20 @@ __device__ __forceinline__ void head_epilogue(const Params &p, const HeadCtx &hc
     }
     float r;
     const uint8_t sf = nvfp4_scale(gmax, has_gs, gs_inv, r);
+    if constexpr (QPG == 4) {  // the group's 16 codes: 8 contiguous bytes, one store
+      const int d = d0 + 4 * q0;
+      uint32_t w[4];
 #pragma unroll
-    for (int q = 0; q < QPG; ++q) {
-      const int d = d0 + 4 * (q0 + q);
-      const uint16_t w = nvfp4_quad(&v[4 * (q0 + q)], r);
-      *reinterpret_cast<uint16_t *>(slot_base + t * 64 + (d >> 6) * 32 + ((d & 63) >> 1)) = w;
+      for (int q = 0; q < 4; ++q) w[q] = nvfp4_quad(&v[4 * (q0 + q)], r);
+      *reinterpret_cast<uint2 *>(slot_base + t * 64 + (d >> 6) * 32 + ((d & 63) >> 1)) =
+          make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+    } else {
+#pragma unroll
+      for (int q = 0; q < QPG; ++q) {
+        const int d = d0 + 4 * (q0 + q);
+        const uint16_t w = nvfp4_quad(&v[4 * (q0 + q)], r);
+        *reinterpret_cast<uint16_t *>(slot_base + t * 64 + (d >> 6) * 32 + ((d & 63) >> 1)) = w;
+      }
     }
     const int dg = d0 + 4 * q0;  // first dim of the group part held here
     if ((dg & 15) == 0) {
