@@ -107,9 +107,12 @@ enum pa_flags {
   PA_FLAG_NO_PDL = 1 << 3,          /* launch without programmatic dependent launch */
   PA_FLAG_GEMM_SINGLE = 1 << 4,     /* testing: tensor-core path on single CTAs (128 x 128 tiles) */
   PA_FLAG_GEMM_PAIR = 1 << 5,       /* testing: tensor-core path on CTA pairs (256 x 256 tiles) */
-  PA_FLAG_FUSE = 1 << 6             /* skinny path in one kernel (the row normalisation inside the
+  PA_FLAG_FUSE = 1 << 6,            /* skinny path in one kernel (the row normalisation inside the
                                        GEMV's clusters) where the shape allows; measured slower than
                                        prologue + GEMV at the decode shape, so not the default */
+  PA_FLAG_EXACT_NORM = 1 << 7       /* testing: the many-row prologue computes every activation code
+                                       from the exact normalised value (the fast path's fallback);
+                                       results are bitwise the same as without it */
 };
 
 /* ----------------------------------------------------------- config */

@@ -26,7 +26,7 @@ PA_DEV_SLOT_RANGE, PA_DEV_POS_RANGE, PA_DEV_WAIT_TIMEOUT = 1, 2, 4
 PA_WEIGHT_FP8_PER_CHANNEL, PA_WEIGHT_MXFP8 = 0, 1
 PA_CACHE_FP8, PA_CACHE_NVFP4 = 0, 1
 PA_FLAG_STATIC_KV_SCALE, PA_FLAG_FORCE_GEMV, PA_FLAG_FORCE_GEMM, PA_FLAG_NO_PDL = 1, 2, 4, 8
-PA_FLAG_GEMM_SINGLE, PA_FLAG_GEMM_PAIR, PA_FLAG_FUSE = 16, 32, 64
+PA_FLAG_GEMM_SINGLE, PA_FLAG_GEMM_PAIR, PA_FLAG_FUSE, PA_FLAG_EXACT_NORM = 16, 32, 64, 128
 PA_PATH_GEMV, PA_PATH_GEMM_SINGLE, PA_PATH_GEMM_PAIR, PA_PATH_GEMV_FUSED = 0, 1, 2, 3
 
 _vp = ctypes.c_void_p

@@ -288,6 +288,7 @@ int pre_attn_run(pa_handle *h, int M, const pa_step_inputs *in, const pa_weights
   p.bs = c.block_size;
   p.kps = c.kv_page_stride;
   p.static_kv = (c.flags & PA_FLAG_STATIC_KV_SCALE) ? 1 : 0;
+  p.exact_norm = (c.flags & PA_FLAG_EXACT_NORM) ? 1 : 0;
   p.eps = c.eps;
   p.ar = static_cast<const __nv_bfloat16 *>(in->ar);
   p.res = static_cast<const __nv_bfloat16 *>(in->res);

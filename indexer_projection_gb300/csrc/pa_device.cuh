@@ -33,6 +33,7 @@ struct Params {
   int bs;                // tokens per page
   int kps;               // FP8 page16_of stride (8 = identity)
   int static_kv;         // FP8 caches: K / V scale fixed at 1
+  int exact_norm;        // testing: the prologue's exact path for every element
   float eps;
   // inputs
   const __nv_bfloat16 *ar, *res, *g_in;

@@ -188,6 +188,39 @@ __device__ __forceinline__ float amax8(const float (&n)[8]) {
   return a;
 }
 
+// ------------------------------------------------ fast path with a check
+// The exact n above costs ~17 instructions an element, the true divide of
+// the per-channel quantiser ~10 more: at the tensor-core path's thousands of
+// rows that makes the prologue instruction-bound.  Only the FP8 codes and
+// the scales leave the prologue, so it first computes them from a cheap n
+// (t = RN(RN(acc * f) * RN(1 + gamma)), f = RN(rh + rl): within 4 * 2^-24 of
+// n, relative) and keeps a result only where every value within a relative
+// kSafe of it gives the same code (or scale); there the exact n must give it
+// too.  Elsewhere (about one element in 2^16) it recomputes exactly.
+constexpr float kSafe = 0x1p-20f;  // > 4 * 2^-24 (t) + 2 * 2^-24 (the reciprocal of s)
+
+__device__ __forceinline__ void napprox8(const float (&acc)[8], uint4 gw4, float f, float (&t)[8]) {
+  const uint32_t gw[4] = {gw4.x, gw4.y, gw4.z, gw4.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float g1 = __fadd_rn(1.0f, bf16_to_f32(i & 1 ? gw[i >> 1] >> 16 : gw[i >> 1] & 0xffff));
+    t[i] = __fmul_rn(__fmul_rn(acc[i], f), g1);
+  }
+}
+// e4m3 codes of 8 values q = t * k, and whether each code is the same for
+// every value within a relative kSafe of q.
+__device__ __forceinline__ bool codes8_checked(const float (&t)[8], float k, uint2 &w) {
+  float q[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) q[i] = __fmul_rn(t[i], k);
+  const float lo = 1.0f - kSafe, hi = 1.0f + kSafe;
+  w.x = e4m3x4(q[0], q[1], q[2], q[3]);
+  w.y = e4m3x4(q[4], q[5], q[6], q[7]);
+  const uint32_t l0 = e4m3x4(q[0] * lo, q[1] * lo, q[2] * lo, q[3] * lo), l1 = e4m3x4(q[4] * lo, q[5] * lo, q[6] * lo, q[7] * lo);
+  const uint32_t h0 = e4m3x4(q[0] * hi, q[1] * hi, q[2] * hi, q[3] * hi), h1 = e4m3x4(q[4] * hi, q[5] * hi, q[6] * hi, q[7] * hi);
+  return (w.x == l0) & (w.x == h0) & (w.y == l1) & (w.y == h1);
+}
+
 // Normalise and quantise token row m with the NTHR threads of the block
 // (every thread must call it).  Chunks of 8 elements: thread tid holds chunks
 // tid + NTHR * j, j < MAXC, so H <= 8 * NTHR * MAXC; NTHR % 4 == 0 keeps the
@@ -220,23 +253,53 @@ __device__ __forceinline__ void norm_quant_row(const Params &p, const int m, flo
   }
   float rh, rl;
   block_rstd_dd<NTHR>(ss, ss_lo, red2, H, p.eps, rh, rl);
-  float amax = 0.f;
-#pragma unroll
-  for (int j = 0; j < MAXC; ++j) {
-    const int c = tid + NTHR * j;
-    if (c < nch) {
-      norm8(acc[j], gpre[j], rh, rl);
-      amax = fmaxf(amax, amax8(acc[j]));
-    }
-  }
+  const float f = __fadd_rn(rh, rl);
   uint2 *xq = reinterpret_cast<uint2 *>(p.xq + (int64_t)m * H);
   if (WFMT == 0) {
-    const float tmax = block_max<NTHR>(amax, red);
-    const float s = tmax == 0.f ? 1.0f : __fdiv_rn(tmax, kFp8Max);
+    // the scale s = amax(n) / 448, from the approximate amax where every
+    // amax within kSafe of it gives the same s, else from the exact n
+    float amax = 0.f;
 #pragma unroll
     for (int j = 0; j < MAXC; ++j) {
       const int c = tid + NTHR * j;
-      if (c < nch) xq[c] = quant8_ptpc(acc[j], s);
+      if (c < nch) {
+        float t[8];
+        napprox8(acc[j], gpre[j], f, t);
+        amax = fmaxf(amax, amax8(t));
+      }
+    }
+    float tmax = block_max<NTHR>(amax, red);
+    const float s_lo = __fdiv_rn(tmax * (1.0f - kSafe), kFp8Max), s_hi = __fdiv_rn(tmax * (1.0f + kSafe), kFp8Max);
+    if (tmax != 0.f && (s_lo != s_hi || p.exact_norm)) {  // block-uniform: the rare exact amax
+      amax = 0.f;
+#pragma unroll
+      for (int j = 0; j < MAXC; ++j) {
+        const int c = tid + NTHR * j;
+        if (c < nch) {
+          float n[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) n[i] = acc[j][i];
+          norm8(n, gpre[j], rh, rl);
+          amax = fmaxf(amax, amax8(n));
+        }
+      }
+      tmax = block_max<NTHR>(amax, red);
+    }
+    const float s = tmax == 0.f ? 1.0f : __fdiv_rn(tmax, kFp8Max);
+    const float rs = __frcp_rn(s);
+#pragma unroll
+    for (int j = 0; j < MAXC; ++j) {
+      const int c = tid + NTHR * j;
+      if (c < nch) {
+        float t[8];
+        napprox8(acc[j], gpre[j], f, t);
+        uint2 w;
+        if (!codes8_checked(t, rs, w) || p.exact_norm) {  // near a code boundary: exact n and a true divide
+          norm8(acc[j], gpre[j], rh, rl);
+          w = quant8_ptpc(acc[j], s);
+        }
+        xq[c] = w;
+      }
     }
     if (tid == 0) p.x_scale[m] = s;
   } else {
@@ -245,12 +308,35 @@ __device__ __forceinline__ void norm_quant_row(const Params &p, const int m, flo
     for (int j = 0; j < MAXC; ++j) {
       const int c = tid + NTHR * j;
       if (j * NTHR < nch) {  // warp-uniform: every lane reaches the shuffles
-        float bm = c < nch ? amax8(acc[j]) : 0.f;
+        float t[8];
+        float bm = 0.f;
+        if (c < nch) {
+          napprox8(acc[j], gpre[j], f, t);
+          bm = amax8(t);
+        }
         bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
         bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+        // the exponent is exact where every amax within kSafe gives it
+        const bool e_ok = mx_exponent(bm * (1.0f - kSafe)) == mx_exponent(bm * (1.0f + kSafe)) && !p.exact_norm;
+        const bool exact = __any_sync(0xffffffffu, !e_ok);  // warp-uniform
+        if (exact) {  // rare: this warp's blocks from the exact n (acc[j] becomes n)
+          if (c < nch) {
+            norm8(acc[j], gpre[j], rh, rl);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) t[i] = acc[j][i];
+          }
+          bm = c < nch ? amax8(t) : 0.f;
+          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+        }
         if (c < nch) {
           const int e = mx_exponent(bm);
-          xq[c] = quant8_mx(acc[j], pow2_neg(e));
+          uint2 w;
+          if (!codes8_checked(t, pow2_neg(e), w) || p.exact_norm) {  // near a code boundary: from the exact n
+            if (!exact) norm8(acc[j], gpre[j], rh, rl);
+            w = quant8_mx(acc[j], pow2_neg(e));
+          }
+          xq[c] = w;
           if ((c & 3) == 0) p.xsf[sf128x4_offset(m, c >> 2, ksf)] = (uint8_t)(e + 127);
         }
       }

@@ -110,3 +110,22 @@ def test_path_choice():
     assert path(8192, B.PA_FLAG_GEMM_SINGLE) == B.PA_PATH_GEMM_SINGLE
     assert path(64, B.PA_FLAG_GEMM_PAIR) == B.PA_PATH_GEMM_PAIR
     assert path(17) in (B.PA_PATH_GEMM_SINGLE, B.PA_PATH_GEMM_PAIR)
+
+
+@pytest.mark.parametrize("fmt", ["ptpc", "mx"])
+def test_prologue_fast_path_is_bitwise_the_exact_path(fmt):
+    # the many-row prologue quantises from a cheap normalised value where
+    # every value within 2^-20 of it gives the same code and scale, and from
+    # the exact one elsewhere: forcing the exact path everywhere must change
+    # no output bit (outlier rows push many values near code boundaries)
+    from indexer_projection_gb300 import binding as B
+    wl = small("fastpath", 2048, fmt=fmt, H=6144, nkv=1, seed=71, outlier_frac=0.05)
+    st = workloads.host_state(wl)
+    outs = []
+    for extra in (0, B.PA_FLAG_EXACT_NORM):
+        g = harness.GpuRun(wl, st, flags=_flags() | extra)
+        g.run()
+        outs.append(g.results())
+        assert g.runner.device_status() == 0
+    for k in outs[0]:
+        assert np.array_equal(outs[0][k], outs[1][k]), k
