@@ -66,10 +66,15 @@ constexpr int kWChunkBytes = kHeadDim * kChunk;  // 16 KB: 128 rows x 128 B
 constexpr int kXChunkBytes = 16 * kChunk;        // 2 KB: 16 token rows x 128 B
 constexpr int kSfAtom = 512;       // F8_128x4: 128 rows x 4 K-blocks
 constexpr int kMaxTok = 16;
-// One 16-column accumulator per staged chunk (independent MMA chains that
-// the tensor core can overlap; summed when read back), scale factors after.
-constexpr int kTmemCols = 64;
+// Tensor memory (128 columns).  Weights read from shared memory: one
+// 16-column accumulator per staged chunk (independent MMA chains, summed when
+// read back), scale factors after them.  Per-channel weights of a K range
+// that fits one batch are first copied into tensor memory (before the wait
+// on the prologue), so the MMAs after it read only the activations from
+// shared memory: two accumulators, then the 12 x 8 columns of A.
+constexpr int kTmemCols = 128;
 constexpr int kSfaCol = 16 * kStageChunks, kSfbCol = kSfaCol + 4;
+constexpr int kTaCol = 32;           // A in tensor memory: column kTaCol + 8q for MMA q
 constexpr uint32_t kIdescF8 = idesc_f8(128, 16);
 constexpr uint32_t kIdescMx = idesc_mx(128, 16);
 constexpr int kFusedMaxKc = 384;   // fused variant: 3 chunks of 8 elements a thread
@@ -317,6 +322,19 @@ __global__ void __launch_bounds__(kGvThreads, 3) gemv_kernel(Params p, int kc, i
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ss.tmem;
+  // per-channel weights of a single batch: into tensor memory while the
+  // prologue runs (the copies complete before the MMAs issued after them)
+  const bool a_tmem = WFMT == 0 && nch > 0 && nch <= kStageChunks;
+  if (a_tmem) {
+    cp_async_wait<0>();  // this thread's weight copies
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (warp == 4 && lane == 0) {
+      tc_fence_after();
+      for (int q = 0; q < 4 * nch; ++q)
+        tc_cp_128x256b(tmem + kTaCol + 8 * q, sdesc_sw128(smem_u32(w_s + (q >> 2) * kWChunkBytes)) + 2 * (q & 3));
+    }
+  }
   if (use_pdl) {
     pdl_trigger();
     pdl_wait();
@@ -366,7 +384,13 @@ __global__ void __launch_bounds__(kGvThreads, 3) gemv_kernel(Params p, int kc, i
       fence_proxy_async_smem();
       __syncthreads();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == 4 && lane == 0 && a_tmem) {
+      tc_fence_after();
+      for (int q = 0; q < 4 * nch; ++q)  // two accumulator chains
+        mma_f8_ta(tmem + 16 * (q & 1), tmem + kTaCol + 8 * q,
+                  sdesc_sw128(smem_u32(x_s + (q >> 2) * kXChunkBytes)) + 2 * (q & 3), kIdescF8, q >= 2);
+      tc_commit(&ss.mma_bar);
+    } else if (warp == 4 && lane == 0) {
       tc_fence_after();
       const int n = nch - c0 < kStageChunks ? nch - c0 : kStageChunks;
       for (int j = 0; j < n; ++j) {
@@ -402,7 +426,7 @@ __global__ void __launch_bounds__(kGvThreads, 3) gemv_kernel(Params p, int kc, i
     if (ss.ok) {
 #pragma unroll
       for (int j = 0; j < kStageChunks; ++j) {
-        if (j < nch) {  // accumulator j holds chunks j, j + 3, ...
+        if (j < (a_tmem ? (nch > 0 ? 2 : 0) : nch)) {  // smem path: accumulator j holds chunks j, j + 3, ...
           float u[16];
           tc_ld16(tmem + ((uint32_t)(warp * 32) << 16) + 16 * j, u);
           tc_wait_ld();
