@@ -81,9 +81,11 @@ def step_flops(wl) -> int:
     return 2 * wl.M * wl.N * wl.H
 
 
-KERNEL_SOURCES = {"gemv": ("pa_gemv.cu", "pa_device.cuh"), "gemv_fused": ("pa_gemv.cu", "pa_norm.cuh", "pa_device.cuh"), "gemm": ("pa_gemm.cu", "pa_device.cuh"),
+KERNEL_SOURCES = {"gemv": ("pa_gemv.cu", "pa_device.cuh", "pa_tc.cuh", "pa_norm.cuh"),
+                  "gemv_fused": ("pa_gemv.cu", "pa_device.cuh", "pa_tc.cuh", "pa_norm.cuh"),
+                  "gemm": ("pa_gemm.cu", "pa_device.cuh", "pa_tc.cuh"),
                   "gemm2": ("pa_gemm2.cu", "pa_device.cuh"),
-                  "prologue": ("pa_prologue.cu", "pa_device.cuh")}
+                  "prologue": ("pa_prologue.cu", "pa_device.cuh", "pa_norm.cuh")}
 
 
 def kernel_sha(kernel: str) -> str:
