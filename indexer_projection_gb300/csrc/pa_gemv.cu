@@ -424,15 +424,22 @@ __global__ void __launch_bounds__(kGvThreads, 3) gemv_kernel(Params p, int kc, i
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = 0.f;
     if (ss.ok) {
+      // the accumulators used (smem path: accumulator j holds chunks j, j + 3,
+      // ...; tensor-memory A: two chains); two loads in flight per wait
+      const int nacc = a_tmem ? (nch > 0 ? 2 : 0) : (nch < kStageChunks ? nch : kStageChunks);
+      const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+      float u[16];
+      if (nacc > 0) tc_ld16(trow, v);
+      if (nacc > 1) tc_ld16(trow + 16, u);
+      tc_wait_ld();
+      if (nacc > 1)
 #pragma unroll
-      for (int j = 0; j < kStageChunks; ++j) {
-        if (j < (a_tmem ? (nch > 0 ? 2 : 0) : nch)) {  // smem path: accumulator j holds chunks j, j + 3, ...
-          float u[16];
-          tc_ld16(tmem + ((uint32_t)(warp * 32) << 16) + 16 * j, u);
-          tc_wait_ld();
+        for (int i = 0; i < 16; ++i) v[i] += u[i];
+      if (nacc > 2) {
+        tc_ld16(trow + 32, u);
+        tc_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] += u[i];
-        }
+        for (int i = 0; i < 16; ++i) v[i] += u[i];
       }
     }
   }
