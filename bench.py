@@ -181,6 +181,25 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sel)}
 
 
+# ------------------------------------------------------------ several ranks
+
+def max_over_ranks(values, world: int, device=None):
+    """Element-wise max of `values` over the ranks (the slowest rank's times);
+    the input itself when there is one rank."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def tokens_per_second(world: int, rows_per_step: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank processes its own rows each step."""
+    return world * rows_per_step / (ms_per_step * 1e-3)
+
+
 # ----------------------------------------------------------------- our arm
 
 class DeviceWorkload:
@@ -319,11 +338,7 @@ def run_ours(args, wl, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     t_wall1 = time.time()
     barrier()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        tm = torch.tensor([ms], device=dev)
-        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
-        ms = float(tm.item())
+    ms = max_over_ranks([e0.elapsed_time(e1)], world, dev)[0]
     sampler.stop()
     clocks = sampler.summary(t_wall0, t_wall1)
     del graphs
@@ -404,13 +419,10 @@ def run_ours(args, wl, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     e2e_ms = a.elapsed_time(b) / E
     del ge
-    if world > 1:
-        tm = torch.tensor([e2e_ms, e2e_eager_ms], device=dev)
-        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
-        e2e_ms, e2e_eager_ms = float(tm[0].item()), float(tm[1].item())
+    e2e_ms, e2e_eager_ms = max_over_ranks([e2e_ms, e2e_eager_ms], world, dev)
 
     ms_step = ms / K
-    tokens_s = world * wl.M / (ms_step * 1e-3)
+    tokens_s = tokens_per_second(world, wl.M, ms_step)
     nb = step_bytes(wl)
     path = B.pre_attn_path(dw.runner.handle, wl.M)
     gemm = path in (B.PA_PATH_GEMM_SINGLE, B.PA_PATH_GEMM_PAIR)
@@ -448,11 +460,11 @@ def run_ours(args, wl, rank, world, local_rank):
         "roofline": roof,
         "step_hbm_frac": round(step_roof, 4),
         "gpu_launches": launches_per_step * K,
-        "e2e": {"value": round(world * wl.M / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(tokens_per_second(world, wl.M, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E,
                 "how": "pinned host inputs -> device, pre_attn_run, outputs -> pinned host, every step; "
                        "the step's API calls captured in a CUDA graph",
-                "eager_value": round(world * wl.M / (e2e_eager_ms * 1e-3), 1)},
+                "eager_value": round(tokens_per_second(world, wl.M, e2e_eager_ms), 1)},
         "clocks": clocks,
     }
     if gemm:
