@@ -105,6 +105,10 @@ __device__ __forceinline__ void named_bar_sync(int id, int n) {
 }
 
 __device__ __forceinline__ int64_t ld_i64(const int64_t *p) { return __ldg(p); }
+// A hint that brings the line into L2 (and its translation into the TLBs).
+// It orders nothing and changes no value a later load returns, so it may be
+// issued for an input before the wait on the kernel that produces it.
+__device__ __forceinline__ void prefetch_l2(const void *p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 __device__ __forceinline__ int ld_acquire(const int *p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -414,7 +418,9 @@ __device__ __forceinline__ int64_t load_pos(const Params &p, int m) {
 //   index_q norm + rope -> bf16 and / or e4m3(z)
 //   index_k norm + rope -> FP8: e4m3(bf16(z)) in the index cache; NVFP4 unit scale
 // A slot < 0 skips that cache; a slot beyond the cache skips it and flags.
-template <int E>
+// CF: the cache format when known at compile time (0 FP8, 1 NVFP4; the other
+// format's code is then left out of the kernel), else -1 (p.cache_fmt).
+template <int E, int CF = -1>
 __device__ __forceinline__ void head_epilogue(const Params &p, const HeadCtx &hc, float (&v)[E], int d0) {
   const int h = hc.head;
   const bool is_q = h < p.k0, is_k = h >= p.k0 && h < p.v0, is_v = h >= p.v0 && h < p.iq0;
@@ -469,7 +475,7 @@ __device__ __forceinline__ void head_epilogue(const Params &p, const HeadCtx &hc
   const bool is_ik = !is_k && !is_v;
   const int64_t slot = is_ik ? hc.islot : hc.slot;
   if (slot < 0) return;
-  if (p.cache_fmt == 0) {
+  if ((CF >= 0 ? CF : p.cache_fmt) == 0) {
     // ---------------------------------------------------------- FP8 caches
     if (is_ik) {
       if (slot >= p.num_index_slots) {

@@ -39,13 +39,15 @@
 // prologue's work, so the decode step is one launch.  The 16 threads of
 // token group m of every CTA add ar + res over the CTA's K range (the
 // residual is written by head 0's cluster), reduce sum(acc^2) as a
-// double-float and exchange the 16 K-range partials across the cluster
-// (st.async, byte-counted); every CTA then sums them in the same order, so
-// all agree bit for bit on rstd.  The correctly rounded n (pa_norm.cuh) and,
-// for the per-channel format, a second exchange of the K-range amax give the
-// FP8 codes, written straight into the MMA's B operand (and the MXFP8 scale
-// atoms into their tcgen05.cp source): nothing goes through global memory
-// between the inputs and the outputs.
+// double-float, and for the per-channel format the maximum of |acc (1 +
+// gam)| (the row's amax before the factor rstd), and exchange the 16 K-range
+// partials across the cluster in one st.async each (byte-counted); every CTA
+// then combines them in the same order, so all agree bit for bit on rstd and
+// the scale.  The correctly rounded n (pa_norm.cuh) gives the FP8 codes,
+// written straight into the MMA's B operand (and the MXFP8 scale atoms into
+// their tcgen05.cp source): nothing goes through global memory between the
+// inputs and the outputs.  The rows' inputs are prefetched into L2 before
+// the wait (a hint: the loads after it still see the producer's writes).
 //
 // The weight, its scales, the head's gamma and w_scale are read before the
 // wait on the previous kernel: they must not be written by work still in
@@ -86,8 +88,7 @@ struct GvLayout {
   int sfa;   // MXFP8 [kStageChunks] weight scale atoms
   int sfb;   // MXFP8 [nchunks] activation scale atoms
   int recv;  // [TS][C][128] f32 partial rows received from the cluster
-  int ex1;   // fused: [16 K ranges][16 tokens] float2 sum(acc^2) partials
-  int ex2;   // fused: [16 K ranges][16 tokens] f32 amax partials
+  int ex1;   // fused: [16 K ranges][16 tokens] float4 partials: sum(acc^2), max |acc (1 + gam)|
   int gin;   // fused: the K range's input-norm gamma (bf16)
   int total;
 };
@@ -101,8 +102,7 @@ __host__ __device__ inline GvLayout gv_layout(int C, int kc, int mx) {
   L.sfb = L.sfa + (mx ? kStageChunks * kSfAtom : 0);
   L.recv = L.sfb + (mx ? nch * kSfAtom : 0);
   L.ex1 = L.recv + ts * C * kHeadDim * 4;
-  L.ex2 = L.ex1 + 16 * kMaxTok * 8;
-  L.gin = L.ex2 + 16 * kMaxTok * 4;
+  L.gin = L.ex1 + 16 * kMaxTok * 16;
   L.total = L.gin + kc * 2;
   return L;
 }
@@ -116,7 +116,7 @@ struct GvStatic {
   int64_t slot[2], islot[2];
   uint64_t mma_bar;              // the MMAs of a batch have completed
   uint64_t recv_bar;             // partial rows received (transaction bytes)
-  uint64_t ex1_bar, ex2_bar;     // fused: the cluster's norm partials received
+  uint64_t ex1_bar;              // fused: the cluster's norm partials received
   uint32_t tmem;
   int ok;
 };
@@ -136,16 +136,15 @@ __device__ __forceinline__ void st_async_b32(uint32_t caddr, float v, uint32_t c
 // of the cluster; leaves the per-token scales in xs (per-channel format).
 template <int WFMT>
 __device__ __forceinline__ void fused_norm_quant(const Params &p, int tid, int ks, int k0, int k1, int h,
-                                                 uint8_t *x_s, uint8_t *sfb_s, float2 *ex1, float *ex2,
-                                                 const uint4 *gin_s, float *xs, uint64_t *ex1_bar,
-                                                 uint64_t *ex2_bar) {
+                                                 uint8_t *x_s, uint8_t *sfb_s, float4 *ex1, const uint4 *gin_s,
+                                                 float *xs, uint64_t *ex1_bar) {
   constexpr int kJ = kFusedMaxKc / 8 / 16;  // chunks a thread
   const int M = p.M, K = p.H;
   const int m = tid >> 4, sub = tid & 15;
   const int cpt = (k1 - k0) / 8;  // chunks of 8 elements a token in the range
   const bool active = m < M;
   float acc[kJ][8];
-  float sh = 0.f, sl = 0.f;
+  float sh = 0.f, sl = 0.f, mh = 0.f, ml = 0.f;
   if (active) {
     const uint4 *ar = reinterpret_cast<const uint4 *>(p.ar + (int64_t)m * K + k0);
     const uint4 *res = reinterpret_cast<const uint4 *>(p.res + (int64_t)m * K + k0);
@@ -157,27 +156,34 @@ __device__ __forceinline__ void fused_norm_quant(const Params &p, int tid, int k
         uint4 rb;
         acc8(__ldcs(ar + c), __ldcs(res + c), acc[j], rb, sh, sl);
         if (rout) __stcs(rout + c, rb);
+        if (WFMT == 0) absprod_max8(acc[j], gin_s[c], mh, ml);
       }
     }
   }
-  // the token's sum over this K range, in all 16 lanes of the group
+  // the token's partials over this K range, in all 16 lanes of the group
 #pragma unroll
   for (int o = 8; o > 0; o >>= 1) {
     const float oh = __shfl_xor_sync(0xffffffffu, sh, o), ol = __shfl_xor_sync(0xffffffffu, sl, o);
     dd_add(sh, sl, oh, ol);
+    if (WFMT == 0) {
+      const float qh = __shfl_xor_sync(0xffffffffu, mh, o), ql = __shfl_xor_sync(0xffffffffu, ml, o);
+      pair_max(mh, ml, qh, ql);
+    }
   }
   cluster_wait();  // every CTA of the cluster has initialised its barriers
-  // lane sub of token m's group sends this range's partial to cluster CTA sub
+  // lane sub of token m's group sends this range's partials to cluster CTA sub
   if (active) {
-    float2 *dst = ex1 + ks * kMaxTok + m;
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
-                     mapa(smem_u32(dst), sub)),
-                 "f"(sh), "f"(sl), "r"(mapa(smem_u32(ex1_bar), sub))
-                 : "memory");
+    float4 *dst = ex1 + ks * kMaxTok + m;
+    if (WFMT == 0)
+      st_async_v4(mapa(smem_u32(dst), sub), make_float4(sh, sl, mh, ml), mapa(smem_u32(ex1_bar), sub));
+    else
+      asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+                       mapa(smem_u32(dst), sub)),
+                   "f"(sh), "f"(sl), "r"(mapa(smem_u32(ex1_bar), sub))
+                   : "memory");
   }
   const bool ok1 = mbar_wait_cluster(ex1_bar, 0, p.status);
   float rh = 0.f, rl = 0.f;
-  float amax = 0.f;
   if (active && ok1) {
     float th = ex1[m].x, tl = ex1[m].y;  // the 16 K ranges in order: the same sum in every CTA
 #pragma unroll
@@ -186,10 +192,7 @@ __device__ __forceinline__ void fused_norm_quant(const Params &p, int tid, int k
 #pragma unroll
     for (int j = 0; j < kJ; ++j) {
       const int c = sub + 16 * j;
-      if (c < cpt) {
-        norm8(acc[j], gin_s[c], rh, rl);
-        amax = fmaxf(amax, amax8(acc[j]));
-      }
+      if (c < cpt) norm8(acc[j], gin_s[c], rh, rl);
     }
   }
   // quantise into the B operand: chunk c of token m is K bytes 8c .. 8c + 7 of
@@ -198,20 +201,11 @@ __device__ __forceinline__ void fused_norm_quant(const Params &p, int tid, int k
     *reinterpret_cast<uint2 *>(x_s + (c >> 4) * kXChunkBytes + swz(m, (c & 15) >> 1) + 8 * (c & 1)) = w;
   };
   if (WFMT == 0) {
+    if (active && ok1) {
+      float qh = ex1[m].z, ql = ex1[m].w;
 #pragma unroll
-    for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    if (active) {
-      float *dst = ex2 + ks * kMaxTok + m;
-      asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
-                       mapa(smem_u32(dst), sub)),
-                   "r"(__float_as_uint(amax)), "r"(mapa(smem_u32(ex2_bar), sub))
-                   : "memory");
-    }
-    const bool ok2 = mbar_wait_cluster(ex2_bar, 0, p.status);
-    if (active && ok1 && ok2) {
-      float tmax = 0.f;
-#pragma unroll
-      for (int q = 0; q < 16; ++q) tmax = fmaxf(tmax, ex2[q * kMaxTok + m]);
+      for (int q = 1; q < 16; ++q) pair_max(qh, ql, ex1[q * kMaxTok + m].z, ex1[q * kMaxTok + m].w);
+      const float tmax = amax_from_pair(qh, ql, rh, rl);
       const float s = tmax == 0.f ? 1.0f : __fdiv_rn(tmax, kFp8Max);
 #pragma unroll
       for (int j = 0; j < kJ; ++j) {
@@ -238,7 +232,7 @@ __device__ __forceinline__ void fused_norm_quant(const Params &p, int tid, int k
   }
 }
 
-template <int WFMT, int C, bool FUSED>
+template <int WFMT, int C, bool FUSED, int CF>
 __global__ void __launch_bounds__(kGvThreads, 3) gemv_kernel(Params p, int kc, int use_pdl) {
   static_assert(!FUSED || C == 16, "the fused variant exchanges norm partials among 16 K ranges");
   constexpr int TS = (kMaxTok + C - 1) / C;
@@ -248,8 +242,7 @@ __global__ void __launch_bounds__(kGvThreads, 3) gemv_kernel(Params p, int kc, i
   const GvLayout L = gv_layout(C, kc, WFMT);
   uint8_t *w_s = dsm + L.w, *x_s = dsm + L.x, *sfa_s = dsm + L.sfa, *sfb_s = dsm + L.sfb;
   float *recv = reinterpret_cast<float *>(dsm + L.recv);
-  float2 *ex1 = reinterpret_cast<float2 *>(dsm + L.ex1);
-  float *ex2 = reinterpret_cast<float *>(dsm + L.ex2);
+  float4 *ex1 = reinterpret_cast<float4 *>(dsm + L.ex1);
   uint4 *gin_s = reinterpret_cast<uint4 *>(dsm + L.gin);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -258,7 +251,6 @@ __global__ void __launch_bounds__(kGvThreads, 3) gemv_kernel(Params p, int kc, i
   const int h = blockIdx.x / C;
   const int k0 = ks * kc, k1 = k0 + kc < K ? k0 + kc : K;
   const int nch = k1 > k0 ? (k1 - k0) / kChunk : 0;
-  const uint8_t *wrow = p.w + (int64_t)h * kHeadDim * K + k0;  // row 0 of the head, this range
 
   if (tid == 0) {
     int ntok = 0;  // tokens rank + C * j < M finished here; 512 bytes from each CTA for each
@@ -267,12 +259,9 @@ __global__ void __launch_bounds__(kGvThreads, 3) gemv_kernel(Params p, int kc, i
     mbar_init(&ss.recv_bar, 1);
     if (ntok) mbar_expect_tx(&ss.recv_bar, (uint32_t)(ntok * C * kHeadDim * 4));
     else mbar_arrive(&ss.recv_bar);
-    if (FUSED) {  // every CTA sends 8 (then 4) bytes per token to every CTA
+    if (FUSED) {  // every CTA sends 16 (MXFP8: 8) bytes per token to every CTA
       mbar_init(&ss.ex1_bar, 1);
-      mbar_expect_tx(&ss.ex1_bar, (uint32_t)(16 * M * 8));
-      mbar_init(&ss.ex2_bar, 1);
-      if (WFMT == 0) mbar_expect_tx(&ss.ex2_bar, (uint32_t)(16 * M * 4));
-      else mbar_arrive(&ss.ex2_bar);
+      mbar_expect_tx(&ss.ex1_bar, (uint32_t)(16 * M * (WFMT == 0 ? 16 : 8)));
     }
     ss.ok = 1;
     fence_mbar_init();
@@ -281,6 +270,7 @@ __global__ void __launch_bounds__(kGvThreads, 3) gemv_kernel(Params p, int kc, i
   cluster_arrive_relaxed();  // matched by cluster_wait() before the first remote store
 
   // ------------------------------- the weight stream (batch 0), before the wait
+  const uint8_t *wrow = p.w + (int64_t)h * kHeadDim * K + k0;  // row 0 of the head, this range
   auto issue_weights = [&](int c0) {
     const int n = nch - c0 < kStageChunks ? nch - c0 : kStageChunks;
     for (int i = tid; i < n * kHeadDim * 8; i += kGvThreads) {
@@ -335,6 +325,16 @@ __global__ void __launch_bounds__(kGvThreads, 3) gemv_kernel(Params p, int kc, i
         tc_cp_128x256b(tmem + kTaCol + 8 * q, sdesc_sw128(smem_u32(w_s + (q >> 2) * kWChunkBytes)) + 2 * (q & 3));
     }
   }
+  if (FUSED && (tid >> 4) < M)  // the rows' inputs over this K range: a hint before the wait
+    for (int c = tid & 15; c < (k1 - k0) / 8; c += 16) {
+      prefetch_l2(p.ar + (int64_t)(tid >> 4) * K + k0 + 8 * c);
+      prefetch_l2(p.res + (int64_t)(tid >> 4) * K + k0 + 8 * c);
+    }
+  if (warp == 7 && lane < TS && ks + C * lane < M) {  // inputs: a hint before the wait
+    prefetch_l2(p.pos + ks + C * lane);
+    prefetch_l2(p.slot + ks + C * lane);
+    prefetch_l2(p.islot + ks + C * lane);
+  }
   if (use_pdl) {
     pdl_trigger();
     pdl_wait();
@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(kGvThreads, 3) gemv_kernel(Params p, int kc, i
     cp_async16(&ss.cs[lane >> 3][8 * (lane & 7)], p.cos_sin + pos * kRotDim + 8 * (lane & 7));
   }
   cp_async_commit();
-  if (FUSED) fused_norm_quant<WFMT>(p, tid, ks, k0, k1, h, x_s, sfb_s, ex1, ex2, gin_s, ss.xs, &ss.ex1_bar, &ss.ex2_bar);
+  if (FUSED) fused_norm_quant<WFMT>(p, tid, ks, k0, k1, h, x_s, sfb_s, ex1, gin_s, ss.xs, &ss.ex1_bar);
   cp_async_wait<1>();  // weights of batch 0 and the activations
   fence_proxy_async_smem();
   __syncthreads();
@@ -443,6 +443,7 @@ __global__ void __launch_bounds__(kGvThreads, 3) gemv_kernel(Params p, int kc, i
       }
     }
   }
+  cp_async_wait<0>();  // the cos / sin rows (their own, last group), read by the epilogue
   tc_fence_before();
   __syncthreads();
   if (warp == 4) {
@@ -487,7 +488,7 @@ __global__ void __launch_bounds__(kGvThreads, 3) gemv_kernel(Params p, int kc, i
   hc.islot = ss.islot[warp];
   hc.cs_row = ss.cs[warp];
   hc.g_q = hc.g_k = hc.g_iq = hc.g_ik = ss.gam;
-  head_epilogue<4>(p, hc, y, d0);
+  head_epilogue<4, CF>(p, hc, y, d0);
 }
 
 namespace {
@@ -509,8 +510,10 @@ int pick_cluster(int smem16) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
   if (cached[dev].c && cached[dev].smem >= smem16) return cached[dev].c;
   int c = 8;
-  const void *k16[2] = {reinterpret_cast<const void *>(gemv_kernel<WFMT, 16, false>),
-                        reinterpret_cast<const void *>(gemv_kernel<WFMT, 16, true>)};
+  const void *k16[4] = {reinterpret_cast<const void *>(gemv_kernel<WFMT, 16, false, 0>),
+                        reinterpret_cast<const void *>(gemv_kernel<WFMT, 16, true, 0>),
+                        reinterpret_cast<const void *>(gemv_kernel<WFMT, 16, false, 1>),
+                        reinterpret_cast<const void *>(gemv_kernel<WFMT, 16, true, 1>)};
   bool failed = false;
   for (const void *k : k16) {
     if (!failed) failed = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess;
@@ -537,11 +540,11 @@ int pick_cluster(int smem16) {
   return c;
 }
 
-template <int WFMT, int C, bool FUSED>
+template <int WFMT, int C, bool FUSED, int CF>
 cudaError_t launch_c(const Params &p, bool pdl, cudaStream_t stream) {
   const int kc = gv_kc(p.H, C);
   const int smem = gv_smem(C, kc, WFMT);
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemv_kernel<WFMT, C, FUSED>), smem);
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemv_kernel<WFMT, C, FUSED, CF>), smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
@@ -557,7 +560,7 @@ cudaError_t launch_c(const Params &p, bool pdl, cudaStream_t stream) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, gemv_kernel<WFMT, C, FUSED>, p, kc, (int)pdl);
+  return cudaLaunchKernelEx(&cfg, gemv_kernel<WFMT, C, FUSED, CF>, p, kc, (int)pdl);
 }
 
 template <int WFMT>
@@ -565,11 +568,11 @@ bool fused_ok(int H) {
   return gv_kc(H, 16) <= kFusedMaxKc && pick_cluster<WFMT>(gv_smem(16, gv_kc(H, 16), WFMT)) == 16;
 }
 
-template <int WFMT>
+template <int WFMT, int CF>
 cudaError_t launch_t(const Params &p, bool fused, bool pdl, cudaStream_t stream) {
-  if (fused) return launch_c<WFMT, 16, true>(p, pdl, stream);
-  if (pick_cluster<WFMT>(gv_smem(16, gv_kc(p.H, 16), WFMT)) == 16) return launch_c<WFMT, 16, false>(p, pdl, stream);
-  return launch_c<WFMT, 8, false>(p, pdl, stream);
+  if (fused) return launch_c<WFMT, 16, true, CF>(p, pdl, stream);
+  if (pick_cluster<WFMT>(gv_smem(16, gv_kc(p.H, 16), WFMT)) == 16) return launch_c<WFMT, 16, false, CF>(p, pdl, stream);
+  return launch_c<WFMT, 8, false, CF>(p, pdl, stream);
 }
 
 }  // namespace
@@ -577,7 +580,9 @@ cudaError_t launch_t(const Params &p, bool fused, bool pdl, cudaStream_t stream)
 bool gemv_fuses_prologue(int H, int weight_fmt) { return weight_fmt == 0 ? fused_ok<0>(H) : fused_ok<1>(H); }
 
 cudaError_t launch_gemv(const Params &p, bool fused, bool pdl, cudaStream_t stream) {
-  return p.weight_fmt == 0 ? launch_t<0>(p, fused, pdl, stream) : launch_t<1>(p, fused, pdl, stream);
+  if (p.cache_fmt == 0)
+    return p.weight_fmt == 0 ? launch_t<0, 0>(p, fused, pdl, stream) : launch_t<1, 0>(p, fused, pdl, stream);
+  return p.weight_fmt == 0 ? launch_t<0, 1>(p, fused, pdl, stream) : launch_t<1, 1>(p, fused, pdl, stream);
 }
 
 }  // namespace pa

@@ -181,6 +181,37 @@ __device__ __forceinline__ uint2 quant8_mx(const float (&n)[8], float inv) {
   w.y = e4m3x4(n[4] * inv, n[5] * inv, n[6] * inv, n[7] * inv);
   return w;
 }
+// The per-channel scale without a second pass over n: n = acc * rstd *
+// (1 + gam) is rounded monotonically and rstd is common to the row, so
+// max |n| is the row's maximum of |acc * (1 + gam)| times rstd, rounded once.
+// The products are kept as pairs hi + lo (hi = RN, relative error ~2^-46) and
+// compared on (hi, lo) in order; amax_from_pair rounds the pair times the
+// rstd pair to f32 like norm8 does.
+__device__ __forceinline__ void pair_max(float &mh, float &ml, float h, float l) {
+  if (h > mh || (h == mh && l > ml)) {
+    mh = h;
+    ml = l;
+  }
+}
+__device__ __forceinline__ void absprod_max8(const float (&acc)[8], uint4 gw4, float &mh, float &ml) {
+  const uint32_t gw[4] = {gw4.x, gw4.y, gw4.z, gw4.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float gam = bf16_to_f32(i & 1 ? gw[i >> 1] >> 16 : gw[i >> 1] & 0xffff);
+    float a1, a2, s1, s2;
+    two_prod(acc[i], gam, a1, a2);
+    two_sum(acc[i], a1, s1, s2);  // acc * (1 + gam) = s1 + s2 + a2
+    const float lo = __fadd_rn(s2, a2);
+    const float h = __fadd_rn(s1, lo);
+    const float l = __fsub_rn(lo, __fsub_rn(h, s1));
+    pair_max(mh, ml, fabsf(h), h < 0.f ? -l : l);
+  }
+}
+__device__ __forceinline__ float amax_from_pair(float mh, float ml, float rh, float rl) {
+  float q, e;
+  two_prod(mh, rh, q, e);
+  return __fadd_rn(q, __fmaf_rn(mh, rl, __fmaf_rn(ml, rh, e)));
+}
 __device__ __forceinline__ float amax8(const float (&n)[8]) {
   float a = 0.f;
 #pragma unroll

@@ -42,19 +42,23 @@ __global__ void __launch_bounds__(NTHR) prologue_kernel(Params p, int use_pdl) {
 // One cluster of C CTAs per token row (blockIdx.x / C); CTA r takes the
 // row's elements [r * kc, (r + 1) * kc), kc a multiple of 32 (one 8-element
 // chunk a thread; the four chunks of an MXFP8 block in lanes 4i .. 4i + 3).
-// The CTAs' double-float partial sums of acc^2, and for the per-channel
-// format the partial amax, are sent to every CTA of the cluster with
-// byte-counted st.async; each CTA combines the C partials in the same order,
-// so all agree bit for bit on rstd and on the scale.
+// Each CTA sends its double-float partial sum of acc^2, and for the
+// per-channel format its partial maximum of |acc * (1 + gam)| (absprod_max8),
+// to every CTA of the cluster in one byte-counted st.async; each CTA combines
+// the C partials in the same order, so all agree bit for bit on rstd and on
+// the scale, and one exchange serves both.
+// The row's inputs are prefetched into L2 before the wait on the producing
+// kernel (a hint: the loads after the wait still see its writes); after the
+// wait CTA 0 of the row prefetches the row's cos / sin line for the GEMV's
+// head epilogue.
 template <int WFMT, int C>
 __global__ void __launch_bounds__(128 * 16 / C) prologue_rows_kernel(Params p, int kc, int use_pdl) {
   constexpr int NTHR = 128 * 16 / C;
   constexpr int W = NTHR / 32;
-  __shared__ float2 ex1[C];          // the C partial sums of acc^2
-  __shared__ float ex2[C];           // the C partial amax (per-channel format)
-  __shared__ float2 wred[W];
-  __shared__ float wmax[W];
-  __shared__ __align__(8) uint64_t bar1, bar2;
+  constexpr int XB = WFMT == 0 ? 16 : 8;  // bytes a CTA sends to each CTA
+  __shared__ float4 ex1[C];               // the C partials: sum of acc^2 (hi, lo), max product (hi, lo)
+  __shared__ float4 wred[W];
+  __shared__ __align__(8) uint64_t bar1;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int m = blockIdx.x / C, r = (int)cta_rank();
   const int H = p.H, ksf = H >> 5;
@@ -63,43 +67,60 @@ __global__ void __launch_bounds__(128 * 16 / C) prologue_rows_kernel(Params p, i
   const bool act = k0 + 8 * tid < k1;
   if (tid == 0) {
     mbar_init(&bar1, 1);
-    mbar_expect_tx(&bar1, C * 8);
-    mbar_init(&bar2, 1);
-    if (WFMT == 0) mbar_expect_tx(&bar2, C * 4);
-    else mbar_arrive(&bar2);
+    mbar_expect_tx(&bar1, C * XB);
     fence_mbar_init();
   }
   cluster_arrive_relaxed();
+  const uint4 *ar = reinterpret_cast<const uint4 *>(p.ar + (int64_t)m * H) + c;
+  const uint4 *res = reinterpret_cast<const uint4 *>(p.res + (int64_t)m * H) + c;
+  const bool cs_thread = r == 0 && tid == 0;
   uint4 gw = make_uint4(0u, 0u, 0u, 0u);
-  if (act) gw = __ldg(reinterpret_cast<const uint4 *>(p.g_in) + c);  // a model constant
+  if (act) {
+    gw = __ldg(reinterpret_cast<const uint4 *>(p.g_in) + c);  // a model constant
+    prefetch_l2(ar);
+    prefetch_l2(res);
+  }
+  if (cs_thread) prefetch_l2(p.pos + m);
   if (use_pdl) {
     pdl_trigger();
     pdl_wait();
   }
+  int64_t cpos = -1;  // loaded now, used last
+  if (cs_thread) cpos = ld_i64(p.pos + m);
   float acc[8];
-  float sh = 0.f, sl = 0.f;
+  float sh = 0.f, sl = 0.f, mh = 0.f, ml = 0.f;
   if (act) {
     uint4 rb;
-    acc8(__ldcs(reinterpret_cast<const uint4 *>(p.ar + (int64_t)m * H) + c),
-         __ldcs(reinterpret_cast<const uint4 *>(p.res + (int64_t)m * H) + c), acc, rb, sh, sl);
+    acc8(__ldcs(ar), __ldcs(res), acc, rb, sh, sl);
     if (p.residual) __stcs(reinterpret_cast<uint4 *>(p.residual + (int64_t)m * H) + c, rb);
+    if (WFMT == 0) absprod_max8(acc, gw, mh, ml);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float oh = __shfl_xor_sync(0xffffffffu, sh, o), ol = __shfl_xor_sync(0xffffffffu, sl, o);
     dd_add(sh, sl, oh, ol);
+    if (WFMT == 0) {
+      const float qh = __shfl_xor_sync(0xffffffffu, mh, o), ql = __shfl_xor_sync(0xffffffffu, ml, o);
+      pair_max(mh, ml, qh, ql);
+    }
   }
-  if (lane == 0) wred[warp] = make_float2(sh, sl);
+  if (lane == 0) wred[warp] = make_float4(sh, sl, mh, ml);
   __syncthreads();
-  cluster_wait();  // every CTA of the cluster has initialised its barriers
-  if (tid < C) {   // the CTA's partial, to CTA tid
-    float th = wred[0].x, tl = wred[0].y;
+  cluster_wait();  // every CTA of the cluster has initialised its barrier
+  if (tid < C) {   // the CTA's partials, to CTA tid
+    float th = wred[0].x, tl = wred[0].y, qh = wred[0].z, ql = wred[0].w;
 #pragma unroll
-    for (int w = 1; w < W; ++w) dd_add(th, tl, wred[w].x, wred[w].y);
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
-                     mapa(smem_u32(&ex1[r]), tid)),
-                 "f"(th), "f"(tl), "r"(mapa(smem_u32(&bar1), tid))
-                 : "memory");
+    for (int w = 1; w < W; ++w) {
+      dd_add(th, tl, wred[w].x, wred[w].y);
+      pair_max(qh, ql, wred[w].z, wred[w].w);
+    }
+    if (WFMT == 0)
+      st_async_v4(mapa(smem_u32(&ex1[r]), tid), make_float4(th, tl, qh, ql), mapa(smem_u32(&bar1), tid));
+    else
+      asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+                       mapa(smem_u32(&ex1[r]), tid)),
+                   "f"(th), "f"(tl), "r"(mapa(smem_u32(&bar1), tid))
+                   : "memory");
   }
   const bool ok1 = mbar_wait_cluster(&bar1, 0, p.status);
   float th = ex1[0].x, tl = ex1[0].y;  // the C partials in order: the same sum in every CTA
@@ -107,35 +128,18 @@ __global__ void __launch_bounds__(128 * 16 / C) prologue_rows_kernel(Params p, i
   for (int q = 1; q < C; ++q) dd_add(th, tl, ex1[q].x, ex1[q].y);
   float rh, rl;
   rstd_from_dd(th, tl, H, p.eps, rh, rl);
-  float amax = 0.f;
-  if (act && ok1) {
-    norm8(acc, gw, rh, rl);
-    amax = amax8(acc);
-  }
+  if (act && ok1) norm8(acc, gw, rh, rl);
   uint2 *xq = reinterpret_cast<uint2 *>(p.xq + (int64_t)m * H);
   if (WFMT == 0) {
+    float qh = ex1[0].z, ql = ex1[0].w;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    if (lane == 0) wmax[warp] = amax;
-    __syncthreads();
-    if (tid < C) {
-      float t = wmax[0];
-#pragma unroll
-      for (int w = 1; w < W; ++w) t = fmaxf(t, wmax[w]);
-      asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
-                       mapa(smem_u32(&ex2[r]), tid)),
-                   "r"(__float_as_uint(t)), "r"(mapa(smem_u32(&bar2), tid))
-                   : "memory");
-    }
-    const bool ok2 = mbar_wait_cluster(&bar2, 0, p.status);
-    float tmax = ex2[0];
-#pragma unroll
-    for (int q = 1; q < C; ++q) tmax = fmaxf(tmax, ex2[q]);
+    for (int q = 1; q < C; ++q) pair_max(qh, ql, ex1[q].z, ex1[q].w);
+    const float tmax = amax_from_pair(qh, ql, rh, rl);
     const float s = tmax == 0.f ? 1.0f : __fdiv_rn(tmax, kFp8Max);
-    if (act && ok1 && ok2) xq[c] = quant8_ptpc(acc, s);
+    if (act && ok1) xq[c] = quant8_ptpc(acc, s);
     if (r == 0 && tid == 0) p.x_scale[m] = s;
   } else {
-    float bm = act ? amax : 0.f;
+    float bm = act ? amax8(acc) : 0.f;
     bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
     bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
     if (act && ok1) {
@@ -144,6 +148,7 @@ __global__ void __launch_bounds__(128 * 16 / C) prologue_rows_kernel(Params p, i
       if ((c & 3) == 0) p.xsf[sf128x4_offset(m, c >> 2, ksf)] = (uint8_t)(e + 127);
     }
   }
+  if (cs_thread && cpos >= 0 && cpos < p.max_pos) prefetch_l2(p.cos_sin + cpos * kRotDim);
 }
 
 __global__ void pack_scales_kernel(const uint8_t *src, uint8_t *dst, int rows, int ksf) {
