@@ -285,6 +285,12 @@ __global__ void __launch_bounds__(kGvThreads, 3) gemv_kernel(Params p, int kc, i
       }
     cp_async_commit();
   };
+  if (FUSED && (tid >> 4) < M)  // the rows' inputs over this K range: a hint before the wait,
+                                // issued ahead of the weight stream
+    for (int c = tid & 15; c < (k1 - k0) / 8; c += 16) {
+      prefetch_l2(p.ar + (int64_t)(tid >> 4) * K + k0 + 8 * c);
+      prefetch_l2(p.res + (int64_t)(tid >> 4) * K + k0 + 8 * c);
+    }
   if (FUSED) {  // the K range's input-norm gamma (a model constant), its own group
     for (int i = tid; i < (k1 - k0) / 8; i += kGvThreads) cp_async16(gin_s + i, p.g_in + k0 + 8 * i);
     cp_async_commit();
@@ -325,11 +331,6 @@ __global__ void __launch_bounds__(kGvThreads, 3) gemv_kernel(Params p, int kc, i
         tc_cp_128x256b(tmem + kTaCol + 8 * q, sdesc_sw128(smem_u32(w_s + (q >> 2) * kWChunkBytes)) + 2 * (q & 3));
     }
   }
-  if (FUSED && (tid >> 4) < M)  // the rows' inputs over this K range: a hint before the wait
-    for (int c = tid & 15; c < (k1 - k0) / 8; c += 16) {
-      prefetch_l2(p.ar + (int64_t)(tid >> 4) * K + k0 + 8 * c);
-      prefetch_l2(p.res + (int64_t)(tid >> 4) * K + k0 + 8 * c);
-    }
   if (warp == 7 && lane < TS && ks + C * lane < M) {  // inputs: a hint before the wait
     prefetch_l2(p.pos + ks + C * lane);
     prefetch_l2(p.slot + ks + C * lane);

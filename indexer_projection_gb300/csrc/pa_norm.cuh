@@ -212,6 +212,23 @@ __device__ __forceinline__ float amax_from_pair(float mh, float ml, float rh, fl
   two_prod(mh, rh, q, e);
   return __fadd_rn(q, __fmaf_rn(mh, rl, __fmaf_rn(ml, rh, e)));
 }
+// The block's maximum pair (every thread gets it); red: NTHR / 32 entries.
+template <int NTHR>
+__device__ __forceinline__ void block_pair_max(float &mh, float &ml, float2 *red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float qh = __shfl_xor_sync(0xffffffffu, mh, o), ql = __shfl_xor_sync(0xffffffffu, ml, o);
+    pair_max(mh, ml, qh, ql);
+  }
+  __syncthreads();  // red may still be read by a previous reduction
+  if (lane == 0) red[warp] = make_float2(mh, ml);
+  __syncthreads();
+  mh = red[0].x;
+  ml = red[0].y;
+#pragma unroll
+  for (int w = 1; w < NTHR / 32; ++w) pair_max(mh, ml, red[w].x, red[w].y);
+}
 __device__ __forceinline__ float amax8(const float (&n)[8]) {
   float a = 0.f;
 #pragma unroll
@@ -265,7 +282,7 @@ __device__ __forceinline__ void norm_quant_row(const Params &p, const int m, flo
   const uint4 *res = reinterpret_cast<const uint4 *>(p.res + (int64_t)m * H);
   uint4 *rout = p.residual ? reinterpret_cast<uint4 *>(p.residual + (int64_t)m * H) : nullptr;
   float acc[MAXC][8];
-  float ss = 0.f, ss_lo = 0.f;
+  float ss = 0.f, ss_lo = 0.f, mh = 0.f, ml = 0.f;
   uint4 gpre[MAXC];  // the input-norm gamma, loaded with the row
   const uint4 *g4 = reinterpret_cast<const uint4 *>(p.g_in);
 #pragma unroll
@@ -280,6 +297,7 @@ __device__ __forceinline__ void norm_quant_row(const Params &p, const int m, flo
       uint4 rb;
       acc8(__ldcs(ar + c), __ldcs(res + c), acc[j], rb, ss, ss_lo);
       if (rout) __stcs(rout + c, rb);
+      if (WFMT == 0) absprod_max8(acc[j], gpre[j], mh, ml);
     }
   }
   float rh, rl;
@@ -287,35 +305,9 @@ __device__ __forceinline__ void norm_quant_row(const Params &p, const int m, flo
   const float f = __fadd_rn(rh, rl);
   uint2 *xq = reinterpret_cast<uint2 *>(p.xq + (int64_t)m * H);
   if (WFMT == 0) {
-    // the scale s = amax(n) / 448, from the approximate amax where every
-    // amax within kSafe of it gives the same s, else from the exact n
-    float amax = 0.f;
-#pragma unroll
-    for (int j = 0; j < MAXC; ++j) {
-      const int c = tid + NTHR * j;
-      if (c < nch) {
-        float t[8];
-        napprox8(acc[j], gpre[j], f, t);
-        amax = fmaxf(amax, amax8(t));
-      }
-    }
-    float tmax = block_max<NTHR>(amax, red);
-    const float s_lo = __fdiv_rn(tmax * (1.0f - kSafe), kFp8Max), s_hi = __fdiv_rn(tmax * (1.0f + kSafe), kFp8Max);
-    if (tmax != 0.f && (s_lo != s_hi || p.exact_norm)) {  // block-uniform: the rare exact amax
-      amax = 0.f;
-#pragma unroll
-      for (int j = 0; j < MAXC; ++j) {
-        const int c = tid + NTHR * j;
-        if (c < nch) {
-          float n[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) n[i] = acc[j][i];
-          norm8(n, gpre[j], rh, rl);
-          amax = fmaxf(amax, amax8(n));
-        }
-      }
-      tmax = block_max<NTHR>(amax, red);
-    }
+    // the scale s = amax(n) / 448: the row's max |acc (1 + gamma)| times rstd
+    block_pair_max<NTHR>(mh, ml, red2);
+    const float tmax = amax_from_pair(mh, ml, rh, rl);
     const float s = tmax == 0.f ? 1.0f : __fdiv_rn(tmax, kFp8Max);
     const float rs = __frcp_rn(s);
 #pragma unroll

@@ -135,3 +135,44 @@ def test_fused_single_kernel(fmt):
                              outlier_frac=0.2), flags=flags)
     check(workloads.Workload("fz_one", H=6144, nkv=2, M=1, weight_fmt=fmt, cache_fmt="fp8", seed=92,
                              positions="uniform", max_pos=500, pool_pages16=64), flags=flags)
+
+
+@pytest.mark.parametrize("fmt,H,M,seed", [("ptpc", 6144, 8, 91), ("ptpc", 4352, 3, 92), ("ptpc", 512, 4, 93),
+                                          ("ptpc", 6144, 16, 96), ("mx", 6144, 16, 94), ("mx", 512, 5, 95)])
+def test_skinny_prologue_codes_and_scales_are_the_oracles(fmt, H, M, seed):
+    # White box.  The skinny path's prologue leaves in the workspace the
+    # per-token scales at byte 256 (per-channel format) and the FP8 codes
+    # [M, H] at the next 256-byte boundary (after the MXFP8 scale atoms,
+    # F8_128x4 over M rounded up to 128).  The per-channel scale comes from
+    # one exchange (max |acc (1 + gamma)| times rstd, rounded once), not from
+    # a pass over the normalised row: every scale and every code must still
+    # be the oracle's.  A third of the rows are outliers (x50).
+    import oracle
+    wl = workloads.Workload(f"pq{H}", H=H, nkv=1, M=M, weight_fmt=fmt, cache_fmt="fp8", seed=seed,
+                            outlier_frac=0.3, max_pos=4096, pool_pages16=2048)
+    st = workloads.host_state(wl)
+    g = harness.GpuRun(wl, st, flags=_gemv_flags())
+    g.run()
+    assert g.runner.device_status() == 0
+    ws = g.runner.workspace.cpu().numpy()
+
+    def up(x):
+        return (x + 255) // 256 * 256
+    ksf = H // 32
+    xs_off = 256
+    xsf_off = up(xs_off + 4 * M)
+    xq_off = xsf_off + (up((M + 127) // 128 * 128 * ksf) if fmt == "mx" else 0)
+    cfg = oracle.oracle_config(wl)
+    ref = [oracle.prologue_row(cfg, st["ar"][m], st["res"][m], st["g_in"]) for m in range(M)]
+    xq = ws[xq_off:xq_off + M * H].reshape(M, H)
+    for m in range(M):
+        assert np.array_equal(xq[m], ref[m][1]), m
+    if fmt == "ptpc":
+        xs = ws[xs_off:xs_off + 4 * M].view(np.float32)
+        assert np.array_equal(xs, np.array([r[2] for r in ref], np.float32))
+    else:
+        rows = np.stack([r[3] for r in ref])
+        got = ws[xsf_off:xsf_off + (M + 127) // 128 * 128 * ksf]
+        want = oracle.pack_sf128x4(rows, pad=0)
+        real = oracle.pack_sf128x4(np.ones_like(rows), pad=0) == 1
+        assert np.array_equal(got[real], want[real])
