@@ -243,8 +243,10 @@ __device__ __forceinline__ float amax8(const float (&n)[8]) {
 // the scales leave the prologue, so it first computes them from a cheap n
 // (t = RN(RN(acc * f) * RN(1 + gamma)), f = RN(rh + rl): within 4 * 2^-24 of
 // n, relative) and keeps a result only where every value within a relative
-// kSafe of it gives the same code (or scale); there the exact n must give it
-// too.  Elsewhere (about one element in 2^16) it recomputes exactly.
+// kSafe of it gives the same code (or MXFP8 block exponent); there the exact
+// n must give it too.  Elsewhere (about one element in 2^16) it recomputes
+// exactly.  (The per-channel scale needs no check: it comes from the row's
+// max |acc (1 + gamma)| times rstd, rounded once; see absprod_max8.)
 constexpr float kSafe = 0x1p-20f;  // > 4 * 2^-24 (t) + 2 * 2^-24 (the reciprocal of s)
 
 __device__ __forceinline__ void napprox8(const float (&acc)[8], uint4 gw4, float f, float (&t)[8]) {

@@ -6,9 +6,11 @@
 //   prologue_rows_kernel  one thread-block cluster per token row, a K slice
 //                         per CTA: the skinny path's few rows, whose latency
 //                         the step waits on; the correctly rounded norm costs
-//                         ~50 instructions an element, too much for a few
+//                         ~30 instructions an element, too much for a few
 //                         SMs, so each row is spread over C SMs and the row
 //                         sums are exchanged through distributed shared memory
+//                         (one exchange carries the sum of squares and the
+//                         per-channel amax)
 #include "pa_device.cuh"
 #include "pa_launch.h"
 #include "pa_norm.cuh"
