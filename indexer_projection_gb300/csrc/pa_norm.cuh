@@ -51,9 +51,13 @@ __device__ __forceinline__ void dd_add(float &hi, float &lo, float x, float xl) 
 __device__ __forceinline__ void rstd_from_dd(float sh, float sl, int H, float eps, float &rh, float &rl) {
   // x = sum / H + eps
   const float fh = (float)H;
-  const float qh = __fdiv_rn(sh, fh);
-  const float rem = __fmaf_rn(-qh, fh, sh);  // exact: sh - qh * H
-  const float ql = __fdiv_rn(__fadd_rn(rem, sl), fh);
+  const float inv = __frcp_rn(fh);
+  // sum / H as qh + ql: qh within two ulps of sh / H, the remainder
+  // sh - qh * H from one FMA (a few ulps of it at worst, itself ~2^-22 of sh),
+  // so the pair is good to ~2^-46 without a divide
+  const float qh = __fmul_rn(sh, inv);
+  const float rem = __fmaf_rn(-qh, fh, sh);
+  const float ql = __fmul_rn(__fadd_rn(rem, sl), inv);
   float xh, xe;
   two_sum(qh, eps, xh, xe);
   const float xl = __fadd_rn(ql, xe);

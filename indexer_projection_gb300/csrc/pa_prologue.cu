@@ -125,20 +125,36 @@ __global__ void __launch_bounds__(128 * 16 / C) prologue_rows_kernel(Params p, i
                    : "memory");
   }
   const bool ok1 = mbar_wait_cluster(&bar1, 0, p.status);
-  float th = ex1[0].x, tl = ex1[0].y;  // the C partials in order: the same sum in every CTA
+  // the C partials combined by a fixed shuffle tree (lane l starts from
+  // partial l % C) and taken from lane 0: the same sum and maximum in every
+  // warp of every CTA of the cluster
+  float th = ex1[lane & (C - 1)].x, tl = ex1[lane & (C - 1)].y;
+  float qh = ex1[lane & (C - 1)].z, ql = ex1[lane & (C - 1)].w;
 #pragma unroll
-  for (int q = 1; q < C; ++q) dd_add(th, tl, ex1[q].x, ex1[q].y);
+  for (int o = C / 2; o > 0; o >>= 1) {
+    const float oh = __shfl_xor_sync(0xffffffffu, th, o), ol = __shfl_xor_sync(0xffffffffu, tl, o);
+    dd_add(th, tl, oh, ol);
+    if (WFMT == 0) {
+      const float a = __shfl_xor_sync(0xffffffffu, qh, o), b = __shfl_xor_sync(0xffffffffu, ql, o);
+      pair_max(qh, ql, a, b);
+    }
+  }
+  th = __shfl_sync(0xffffffffu, th, 0);
+  tl = __shfl_sync(0xffffffffu, tl, 0);
+  qh = __shfl_sync(0xffffffffu, qh, 0);
+  ql = __shfl_sync(0xffffffffu, ql, 0);
   float rh, rl;
   rstd_from_dd(th, tl, H, p.eps, rh, rl);
   if (act && ok1) norm8(acc, gw, rh, rl);
   uint2 *xq = reinterpret_cast<uint2 *>(p.xq + (int64_t)m * H);
   if (WFMT == 0) {
-    float qh = ex1[0].z, ql = ex1[0].w;
-#pragma unroll
-    for (int q = 1; q < C; ++q) pair_max(qh, ql, ex1[q].z, ex1[q].w);
     const float tmax = amax_from_pair(qh, ql, rh, rl);
     const float s = tmax == 0.f ? 1.0f : __fdiv_rn(tmax, kFp8Max);
-    if (act && ok1) xq[c] = quant8_ptpc(acc, s);
+    if (act && ok1) {  // n * RN(1 / s) where every value within kSafe gives the same code, else n / s
+      uint2 w;
+      if (!codes8_checked(acc, __frcp_rn(s), w) || p.exact_norm) w = quant8_ptpc(acc, s);
+      xq[c] = w;
+    }
     if (r == 0 && tid == 0) p.x_scale[m] = s;
   } else {
     float bm = act ? amax8(acc) : 0.f;
