@@ -109,11 +109,6 @@ __device__ __forceinline__ int64_t ld_i64(const int64_t *p) { return __ldg(p); }
 // It orders nothing and changes no value a later load returns, so it may be
 // issued for an input before the wait on the kernel that produces it.
 __device__ __forceinline__ void prefetch_l2(const void *p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
-__device__ __forceinline__ int ld_acquire(const int *p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 __device__ __forceinline__ void st_release(int *p, int v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }

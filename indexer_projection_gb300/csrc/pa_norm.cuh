@@ -112,22 +112,6 @@ __device__ __forceinline__ float pow2_neg(int e) {  // 2^-e, e in [-127, 127]
   return e == 127 ? __uint_as_float(0x00400000u) : __uint_as_float((uint32_t)(127 - e) << 23);
 }
 
-template <int NTHR>
-__device__ __forceinline__ float block_max(float v, float *red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  __syncthreads();  // red may still be read by a previous reduction
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  constexpr int W = NTHR / 32;
-  float r = lane < W ? red[lane] : 0.f;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1)
-    if (o < W) r = fmaxf(r, __shfl_xor_sync(0xffffffffu, r, o));
-  return __shfl_sync(0xffffffffu, r, 0);  // lanes >= W saw only zeros
-}
-
 // 8 elements of a row: acc = ar + res in f32, their bf16 residual bits, and
 // the (hi, lo) running sum of acc^2.
 __device__ __forceinline__ void acc8(uint4 a, uint4 r, float (&acc)[8], uint4 &resid, float &ss, float &ss_lo) {
@@ -280,7 +264,7 @@ __device__ __forceinline__ bool codes8_checked(const float (&t)[8], float k, uin
 // tid + NTHR * j, j < MAXC, so H <= 8 * NTHR * MAXC; NTHR % 4 == 0 keeps the
 // four chunks of a 32-element MXFP8 block in lanes 4i .. 4i + 3.
 template <int WFMT, int NTHR, int MAXC>
-__device__ __forceinline__ void norm_quant_row(const Params &p, const int m, float *red, float2 *red2) {
+__device__ __forceinline__ void norm_quant_row(const Params &p, const int m, float2 *red2) {
   static_assert(NTHR % 32 == 0, "whole warps");
   const int tid = threadIdx.x;
   const int H = p.H, nch = H >> 3, ksf = H >> 5;

@@ -25,7 +25,6 @@ namespace pa {
 // the row is done sooner.
 template <int WFMT, int NTHR, int MAXC>
 __global__ void __launch_bounds__(NTHR) prologue_kernel(Params p, int use_pdl) {
-  __shared__ float red[NTHR / 32];
   __shared__ float2 red2[NTHR / 32];
   if (use_pdl) {
     pdl_trigger();
@@ -38,7 +37,7 @@ __global__ void __launch_bounds__(NTHR) prologue_kernel(Params p, int use_pdl) {
       for (int kb = threadIdx.x; kb < ksf; kb += NTHR) p.xsf[sf128x4_offset(m, kb, ksf)] = 127;
     return;
   }
-  norm_quant_row<WFMT, NTHR, MAXC>(p, m, red, red2);
+  norm_quant_row<WFMT, NTHR, MAXC>(p, m, red2);
 }
 
 // One cluster of C CTAs per token row (blockIdx.x / C); CTA r takes the
