@@ -166,6 +166,52 @@ def test_nvfp4_sign_clearing_matches_the_pages_word_trick():
         assert cleared == want
 
 
+def test_nvfp4_product_is_rounded_toward_zero_before_e2m1():
+    # the epilogue page's _nvfp4_quant32 forms v * (1/sf) * (1/global) with a
+    # round-toward-zero f32 multiply, then rounds to E2M1 (nearest, ties to
+    # even).  Groups with a non-trivial global scale put some products within
+    # one f32 step above an E2M1 midpoint, where RZ and RN pick different
+    # codes; the oracle must take the RZ one.  RZ is formed here from the exact
+    # float64 product of the two f32 factors.
+    mags = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+    def e2m1(x):
+        # nearest magnitude (ties to the even code), saturating at 6; sign in bit 3, none on zero
+        a = np.minimum(np.abs(x), 6.0)
+        d = np.abs(a[:, None] - mags[None, :])
+        best = np.argmin(d, axis=1)  # the lower code of a tie
+        nxt = np.minimum(best + 1, 7)
+        tie = (best < 7) & (d[np.arange(a.size), nxt] == d[np.arange(a.size), best])
+        best = np.where(tie & (best % 2 == 1), best + 1, best)
+        return np.where(best == 0, 0, best | np.where(np.signbit(x), 8, 0)).astype(np.uint8)
+
+    r = np.random.default_rng(77)
+    differ = 0
+    for trial in range(3000):
+        gs_inv = np.float32(1.0) / np.float32(r.uniform(0.3, 3.0))
+        v = (r.standard_normal(16) * r.uniform(0.5, 20)).astype(np.float32)
+        # nudge one element onto a midpoint of the scaled grid
+        nib, sfc = oracle.nvfp4_group16(v, float(gs_inv))
+        sf = np.float32(oracle.e4m3_decode(sfc))
+        rcp = np.float32(np.float32(1.0) / sf) * gs_inv
+        mid = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])[r.integers(0, 7)]
+        j = int(r.integers(1, 16))
+        if abs(v[j]) < np.max(np.abs(v)):
+            v[j] = np.float32(mid / np.float64(rcp)) * (1 if r.random() < 0.5 else -1)
+            for _ in range(int(r.integers(0, 3))):
+                v[j] = np.nextafter(v[j], np.float32(np.inf) * np.sign(v[j]))
+        nib, sfc = oracle.nvfp4_group16(v, float(gs_inv))
+        sf = np.float32(oracle.e4m3_decode(sfc))
+        rcp = np.float32(np.float32(1.0) / sf) * gs_inv
+        exact = v.astype(np.float64) * np.float64(rcp)
+        rn = exact.astype(np.float32)
+        rz = np.where(np.abs(rn.astype(np.float64)) > np.abs(exact), np.nextafter(rn, np.float32(0)), rn)
+        want = e2m1(rz.astype(np.float64))
+        assert np.array_equal(nib, want), (trial, v, nib, want)
+        differ += int(np.sum(e2m1(rn.astype(np.float64)) != want))
+    assert differ > 20  # the RZ / RN difference was exercised
+
+
 # ------------------------------------------------------- norm and rope
 
 def test_head_rmsnorm_unit_rms_with_zero_gamma_and_constant_rows():
@@ -248,6 +294,110 @@ def test_prologue_mx_blocks():
     assert np.all((bmax >= 224.0) & (bmax <= 448.0))  # minimal power of two
     n = deq * np.array([oracle.e8m0_decode(c) for c in xsf])[:, None]
     assert abs(math.sqrt(np.mean(n ** 2)) - 1.0) < 0.03
+
+
+def _e4m3_torch(x):
+    """torch's round-to-nearest-even E4M3 cast (values already within +-448)."""
+    t = torch.from_numpy(np.clip(np.asarray(x, np.float32), -448.0, 448.0))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _e4m3_midpoint_distance(x):
+    """Relative distance of each |x| from the nearest midpoint between two
+    neighbouring E4M3 magnitudes (where one rounding step can flip a code)."""
+    mags = np.array(sorted({abs(oracle.e4m3_decode(c)) for c in range(0x7F)}), np.float64)
+    mids = (mags[1:] + mags[:-1]) / 2
+    a = np.abs(np.asarray(x, np.float64))
+    return np.min(np.abs(a[:, None] - mids[None, :]), axis=1) / np.maximum(a, 1e-30)
+
+
+@pytest.mark.parametrize("c,eps", [(0.75, 0.3), (-2.5, 1e-6), (0.0625, 0.01)])
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_prologue_constant_row_with_gamma_has_its_closed_form(c, eps, fmt):
+    # Gemma RMSNorm of a constant row c with per-element gamma (pre_attn page,
+    # norm_quant): mean(acc^2) = c^2 exactly, so n_k = c / sqrt(c^2 + eps) *
+    # (1 + gamma_k) in closed form.  The per-token scale is max|n| / 448 and the
+    # codes are e4m3(n_k / s) = e4m3(448 (1 + gamma_k) sign(c) / max|1 + gamma|).
+    # A (1 - gamma) slip, a gamma read at the wrong index, a dropped eps or an
+    # H - 1 divisor moves a code or the scale.
+    H = 512
+    g = torch.Generator().manual_seed(int(abs(c) * 1000) + fmt)
+    gam = workloads._bf16_bits(torch.randn(H, generator=g) * 0.3)
+    gd = bf16_f64(gam)
+    ar = np.full(H, oracle.bf16_encode(c), np.uint16)
+    res = np.zeros(H, np.uint16)
+    eps32 = float(np.float32(eps))
+    n = c / math.sqrt(c * c + eps32) * (1.0 + gd)           # float64 closed form
+    _, xq, xs, xsf = oracle.prologue_row(_cfg(H, weight_fmt=fmt, eps=eps), ar, res, gam)
+    if fmt == 0:
+        s = np.max(np.abs(n)) / 448.0
+        assert abs(xs - s) <= 2.0 ** -22 * s, (xs, s)
+        q = n / s
+    else:
+        e = np.array([oracle.mx_exponent(float(np.float32(a))) for a in np.abs(n).reshape(-1, 32).max(axis=1)])
+        assert np.array_equal(xsf, (e + 127).astype(np.uint8))
+        q = n * np.repeat(2.0 ** -e, 32)
+    clear = _e4m3_midpoint_distance(q) > 2.0 ** -18        # no f32 rounding can flip these
+    assert clear.mean() > 0.95
+    assert np.array_equal(xq[clear], _e4m3_torch(q)[clear])
+
+
+@pytest.mark.parametrize("H,a,b,eps", [(512, 1.5, -0.25, 1e-6), (6144, 3.0, 0.5, 0.5), (1024, -0.125, 0.0, 0.0),
+                                       (6144, 40.0, -7.0, 1e-6)])
+def test_prologue_two_valued_row_pins_rstd_to_f32_precision(H, a, b, eps):
+    # a row alternating a, b has mean(acc^2) = (a^2 + b^2) / 2 exactly, so
+    # rstd = 1 / sqrt((a^2 + b^2) / 2 + eps) and (gamma = 0) the per-token scale
+    # is max(|a|, |b|) rstd / 448: checked to f32 precision (an H - 1 divisor is
+    # off by 1 / (2H), a dropped eps by eps / mean)
+    row = np.array([oracle.bf16_encode(a), oracle.bf16_encode(b)] * (H // 2), np.uint16)
+    eps32 = float(np.float32(eps))
+    rstd = 1.0 / math.sqrt((a * a + b * b) / 2.0 + eps32)
+    s = max(abs(a), abs(b)) * rstd / 448.0
+    _, xq, xs, _ = oracle.prologue_row(_cfg(H, eps=eps), np.zeros(H, np.uint16), row, np.zeros(H, np.uint16))
+    assert abs(xs - s) <= 2.0 ** -22 * s, (xs, s)
+    q = np.array([a, b] * (H // 2)) * rstd / s
+    clear = _e4m3_midpoint_distance(q) > 2.0 ** -18
+    assert np.array_equal(xq[clear], _e4m3_torch(q)[clear])
+
+
+def bf16_f64(bits):
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _bf16_torch(x):
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("cache", ["fp8", "nvfp4"])
+def test_step_q_and_index_q_heads_are_norm_rope_of_their_own_slice(cache):
+    # q heads (epilogue page, q branch): bf16(z) and e4m3(z * (1 / q_fp8_scale))
+    # with z = RoPE(RMSNorm(y_head, g_q)); index_q heads: bf16(z) and e4m3(z)
+    # with g_iq (pre_attn page head tasks; epilogue page index_q branch).  Each
+    # head is checked against the pinned norm and RoPE of its own slice of the
+    # projection, and the E4M3 / bf16 roundings against torch's casts.  A g_q /
+    # g_iq swap, q without RoPE, q_fp8 times the scale instead of divided by
+    # it, or a head written at another head's offset fails here.
+    wl = workloads.tiny().replace(name=f"qpin_{cache}", nkv=2, n_q=0, n_iq=0, M=3, q_fp8=True, iq_fp8=True,
+                                  q_fp8_scale=0.37, cache_fmt=cache, pool_pages=64,
+                                  weight_fmt="ptpc" if cache == "fp8" else "mx")
+    st = workloads.host_state(wl)
+    y = oracle.run_rows(wl, st, range(wl.M), want_y=True)
+    inv = np.float32(1.0) / np.float32(wl.q_fp8_scale)
+    iq0 = wl.n_q + 2 * wl.nkv
+    assert not np.array_equal(st["g_q"], st["g_iq"])
+    for m in range(wl.M):
+        cs = st["cos_sin"][st["positions"][m]]
+        for j in range(wl.n_q):
+            z = np.float32(oracle.rope_neox(oracle.head_rmsnorm(y[m, j * 128:(j + 1) * 128], st["g_q"], wl.eps), cs))
+            sl = slice(j * 128, (j + 1) * 128)
+            assert np.array_equal(st["q_bf16"][m, sl], _bf16_torch(z)), (m, j)
+            assert np.array_equal(st["q_fp8"][m, sl], _e4m3_torch(z * inv)), (m, j)
+        for j in range(wl.n_iq):
+            h = iq0 + j
+            z = np.float32(oracle.rope_neox(oracle.head_rmsnorm(y[m, h * 128:(h + 1) * 128], st["g_iq"], wl.eps), cs))
+            sl = slice(j * 128, (j + 1) * 128)
+            assert np.array_equal(st["iq_bf16"][m, sl], _bf16_torch(z)), (m, j)
+            assert np.array_equal(st["iq_fp8"][m, sl], _e4m3_torch(z)), (m, j)
 
 
 # ------------------------------------------------------------ projection
@@ -397,6 +547,14 @@ def test_step_fp8_caches_touch_only_the_slots_and_decode_consistently():
         z = oracle.rope_neox(oracle.head_rmsnorm(k, st["g_k"], wl.eps), st["cos_sin"][st["positions"][m]])
         deq = np.array([oracle.e4m3_decode(c) for c in kcodes]) * ks
         assert np.allclose(deq, z, rtol=2 ** -3, atol=ks * 2 ** -8)
+        # exactly (pre_attn page, head tasks: the K store quantises the
+        # bf16-rounded normed + roped value by the scale of its f32 amax):
+        # e4m3(f32(bf16(z)) / ks), ks = f32(amax(f32(z)) / 448)
+        zf = np.float32(z)
+        ks_want = np.float32(np.max(np.abs(zf))) / np.float32(448.0)
+        assert ks == ks_want
+        zb = torch.from_numpy(zf).to(torch.bfloat16).to(torch.float32).numpy()
+        assert np.array_equal(kcodes, _e4m3_torch(zb / ks_want))
         # the index cache row holds e4m3(bf16(index_k))
         ik = y[m, (wl.n_heads - 1) * 128:]
         z = oracle.rope_neox(oracle.head_rmsnorm(ik, st["g_ik"], wl.eps), st["cos_sin"][st["positions"][m]])
