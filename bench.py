@@ -3,18 +3,21 @@
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
                   [--workload decode|spec_decode|prefill|tiny|sweep_m<M>]
+                  [--also prefill|none]
 
 A step is one pre_attn_run() (prologue + skinny GEMV or tcgen05 GEMM with the
 fused head epilogue) over one batch of the workload's synthetic inputs.  The
 timed region is a CUDA graph of exactly K steps; step i uses the i-th of C
 rotating copies of the layer weights and inputs (C chosen so the copies
 exceed twice the L2), so weights stream from HBM as they would across layers.
-Rank 0 prints one JSON line.  Under torchrun each rank runs an independent
-replica (the step has no cross-GPU exchange) and the slowest rank's time sets
-the aggregate tokens/s.
+Rank 0 prints one JSON line: the headline workload (decode by default) and,
+under "prefill", the prefill configuration timed in the same run (its own
+graph of steps, at least a second of them, with its own clock record).
+Under torchrun each rank runs an independent replica (the step has no
+cross-GPU exchange) and the slowest rank's time sets the aggregate tokens/s.
 
---impl reference times the CPU oracle (tests only use it otherwise) on the
-host cores on bounded samples of the same workload.
+--impl reference times the CPU oracle (tests only use it otherwise) on one
+host core on bounded samples of the same workload.
 """
 
 from __future__ import annotations
@@ -24,6 +27,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -56,6 +60,12 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def workload_config(name: str, wl, world: int) -> dict:
+    """The workload as both arms name it (identical keys and values)."""
+    return {"workload": name, "hidden": wl.H, "nkv": wl.nkv, "M": wl.M, "N": wl.N, "weight": wl.weight_fmt,
+            "cache": wl.cache_fmt, "parallelism": f"replicas x{world}"}
+
+
 # ------------------------------------------------------------- byte / flop accounting
 
 def step_bytes(wl) -> dict:
@@ -81,15 +91,15 @@ def step_flops(wl) -> int:
     return 2 * wl.M * wl.N * wl.H
 
 
-KERNEL_SOURCES = {"gemv": ("pa_gemv.cu", "pa_device.cuh", "pa_tc.cuh", "pa_norm.cuh"),
-                  "gemv_fused": ("pa_gemv.cu", "pa_device.cuh", "pa_tc.cuh", "pa_norm.cuh"),
+# sources each kernel is compiled from (ties an ncu summary under profiles/ to them)
+KERNEL_SOURCES = {"skinny": ("pa_gemv.cu", "pa_device.cuh", "pa_tc.cuh", "pa_norm.cuh"),
                   "gemm": ("pa_gemm.cu", "pa_device.cuh", "pa_tc.cuh"),
-                  "gemm2": ("pa_gemm2.cu", "pa_device.cuh"),
+                  "gemm_pair": ("pa_gemm2.cu", "pa_device.cuh", "pa_tc.cuh"),
                   "prologue": ("pa_prologue.cu", "pa_device.cuh", "pa_norm.cuh")}
 
 
 def kernel_sha(kernel: str) -> str:
-    """Hash of the sources a kernel is built from (ties an ncu summary to them)."""
+    """Hash of the sources a kernel is built from."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "indexer_projection_gb300", "csrc", f), "rb") as fh:
@@ -98,8 +108,8 @@ def kernel_sha(kernel: str) -> str:
 
 
 def ncu_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources."""
+    """DRAM bytes per launch from the committed ncu summary
+    profiles/<kernel>_<workload>.md, if it was taken on the current sources."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(path):
         return None
@@ -124,7 +134,7 @@ class ClockSampler:
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, period_ms: int = 50):
+    def __init__(self, gpu_index: int, period_ms: int = 20):
         self.samples = []
         self.proc = None
         self.gpu = gpu_index
@@ -134,7 +144,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 f"-lms", str(self.period), "-i", str(self.gpu)],
+                 "-lms", str(self.period), "-i", str(self.gpu)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (FileNotFoundError, OSError):
             self.proc = None
@@ -158,9 +168,13 @@ class ClockSampler:
             self.thread.join(timeout=5)
 
     def summary(self, t0=None, t1=None):
+        """Clocks of the samples taken between t0 and t1 (all samples, and
+        "window": "run", when the window was too short to hold one)."""
         sel = [p for (t, p) in self.samples if (t0 is None or t >= t0) and (t1 is None or t <= t1)]
+        window = "timed region"
         if not sel:
             sel = [p for (_, p) in self.samples]
+            window = "run"
         if not sel:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
 
@@ -178,7 +192,7 @@ class ClockSampler:
                 if v.lower().startswith("active"):
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sel)}
+                "reasons": sorted(reasons), "samples": len(sel), "window": window}
 
 
 # ------------------------------------------------------------ several ranks
@@ -279,75 +293,39 @@ class DeviceWorkload:
                         index_slot_mapping=self.islot, stream=stream)
 
 
-def run_ours(args, wl, rank, world, local_rank):
-    import torch
-    import torch.distributed as dist
+def path_info(B, path):
+    name = {B.PA_PATH_GEMV: "skinny", B.PA_PATH_GEMV_FUSED: "skinny", B.PA_PATH_GEMM_SINGLE: "gemm",
+            B.PA_PATH_GEMM_PAIR: "gemm_pair"}[path]
+    desc = {B.PA_PATH_GEMV: "pa_prologue_rows_kernel then pa_skinny_proj_kernel (tcgen05 GEMV, a cluster per head), "
+                            "PDL-chained",
+            B.PA_PATH_GEMV_FUSED: "pa_skinny_proj_kernel with the row normalisation inside (one launch)",
+            B.PA_PATH_GEMM_SINGLE: "pa_prologue_kernel then pa_gemm_kernel (tcgen05, 128x128 tiles)",
+            B.PA_PATH_GEMM_PAIR: "pa_prologue_kernel then pa_gemm_pair_kernel (tcgen05 cta_group::2, 256x256 tiles)"}[path]
+    launches = 1 if path == B.PA_PATH_GEMV_FUSED else 2
+    return name, desc, launches
 
-    from indexer_projection_gb300 import binding as B
 
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    peaks, peak_src = measured_peaks()
-    st = workloads.host_state(wl)
-    props = torch.cuda.get_device_properties(dev)
-    l2 = props.L2_cache_size
-    per_copy = step_bytes(wl)["weights"] + 2 * wl.M * wl.H * 2
-    copies = max(2, min(64, math.ceil(2.5 * l2 / per_copy)))
-    flags = {"auto": 0, "single": B.PA_FLAG_GEMM_SINGLE, "pair": B.PA_FLAG_GEMM_PAIR}[args.gemm]
-    if args.fuse:
-        flags |= B.PA_FLAG_FUSE
-    dw = DeviceWorkload(wl, st, copies, dev, flags=flags)
-    stream = torch.cuda.Stream(dev)
-    K, W = args.steps, args.warmup
-
-    def barrier():
-        if world > 1:
-            dist.barrier()
-
-    sampler = ClockSampler(local_rank)
-    sampler.start()
-    with torch.cuda.stream(stream):
-        for i in range(W):
-            dw.step(i, stream)
-    stream.synchronize()
-    # a CUDA graph of exactly K steps (PDL edges kept between the kernels)
-    G = min(K, 4096)
-    full, rest = divmod(K, G)
+def build_graphs(torch, dw, n_steps, stream):
+    """CUDA graphs holding exactly n_steps steps (chunks of at most 4096)."""
+    G = min(n_steps, 4096)
+    full, rest = divmod(n_steps, G)
     graphs = []
-    for n in ([G] if full else []) + ([rest] if rest else []):
+    for n in [G] * min(full, 1) + ([rest] if rest else []):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for i in range(n):
                 dw.step(i, stream)
-        graphs.append((g, n))
-    with torch.cuda.stream(stream):
-        for g, _ in graphs:  # untimed replay: instantiation / first-launch costs
-            g.replay()
-    stream.synchronize()
-    barrier()
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_wall0 = time.time()
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(full):
-            graphs[0][0].replay()
-        if rest:
-            graphs[-1][0].replay()
-        e1.record(stream)
-    torch.cuda.synchronize(dev)
-    t_wall1 = time.time()
-    barrier()
-    ms = max_over_ranks([e0.elapsed_time(e1)], world, dev)[0]
-    sampler.stop()
-    clocks = sampler.summary(t_wall0, t_wall1)
-    del graphs
+        graphs.append(g)
+    order = [graphs[0]] * full + ([graphs[-1]] if rest else [])
+    return graphs, order
 
-    # main-kernel device time: events recorded around it on the launching
-    # stream, steps queued behind a GPU sleep long enough that the host never
-    # starves the GPU between them (else the events would time the host's
-    # launch calls); no programmatic overlap with the prologue here
-    P = min(max(K, 50), 400)
+
+def main_kernel_ms(torch, B, dw, stream, P):
+    """Median device time of the step's main kernel with events recorded
+    around it on the launching stream.  The steps are queued behind a GPU
+    sleep long enough that the host never starves the GPU between them; the
+    events stop the main kernel from overlapping the prologue, so this is the
+    kernel alone, not its share of the pipelined step."""
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(P)]
     for a, b in evs:  # torch creates its CUDA events on first record
         a.record(stream)
@@ -370,15 +348,79 @@ def run_ours(args, wl, rank, world, local_rank):
         profiled_steps(P)
     B.pre_attn_set_profile_events(dw.runner.handle, None, None)
     stream.synchronize()
-    main_ms = statistics.median(a.elapsed_time(b) for a, b in evs[P // 4:])
+    return statistics.median(a.elapsed_time(b) for a, b in evs[P // 4:])
 
-    # end to end through the public API: pinned host inputs in, results out,
-    # every step.  The step's inputs sit in one pinned host block and one
-    # device block (ar | res | positions | slots, each 256-byte aligned), its
-    # outputs in one device block and one pinned host block: one copy each
-    # way per step (per-copy overhead, not bytes, dominated nine copies).
+
+def measure(args, wl, dev, world, K, W, min_seconds=0.0, flags=0):
+    """Time K steps of `wl` in CUDA graphs (repeated until at least
+    min_seconds when asked), the main kernel alone, and the clocks."""
+    import torch
+    import torch.distributed as dist
+
+    from indexer_projection_gb300 import binding as B
+
+    st = workloads.host_state(wl)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    per_copy = step_bytes(wl)["weights"] + 2 * wl.M * wl.H * 2
+    copies = max(2, min(64, math.ceil(2.5 * l2 / per_copy)))
+    dw = DeviceWorkload(wl, st, copies, dev, flags=flags)
+    stream = torch.cuda.Stream(dev)
+    path = B.pre_attn_path(dw.runner.handle, wl.M)
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            dw.step(i, stream)
+    stream.synchronize()
+    graphs, order = build_graphs(torch, dw, K, stream)
+    with torch.cuda.stream(stream):
+        for g in graphs:  # untimed replay: instantiation / first-launch costs
+            g.replay()
+    stream.synchronize()
+    # repeats of the K-step region, when a region alone is too short to be seen by the clock sampler
+    reps = 1
+    if min_seconds > 0:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for g in order:
+                g.replay()
+            e1.record(stream)
+        stream.synchronize()
+        reps = max(1, math.ceil(min_seconds * 1e3 / max(e0.elapsed_time(e1), 1e-3)))
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            for g in order:
+                g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    ms = max_over_ranks([e0.elapsed_time(e1)], world, dev)[0] / reps
+    time.sleep(3 * sampler.period / 1000)
+    clocks = sampler.summary(t_wall0, t_wall1)
+    sampler.stop()
+    del graphs, order
+    main_ms = main_kernel_ms(torch, B, dw, stream, min(max(K, 50), 400))
+    return dict(st=st, dw=dw, stream=stream, path=path, ms=ms, reps=reps, main_ms=main_ms, clocks=clocks,
+                copies=copies, per_copy=per_copy)
+
+
+def end_to_end(torch, wl, st, dw, stream, E, world, dev):
+    """Through the public API: pinned host inputs in, results out, every
+    step.  The step's inputs sit in one pinned host block and one device
+    block (ar | res | positions | slots, each 256-byte aligned), its outputs
+    in one device block and one pinned host block: one copy each way per step
+    (per-copy overhead, not bytes, dominated nine copies)."""
     from indexer_projection_gb300.runner import PreAttn
-    E = min(K, 2000)
+
     def layout(arrays):
         offs, off = [], 0
         for a in arrays:
@@ -407,6 +449,7 @@ def run_ours(args, wl, rank, world, local_rank):
     h_out = torch.empty(out_bytes, dtype=torch.uint8).pin_memory()
     h2d = sum(x.numel() * x.element_size() for x in src_in)
     d2h = sum(x.numel() * x.element_size() for x in out_like)
+
     def e2e_step(i):
         d_in.copy_(h_in, non_blocking=True)
         Li = dw.layers[i % len(dw.layers)]
@@ -425,7 +468,7 @@ def run_ours(args, wl, rank, world, local_rank):
             e2e_step(i)
         b.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_eager_ms = a.elapsed_time(b) / E
+    eager_ms = a.elapsed_time(b) / E
     # the same calls captured once in a CUDA graph (copies included)
     ge = torch.cuda.CUDAGraph()
     with torch.cuda.graph(ge, stream=stream):
@@ -437,60 +480,114 @@ def run_ours(args, wl, rank, world, local_rank):
         ge.replay()
         b.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = a.elapsed_time(b) / E
+    graph_ms = a.elapsed_time(b) / E
     del ge
-    e2e_ms, e2e_eager_ms = max_over_ranks([e2e_ms, e2e_eager_ms], world, dev)
+    graph_ms, eager_ms = max_over_ranks([graph_ms, eager_ms], world, dev)
+    return {"value": round(tokens_per_second(world, wl.M, min(graph_ms, eager_ms)), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E,
+            "how": "pinned host inputs -> device (one copy), pre_attn_run, outputs -> pinned host (one copy), every "
+                   "step; the faster of the calls issued eagerly and the same calls captured in a CUDA graph ("
+                   + ("graph" if graph_ms <= eager_ms else "eager") + ")",
+            "graph_value": round(tokens_per_second(world, wl.M, graph_ms), 1),
+            "eager_value": round(tokens_per_second(world, wl.M, eager_ms), 1)}
 
-    ms_step = ms / K
-    tokens_s = tokens_per_second(world, wl.M, ms_step)
+
+def roofline(B, wl, name, m, peaks, peak_src, workload_name):
+    """The roofline object of the step's dominant kernel.
+
+    Tensor-core path: the GEMM dominates the step (over 80% of it), so its
+    own time (events around it) over 2MNK.  Skinny path: the step is a
+    latency chain of two PDL-overlapped kernels around one HBM stream, and
+    events around the GEMV stop that overlap (the kernel timed that way runs
+    longer than the whole pipelined step), so the figure is the step's:
+    algorithmic bytes of the step over the step time; the GEMV alone is
+    reported beside it, labelled."""
+    ms_step, main_ms = m["ms"] / 1.0, m["main_ms"]
+    _, desc, _ = path_info(B, m["path"])
     nb = step_bytes(wl)
-    path = B.pre_attn_path(dw.runner.handle, wl.M)
-    gemm = path in (B.PA_PATH_GEMM_SINGLE, B.PA_PATH_GEMM_PAIR)
-    kname = {B.PA_PATH_GEMV: "gemv", B.PA_PATH_GEMV_FUSED: "gemv_fused", B.PA_PATH_GEMM_SINGLE: "gemm",
-             B.PA_PATH_GEMM_PAIR: "gemm2"}[path]
-    kdesc = {"gemv": "pa::gemv_kernel<.., false> (tcgen05 GEMV, one cluster per head, after the prologue)",
-             "gemv_fused": "pa::gemv_kernel<.., true> (prologue + tcgen05 GEMV in one kernel, one cluster per head)",
-             "gemm": "pa::gemm_kernel (tcgen05, 128x128 tiles)",
-             "gemm2": "pa::g2::gemm2_kernel (tcgen05 cta_group::2, 256x256 tiles)"}[kname]
-    launches_per_step = 1 if path == B.PA_PATH_GEMV_FUSED else 2
-    if gemm:
+    if name in ("gemm", "gemm_pair"):
         achieved = step_flops(wl) / (main_ms * 1e-3) / 1e12
         peak = peaks["bf16_tflops"] * FP8_OVER_BF16
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(kname, args.workload),
-                "kernel": f"{kdesc}, {main_ms * 1e3:.2f} us/launch",
-                "peak_source": f"{peak_src} bf16 x nominal FP8/BF16 ratio 2"}
-    else:
-        achieved = nb["main"] / (main_ms * 1e-3) / 1e9
-        peak = peaks["hbm_gbs"]
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(kname, args.workload),
-                "kernel": f"{kdesc}, {main_ms * 1e3:.2f} us/launch, {nb['main']} algorithmic bytes",
-                "peak_source": f"{peak_src} hbm_gbs"}
-    step_roof = (nb["step"] / (ms_step * 1e-3) / 1e9) / peaks["hbm_gbs"]
+        return {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(name, workload_name),
+                "kernel": f"{name}: {main_ms * 1e3:.2f} us/launch (events around it), 2*M*N*K = {step_flops(wl)} FLOP",
+                "peak_source": f"{peak_src} bf16 x nominal FP8/BF16 ratio 2 (of measured)"}
+    achieved = nb["step"] / (ms_step * 1e-3) / 1e9
+    peak = peaks["hbm_gbs"]
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": ncu_traffic(name, workload_name),
+            "kernel": f"whole step ({desc}): {nb['step']} algorithmic bytes over {ms_step * 1e3:.3f} us",
+            "main_kernel_alone": {"us": round(main_ms * 1e3, 3), "frac": round(nb["main"] / (main_ms * 1e-3) / 1e9 / peak, 4),
+                                  "note": "the GEMV timed with events around it, which stops its overlap with the "
+                                          "prologue; not a share of the pipelined step"},
+            "peak_source": f"{peak_src} hbm_gbs (of measured)"}
+
+
+def secondary(args, name, dev, world, peaks, peak_src):
+    """A second workload of the same run (prefill): its own graph of steps
+    (at least a second of them), main kernel and clocks."""
+    import torch
+
+    from indexer_projection_gb300 import binding as B
+
+    wl = get_workload(name)
+    K2 = max(20, min(args.steps, 200))
+    m = measure(args, wl, dev, world, K2, max(3, args.warmup), min_seconds=1.0)
+    kname, desc, _ = path_info(B, m["path"])
+    ms = m["ms"]
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    out = {"config": workload_config(name, wl, world), "path": desc, "steps": K2 * m["reps"],
+           "timed_as": f"{m['reps']} replays of a CUDA graph of {K2} steps",
+           "us_per_layer": round(ms * 1e3, 3), "tokens_per_s": round(tokens_per_second(world, wl.M, ms), 1),
+           "step_fp8_frac": round(step_flops(wl) / (ms * 1e-3) / 1e12 / fp8_peak, 4),
+           "step_hbm_frac": round(step_bytes(wl)["step"] / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+           "roofline": roofline(B, wl, kname, m, peaks, peak_src, name), "clocks": m["clocks"]}
+    del m
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args, wl, rank, world, local_rank):
+    import torch
+
+    from indexer_projection_gb300 import binding as B
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    peaks, peak_src = measured_peaks()
+    flags = {"auto": 0, "single": B.PA_FLAG_GEMM_SINGLE, "pair": B.PA_FLAG_GEMM_PAIR}[args.gemm]
+    if args.fuse:
+        flags |= B.PA_FLAG_FUSE
+    K, W = args.steps, args.warmup
+    m = measure(args, wl, dev, world, K, W, flags=flags)
+    kname, desc, launches = path_info(B, m["path"])
+    e2e = end_to_end(torch, wl, m["st"], m["dw"], m["stream"], min(K, 2000), world, dev)
+    ms_step = m["ms"]
+    nb = step_bytes(wl)
     line = {
-        "metric": METRIC, "value": round(tokens_s, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
-        "warmup": W, "ms_per_step": ms_step, "us_per_layer": round(ms_step * 1e3, 3),
+        "metric": METRIC, "value": round(tokens_per_second(world, wl.M, ms_step), 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": ms_step, "us_per_layer": round(ms_step * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 x e4m3 -> f32 (bf16 in/out)", "data": "synthetic (seeded, configs' shapes; random-init weights)",
-        "config": {"workload": args.workload, "hidden": wl.H, "nkv": wl.nkv, "M": wl.M, "N": wl.N,
-                   "weight": wl.weight_fmt, "cache": wl.cache_fmt, "path": kdesc,
-                   "l2": f"{copies} rotating weight+input copies ({copies * per_copy / 1e6:.0f} MB > 2x L2)",
-                   "timing": "CUDA graph of K steps, PDL chained", "parallelism": f"replicas x{world}"},
-        "roofline": roof,
-        "step_hbm_frac": round(step_roof, 4),
-        "gpu_launches": launches_per_step * K,
-        "e2e": {"value": round(tokens_per_second(world, wl.M, min(e2e_ms, e2e_eager_ms)), 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E,
-                "how": "pinned host inputs -> device (one copy), pre_attn_run, outputs -> pinned host (one copy), "
-                       "every step; the faster of the calls issued eagerly and the same calls captured in a CUDA "
-                       "graph (" + ("graph" if e2e_ms <= e2e_eager_ms else "eager") + ")",
-                "graph_value": round(tokens_per_second(world, wl.M, e2e_ms), 1),
-                "eager_value": round(tokens_per_second(world, wl.M, e2e_eager_ms), 1)},
-        "clocks": clocks,
+        "config": workload_config(args.workload, wl, world),
+        "path": desc,
+        "l2": f"inputs larger than L2: {m['copies']} rotating weight+input copies "
+              f"({m['copies'] * m['per_copy'] / 1e6:.0f} MB > 2x L2), no flush",
+        "timing": "CUDA events around one CUDA graph of exactly K steps, PDL chained",
+        "roofline": roofline(B, wl, kname, m, peaks, peak_src, args.workload),
+        "step_hbm_frac": round(nb["step"] / (ms_step * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+        "gpu_launches": launches * K,
+        "e2e": e2e,
+        "clocks": m["clocks"],
     }
-    if gemm:
-        line["step_fp8_frac"] = round(step_flops(wl) / (ms_step * 1e-3) / 1e12 / (peaks["bf16_tflops"] * FP8_OVER_BF16), 4)
+    if kname in ("gemm", "gemm_pair"):
+        line["step_fp8_frac"] = round(step_flops(wl) / (ms_step * 1e-3) / 1e12 /
+                                      (peaks["bf16_tflops"] * FP8_OVER_BF16), 4)
+    st = m["st"]
+    del m
+    torch.cuda.empty_cache()
+    if args.also != "none" and args.also != args.workload:
+        line[args.also] = secondary(args, args.also, dev, world, peaks, peak_src)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, st, budget_s=args.cpu_budget)
     return line
@@ -498,21 +595,53 @@ def run_ours(args, wl, rank, world, local_rank):
 
 # ------------------------------------------------------------ oracle (CPU)
 
-def cpu_baseline(wl, st, budget_s: float = 15.0, threads: int = 1):
-    """The CPU oracle as it stands, on a bounded sample of the workload's rows."""
+def cpu_info() -> dict:
+    model = platform.processor() or platform.machine()
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return {"nproc": os.cpu_count(), "cpu_model": model, "machine": platform.machine()}
+
+
+class OneCore:
+    """Pin this process to one host core for the duration (restored after)."""
+
+    def __enter__(self):
+        self.old = None
+        self.core = None
+        if hasattr(os, "sched_getaffinity"):
+            self.old = os.sched_getaffinity(0)
+            self.core = max(self.old)  # the last core: away from core 0's interrupts
+            os.sched_setaffinity(0, {self.core})
+        return self
+
+    def __exit__(self, *exc):
+        if self.old is not None:
+            os.sched_setaffinity(0, self.old)
+
+
+def cpu_baseline(wl, st, budget_s: float = 15.0):
+    """The CPU oracle as it stands, single-threaded on one pinned core, on a
+    bounded sample of the workload's rows."""
     import oracle
 
     oracle.build()
     ref = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in st.items()}
-    rows_done, t0 = 0, time.perf_counter()
-    r = 0
-    while time.perf_counter() - t0 < budget_s:
-        oracle.run_rows(wl, ref, [r % wl.M], threads=threads)
-        rows_done += 1
-        r += 1
-    dt = time.perf_counter() - t0
-    return {"value": round(rows_done / dt, 3), "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"{rows_done} token rows of the {wl.name} step, one at a time, single-threaded, {dt:.1f} s"}
+    rows_done = 0
+    with OneCore() as pin:
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < budget_s:
+            oracle.run_rows(wl, ref, [rows_done % wl.M], threads=1)
+            rows_done += 1
+        dt = time.perf_counter() - t0
+    return {"value": round(rows_done / dt, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{rows_done} token rows of the {wl.name} step, one at a time, single-threaded on core "
+                      f"{pin.core}, {dt:.1f} s", **cpu_info()}
 
 
 def run_reference(args, wl):
@@ -524,24 +653,26 @@ def run_reference(args, wl):
     # one step = one token row of the workload (the full prologue, projection
     # and head epilogue of that token); the steps timed are capped so the run
     # stays within the budget
-    t0 = time.perf_counter()
-    for i in range(min(args.warmup, 3)):
-        oracle.run_rows(wl, ref, [i % wl.M], threads=1)
-    t_row = (time.perf_counter() - t0) / max(1, min(args.warmup, 3))
-    steps = max(1, min(args.steps, int(args.cpu_budget * 4 / max(t_row, 1e-6))))
-    t0 = time.perf_counter()
-    for i in range(steps):
-        oracle.run_rows(wl, ref, [i % wl.M], threads=1)
-    dt = time.perf_counter() - t0
+    with OneCore() as pin:
+        t0 = time.perf_counter()
+        for i in range(min(args.warmup, 3)):
+            oracle.run_rows(wl, ref, [i % wl.M], threads=1)
+        t_row = (time.perf_counter() - t0) / max(1, min(args.warmup, 3))
+        steps = max(1, min(args.steps, int(args.cpu_budget * 4 / max(t_row, 1e-6))))
+        t0 = time.perf_counter()
+        for i in range(steps):
+            oracle.run_rows(wl, ref, [i % wl.M], threads=1)
+        dt = time.perf_counter() - t0
     v = steps / dt
-    sample = f"{steps} of the {args.steps} requested steps timed; a step = one token row of {wl.name}, single-threaded"
+    sample = (f"{steps} of the {args.steps} requested steps timed; a step = one token row of {wl.name}, "
+              f"single-threaded on core {pin.core}")
     return {"metric": METRIC, "value": round(v, 3), "unit": "tokens/s", "n_gpus": args.gpus, "steps": steps,
             "warmup": args.warmup, "ms_per_step": dt / steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64/f32 (CPU oracle)", "data": "synthetic",
-            "config": {"workload": args.workload, "hidden": wl.H, "nkv": wl.nkv, "M": wl.M, "N": wl.N,
-                       "weight": wl.weight_fmt, "cache": wl.cache_fmt},
-            "impl": "reference",
-            "cpu_baseline": {"value": round(v, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "config": workload_config(args.workload, wl, args.gpus),
+            "path": "the CPU oracle (plain C, single-threaded), one token row a step", "impl": "reference",
+            "cpu_baseline": {"value": round(v, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample,
+                             **cpu_info()},
             "e2e": {"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -552,6 +683,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference", "ours"])
     ap.add_argument("--workload", default="decode")
+    ap.add_argument("--also", default="prefill",
+                    help="a second workload timed in the same run and reported under its name (none: skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--gemm", default="auto", choices=["auto", "single", "pair"],

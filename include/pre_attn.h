@@ -256,23 +256,35 @@ int pre_attn_set_profile_events(pa_handle *h, void *before_main, void *after_mai
  * runtime that owns all device memory through its own pool and hands none
  * out, or a process whose device memory is capped so that any cudaMalloc
  * after start-up fails.
- * It runs the same step as pre_attn_run (same arguments minus the workspace)
- * for 0 <= M <= 16 token rows, with the kernels' scratch (status word,
- * quantised activations and their scales) in a fixed
- * 2 MiB array inside this library; every GPU that loads the library holds
- * that array until the process exits.  It calls no cudaMalloc, cudaFree or
- * allocating library routine.
- *   - The first call on a device looks up the array's device address (with
- *     that device current); make that first call before any stream capture.
+ * It runs the same step as pre_attn_run (same arguments minus the workspace;
+ * the kernels are the ones pre_attn_path(h, M) names) for 0 <= M <= 16 token
+ * rows, with the kernels' scratch (status word, quantised activations and
+ * their scales) in a fixed 2 MiB array inside this library; every GPU that
+ * loads the library holds that array until the process exits.  It calls no
+ * cudaMalloc, cudaFree or allocating library routine.
+ *   - The array's device address is looked up (cudaGetSymbolAddress, with the
+ *     device current) by the first call on each device, and again by the
+ *     first call on a new context of that device (after cudaDeviceReset);
+ *     make the first call before any stream capture.
  *   - All calls share the one array and each clears the part it uses first
  *     (cudaMemsetAsync on `stream`); calls that overlap on the GPU (other
  *     streams, other host threads) race on it, so order them.
- *   - The device status word (PA_DEV_*) lives in that shared array and is
- *     not readable through this entry point.
+ *   - The device status word (PA_DEV_*) of the last call on a device is read
+ *     with pre_attn_noalloc_status.
  * Errors: those of pre_attn_run, and PA_ERR_SHAPE when M > 16, M > the
- * handle's max_tokens, or pre_attn_workspace_bytes(h, M) exceeds 2 MiB. */
+ * handle's max_tokens, or pre_attn_workspace_bytes(h, M) exceeds 2 MiB;
+ * PA_ERR_CUDA (with pre_attn_last_cuda_error) when the lookup or the clear
+ * fails. */
 int pre_attn_run_noalloc(pa_handle *h, int M, const pa_step_inputs *in, const pa_weights *wt,
                          const pa_caches *caches, const pa_outputs *out, void *stream);
+
+/* Read and clear the device status word (PA_DEV_* bits) that the last
+ * pre_attn_run_noalloc on the current device left in the library's static
+ * scratch, into *flags (host).  Each pre_attn_run_noalloc starts from a
+ * cleared word, so the bits describe that one call.  Synchronises `stream`;
+ * allocates nothing.  The pages have no counterpart (see
+ * pre_attn_run_noalloc).  Errors: PA_ERR_NULL, PA_ERR_CUDA. */
+int pre_attn_noalloc_status(uint32_t *flags, void *stream);
 
 /* Main kernels a call can run (pre_attn_path). */
 enum {

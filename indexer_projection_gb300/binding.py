@@ -100,6 +100,7 @@ def load(path: str = LIB_PATH):
         "pre_attn_set_profile_events": (i, [H, _vp, _vp]),
         "pre_attn_run_noalloc": (i, [H, i, ctypes.POINTER(pa_step_inputs), ctypes.POINTER(pa_weights),
                                      ctypes.POINTER(pa_caches), ctypes.POINTER(pa_outputs), _vp]),
+        "pre_attn_noalloc_status": (i, [u32p, _vp]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -201,8 +202,18 @@ def pre_attn_run_noalloc(h, M: int, inputs: pa_step_inputs, weights: pa_weights,
     st = load().pre_attn_run_noalloc(h, int(M), ctypes.byref(inputs), ctypes.byref(weights),
                                      ctypes.byref(caches), ctypes.byref(outputs), stream_ptr(stream))
     if check and st != PA_OK:
-        raise PreAttnError(st, "pre_attn_run_noalloc")
+        extra = pre_attn_last_cuda_error() if st == PA_ERR_CUDA else ""
+        raise PreAttnError(st, "pre_attn_run_noalloc " + extra)
     return st
+
+
+def pre_attn_noalloc_status(stream=None) -> int:
+    """PA_DEV_* bits of the last pre_attn_run_noalloc on the current device (read and cleared)."""
+    v = ctypes.c_uint32(0)
+    st = load().pre_attn_noalloc_status(ctypes.byref(v), stream_ptr(stream))
+    if st != PA_OK:
+        raise PreAttnError(st, "pre_attn_noalloc_status " + (pre_attn_last_cuda_error() if st == PA_ERR_CUDA else ""))
+    return int(v.value)
 
 
 def pre_attn_set_profile_events(h, before_main=None, after_main=None) -> None:

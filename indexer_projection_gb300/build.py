@@ -7,6 +7,7 @@ of include/pre_attn.h.
 
 from __future__ import annotations
 
+import hashlib
 import os
 import shutil
 import subprocess
@@ -16,6 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libpre_attn.so")
+STAMP = LIB + ".sha256"
 SOURCES = ["pa_api.cu", "pa_prologue.cu", "pa_gemv.cu", "pa_gemm.cu", "pa_gemm2.cu", "pa_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
@@ -29,17 +31,38 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
+def source_hash() -> str:
+    """sha256 of everything the library is built from: the sources and headers
+    under csrc/, the public header, this file (flags, source list) and nvcc's
+    version line."""
+    h = hashlib.sha256()
+    deps = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC)) + [os.path.join(ROOT, "include", "pre_attn.h"),
+                                                                     os.path.abspath(__file__)]
+    for d in deps:
+        h.update(os.path.basename(d).encode())
+        with open(d, "rb") as f:
+            h.update(f.read())
+    try:
+        h.update(subprocess.run([nvcc(), "--version"], capture_output=True, text=True).stdout.encode())
+    except (RuntimeError, OSError):
+        pass
+    return h.hexdigest()
+
+
 def _stale() -> bool:
-    if not os.path.exists(LIB):
+    """The library is rebuilt unless it exists and its stamp records the hash
+    of the current sources (file times are not trusted: a copied tree or an
+    archive can make an old binary look newer than its sources)."""
+    if not (os.path.exists(LIB) and os.path.exists(STAMP)):
         return True
-    t = os.path.getmtime(LIB)
-    deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(ROOT, "include", "pre_attn.h"), __file__]
-    return any(os.path.getmtime(d) > t for d in deps)
+    with open(STAMP) as f:
+        return f.read().strip() != source_hash()
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
     if not force and not _stale():
         return LIB
+    digest = source_hash()
     out_dir = os.path.join(ROOT, "_build")
     os.makedirs(out_dir, exist_ok=True)
     cc = nvcc()
@@ -64,6 +87,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(STAMP, "w") as f:
+        f.write(digest + "\n")
     return LIB
 
 

@@ -102,6 +102,10 @@ bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb) {
 
 }  // namespace
 
+namespace pa {
+int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+}  // namespace pa
+
 extern "C" {
 
 const char *pre_attn_strerror(int s) {

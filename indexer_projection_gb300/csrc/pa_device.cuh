@@ -1,6 +1,6 @@
 // Device-side building blocks of the pre-attention step for sm_103a:
 // kernel parameters, PTX wrappers (mbarrier, bulk copies, programmatic
-// dependent launch, legacy mma.sync for the skinny path), FP8 / FP4 codecs
+// dependent launch, thread-block clusters), FP8 / FP4 codecs
 // and the per-head epilogue (Gemma RMSNorm, partial NeoX RoPE, q / index_q
 // outputs, FP8 and NVFP4 paged-cache insertion).
 //
@@ -252,19 +252,6 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
           smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
-}
-
-// ---------------------------------------------------- legacy warp MMA (FP8)
-// D[16x8] += A[16x32] * B[32x8], e4m3 inputs, f32 accumulate.  Fragments:
-// a0: (row g, k 4t..4t+3), a1: (g+8, 4t..), a2: (g, 16+4t..), a3: (g+8, 16+4t..);
-// b0: (k 4t.., col g), b1: (k 16+4t.., col g); c0,c1: (g, 2t, 2t+1), c2,c3: (g+8, ..).
-__device__ __forceinline__ void mma_e4m3_16832(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                               uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // ================================================================ epilogue

@@ -70,7 +70,7 @@ __device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.syn
 
 template <int WFMT>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p,
+    pa_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p,
                 int use_pdl) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -298,7 +298,7 @@ cudaError_t launch_gemm(const Params &p, int num_sms, int grid_override, bool pd
   const int tiles = ((p.M + kBM - 1) / kBM) * (p.N / kBN);
   int grid = grid_override > 0 ? grid_override : num_sms;
   if (grid > tiles) grid = tiles;
-  auto kern = p.weight_fmt == 0 ? gemm_kernel<0> : gemm_kernel<1>;
+  auto kern = p.weight_fmt == 0 ? pa_gemm_kernel<0> : pa_gemm_kernel<1>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), kGemmSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};

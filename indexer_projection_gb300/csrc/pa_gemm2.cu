@@ -31,6 +31,7 @@
 
 #include "pa_device.cuh"
 #include "pa_launch.h"
+#include "pa_tc.cuh"
 
 namespace pa {
 namespace g2 {
@@ -68,27 +69,18 @@ __device__ __forceinline__ void tma_2d_pair(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-__device__ __forceinline__ uint64_t sdesc_sf(uint32_t saddr) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
-}
 // M = 256 (the pair), N = 256, A and B E4M3, K-major.
-constexpr uint32_t kIdescF8 = (1u << 4) | ((uint32_t)(256 >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
-constexpr uint32_t kIdescMx = ((uint32_t)(256 >> 3) << 17) | (1u << 23) | ((uint32_t)(256 >> 4) << 24);
+constexpr uint32_t kIdescF8 = idesc_f8(256, 256);
+constexpr uint32_t kIdescMx = idesc_mx(256, 256);
 
-__device__ __forceinline__ void mma_f8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+__device__ __forceinline__ void mma_f8_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile(
       "{.reg .pred p; setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;}" ::"r"(d),
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
-__device__ __forceinline__ void mma_mx(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa, uint32_t sfb,
+__device__ __forceinline__ void mma_mx_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa, uint32_t sfb,
                                        uint32_t acc) {
   asm volatile(
       "{.reg .pred p; setp.ne.b32 p, %6, 0;\n\t"
@@ -96,7 +88,7 @@ __device__ __forceinline__ void mma_mx(uint32_t d, uint64_t a, uint64_t b, uint3
       "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
       : "memory");
 }
-__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+__device__ __forceinline__ void tc_cp_sf_pair(uint32_t taddr, uint64_t sdesc) {
   asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 // arrive once on the barrier at this offset in both CTAs of the pair
@@ -107,21 +99,6 @@ __device__ __forceinline__ void tc_commit_pair(uint64_t *bar) {
       "h"((uint16_t)3)
       : "memory");
 }
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // The cluster's tiles, in order: tile c, c + C, ... as a running count of
 // K steps (u = tile * ksteps), each tile's K steps [ks0, ks1) = [0, ksteps).
@@ -151,7 +128,7 @@ struct Segs {
 
 template <int WFMT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+    pa_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB, Params p,
                  int use_pdl) {
   extern __shared__ uint8_t smem_raw[];
@@ -257,18 +234,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint64_t ad = sdesc_sw128(a0 + stage * kTile), bd = sdesc_sw128(b0 + stage * kTile);
           if (WFMT == 1) {
-            tc_cp_sf(tmem + kSfaCol, sdesc_sf(sfa0 + stage * 1024));
-            tc_cp_sf(tmem + kSfbCol, sdesc_sf(sfb0 + stage * 1024));
-            tc_cp_sf(tmem + kSfbCol + 4, sdesc_sf(sfb0 + stage * 1024 + kSf));
+            tc_cp_sf_pair(tmem + kSfaCol, sdesc_sf(sfa0 + stage * 1024));
+            tc_cp_sf_pair(tmem + kSfbCol, sdesc_sf(sfb0 + stage * 1024));
+            tc_cp_sf_pair(tmem + kSfbCol + 4, sdesc_sf(sfb0 + stage * 1024 + kSf));
           }
 #pragma unroll
           for (int k = 0; k < kBK / 32; ++k) {
             const uint32_t acc = ks > sg.ks0 || k > 0;
             if (WFMT == 0) {
-              mma_f8(tmem, ad + 2 * k, bd + 2 * k, kIdescF8, acc);
+              mma_f8_pair(tmem, ad + 2 * k, bd + 2 * k, kIdescF8, acc);
             } else {
               const uint32_t idesc = kIdescMx | ((uint32_t)k << 4) | ((uint32_t)k << 29);
-              mma_mx(tmem, ad + 2 * k, bd + 2 * k, idesc, tmem + kSfaCol, tmem + kSfbCol, acc);
+              mma_mx_pair(tmem, ad + 2 * k, bd + 2 * k, idesc, tmem + kSfaCol, tmem + kSfbCol, acc);
             }
           }
           tc_commit_pair(&empty[stage]);
@@ -408,7 +385,7 @@ cudaError_t launch_gemm_pair(const Params &p, int num_sms, int grid_override, bo
   int clusters = (grid_override > 0 ? grid_override : num_sms) / 2;
   if (clusters < 1) clusters = 1;
   if (clusters > tiles) clusters = tiles;
-  auto kern = p.weight_fmt == 0 ? g2::gemm2_kernel<0> : g2::gemm2_kernel<1>;
+  auto kern = p.weight_fmt == 0 ? g2::pa_gemm_pair_kernel<0> : g2::pa_gemm_pair_kernel<1>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), g2::kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};

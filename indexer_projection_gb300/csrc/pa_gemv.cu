@@ -233,7 +233,7 @@ __device__ __forceinline__ void fused_norm_quant(const Params &p, int tid, int k
 }
 
 template <int WFMT, int C, bool FUSED, int CF>
-__global__ void __launch_bounds__(kGvThreads, 3) gemv_kernel(Params p, int kc, int use_pdl) {
+__global__ void __launch_bounds__(kGvThreads, 3) pa_skinny_proj_kernel(Params p, int kc, int use_pdl) {
   static_assert(!FUSED || C == 16, "the fused variant exchanges norm partials among 16 K ranges");
   constexpr int TS = (kMaxTok + C - 1) / C;
   extern __shared__ uint8_t dsm_raw[];
@@ -511,10 +511,10 @@ int pick_cluster(int smem16) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
   if (cached[dev].c && cached[dev].smem >= smem16) return cached[dev].c;
   int c = 8;
-  const void *k16[4] = {reinterpret_cast<const void *>(gemv_kernel<WFMT, 16, false, 0>),
-                        reinterpret_cast<const void *>(gemv_kernel<WFMT, 16, true, 0>),
-                        reinterpret_cast<const void *>(gemv_kernel<WFMT, 16, false, 1>),
-                        reinterpret_cast<const void *>(gemv_kernel<WFMT, 16, true, 1>)};
+  const void *k16[4] = {reinterpret_cast<const void *>(pa_skinny_proj_kernel<WFMT, 16, false, 0>),
+                        reinterpret_cast<const void *>(pa_skinny_proj_kernel<WFMT, 16, true, 0>),
+                        reinterpret_cast<const void *>(pa_skinny_proj_kernel<WFMT, 16, false, 1>),
+                        reinterpret_cast<const void *>(pa_skinny_proj_kernel<WFMT, 16, true, 1>)};
   bool failed = false;
   for (const void *k : k16) {
     if (!failed) failed = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess;
@@ -545,7 +545,7 @@ template <int WFMT, int C, bool FUSED, int CF>
 cudaError_t launch_c(const Params &p, bool pdl, cudaStream_t stream) {
   const int kc = gv_kc(p.H, C);
   const int smem = gv_smem(C, kc, WFMT);
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemv_kernel<WFMT, C, FUSED, CF>), smem);
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(pa_skinny_proj_kernel<WFMT, C, FUSED, CF>), smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
@@ -561,7 +561,7 @@ cudaError_t launch_c(const Params &p, bool pdl, cudaStream_t stream) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, gemv_kernel<WFMT, C, FUSED, CF>, p, kc, (int)pdl);
+  return cudaLaunchKernelEx(&cfg, pa_skinny_proj_kernel<WFMT, C, FUSED, CF>, p, kc, (int)pdl);
 }
 
 template <int WFMT>

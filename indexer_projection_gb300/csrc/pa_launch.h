@@ -7,6 +7,9 @@ namespace pa {
 
 struct Params;
 
+// Keep `e` as this thread's pre_attn_last_cuda_error() text; returns PA_ERR_CUDA.
+int record_cuda_error(cudaError_t e);
+
 // Raise a kernel's dynamic shared-memory limit once per (kernel, device),
 // kept out of the per-call path so the launch sequence also works inside
 // stream capture.  Keyed on the kernel's address: template instances share

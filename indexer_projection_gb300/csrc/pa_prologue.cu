@@ -1,9 +1,9 @@
 // Prologue of the pre-attention step: residual add, Gemma RMSNorm and the
 // activation quantiser (pa_norm.cuh).
-//   prologue_kernel       one CTA per token row: the tensor-core path's many
+//   pa_prologue_kernel       one CTA per token row: the tensor-core path's many
 //                         rows (HBM-bound: 16-byte coalesced loads and stores,
 //                         the row in registers, block reductions)
-//   prologue_rows_kernel  one thread-block cluster per token row, a K slice
+//   pa_prologue_rows_kernel  one thread-block cluster per token row, a K slice
 //                         per CTA: the skinny path's few rows, whose latency
 //                         the step waits on; the correctly rounded norm costs
 //                         ~30 instructions an element, too much for a few
@@ -24,7 +24,7 @@ namespace pa {
 // the per-element work of the correctly rounded norm is spread 4x wider and
 // the row is done sooner.
 template <int WFMT, int NTHR, int MAXC>
-__global__ void __launch_bounds__(NTHR) prologue_kernel(Params p, int use_pdl) {
+__global__ void __launch_bounds__(NTHR) pa_prologue_kernel(Params p, int use_pdl) {
   __shared__ float2 red2[NTHR / 32];
   if (use_pdl) {
     pdl_trigger();
@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(NTHR) prologue_kernel(Params p, int use_pdl) {
 // wait CTA 0 of the row prefetches the row's cos / sin line for the GEMV's
 // head epilogue.
 template <int WFMT, int C, int NT = 128 * 16 / C>
-__global__ void __launch_bounds__(NT) prologue_rows_kernel(Params p, int kc, int use_pdl) {
+__global__ void __launch_bounds__(NT) pa_prologue_rows_kernel(Params p, int kc, int use_pdl) {
   constexpr int NTHR = NT;
   constexpr int W = NTHR / 32;
   constexpr int XB = WFMT == 0 ? 16 : 8;  // bytes a CTA sends to each CTA
@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(NT) prologue_rows_kernel(Params p, int kc, int
   if (cs_thread && cpos >= 0 && cpos < p.max_pos) prefetch_l2(p.cos_sin + cpos * kRotDim);
 }
 
-__global__ void pack_scales_kernel(const uint8_t *src, uint8_t *dst, int rows, int ksf) {
+__global__ void pa_pack_scales_kernel(const uint8_t *src, uint8_t *dst, int rows, int ksf) {
   const int64_t rpad = ((int64_t)rows + 127) / 128 * 128;
   const int64_t total = rpad * ksf;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
@@ -184,18 +184,18 @@ namespace {
 cudaError_t launch_1024(const Params &p, cudaLaunchConfig_t &cfg, bool pdl) {
   cfg.blockDim = dim3(1024);
   const bool mx = p.weight_fmt == 1;
-  if (mx) return cudaLaunchKernelEx(&cfg, prologue_kernel<1, 1024, 2>, p, (int)pdl);  // (one chunk spills)
-  if (p.H <= 8 * 1024) return cudaLaunchKernelEx(&cfg, prologue_kernel<0, 1024, 1>, p, (int)pdl);
-  return cudaLaunchKernelEx(&cfg, prologue_kernel<0, 1024, 2>, p, (int)pdl);
+  if (mx) return cudaLaunchKernelEx(&cfg, pa_prologue_kernel<1, 1024, 2>, p, (int)pdl);  // (one chunk spills)
+  if (p.H <= 8 * 1024) return cudaLaunchKernelEx(&cfg, pa_prologue_kernel<0, 1024, 1>, p, (int)pdl);
+  return cudaLaunchKernelEx(&cfg, pa_prologue_kernel<0, 1024, 2>, p, (int)pdl);
 }
 cudaError_t launch_256(const Params &p, cudaLaunchConfig_t &cfg, bool pdl) {
   cfg.blockDim = dim3(256);
   const int maxc = (p.H + 8 * 256 - 1) / (8 * 256);
   const bool mx = p.weight_fmt == 1;
-  if (maxc <= 2) return cudaLaunchKernelEx(&cfg, mx ? prologue_kernel<1, 256, 2> : prologue_kernel<0, 256, 2>, p, (int)pdl);
-  if (maxc <= 3) return cudaLaunchKernelEx(&cfg, mx ? prologue_kernel<1, 256, 3> : prologue_kernel<0, 256, 3>, p, (int)pdl);
-  if (maxc <= 4) return cudaLaunchKernelEx(&cfg, mx ? prologue_kernel<1, 256, 4> : prologue_kernel<0, 256, 4>, p, (int)pdl);
-  return cudaLaunchKernelEx(&cfg, mx ? prologue_kernel<1, 256, 8> : prologue_kernel<0, 256, 8>, p, (int)pdl);
+  if (maxc <= 2) return cudaLaunchKernelEx(&cfg, mx ? pa_prologue_kernel<1, 256, 2> : pa_prologue_kernel<0, 256, 2>, p, (int)pdl);
+  if (maxc <= 3) return cudaLaunchKernelEx(&cfg, mx ? pa_prologue_kernel<1, 256, 3> : pa_prologue_kernel<0, 256, 3>, p, (int)pdl);
+  if (maxc <= 4) return cudaLaunchKernelEx(&cfg, mx ? pa_prologue_kernel<1, 256, 4> : pa_prologue_kernel<0, 256, 4>, p, (int)pdl);
+  return cudaLaunchKernelEx(&cfg, mx ? pa_prologue_kernel<1, 256, 8> : pa_prologue_kernel<0, 256, 8>, p, (int)pdl);
 }
 }  // namespace
 
@@ -234,8 +234,8 @@ cudaError_t launch_rows(const Params &p, bool pdl, cudaStream_t stream) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  if (small) return cudaLaunchKernelEx(&cfg, prologue_rows_kernel<WFMT, C, 128 * 8 / C>, p, kc, (int)pdl);
-  return cudaLaunchKernelEx(&cfg, prologue_rows_kernel<WFMT, C>, p, kc, (int)pdl);
+  if (small) return cudaLaunchKernelEx(&cfg, pa_prologue_rows_kernel<WFMT, C, 128 * 8 / C>, p, kc, (int)pdl);
+  return cudaLaunchKernelEx(&cfg, pa_prologue_rows_kernel<WFMT, C>, p, kc, (int)pdl);
 }
 
 }  // namespace
@@ -254,7 +254,7 @@ cudaError_t launch_pack_scales(const uint8_t *src, uint8_t *dst, int rows, int k
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(256);
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, pack_scales_kernel, src, dst, rows, ksf);
+  return cudaLaunchKernelEx(&cfg, pa_pack_scales_kernel, src, dst, rows, ksf);
 }
 
 }  // namespace pa

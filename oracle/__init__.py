@@ -13,6 +13,7 @@ cites the symbol it follows.
 from __future__ import annotations
 
 import ctypes
+import hashlib
 import os
 import subprocess
 import threading
@@ -35,13 +36,20 @@ def build(force: bool = False) -> str:
     ``-ffp-contract=off`` keeps every f32 operation separately rounded, as the
     source is written, on both x86-64 and aarch64.
     """
-    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
-        return _LIB_PATH
+    with open(_SRC, "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()
+    stamp = _LIB_PATH + ".sha256"
+    if not force and os.path.exists(_LIB_PATH) and os.path.exists(stamp):
+        with open(stamp) as f:
+            if f.read().strip() == digest:
+                return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
     subprocess.check_call(
         ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
          "-Wall", "-o", tmp, _SRC, "-lm"])
     os.replace(tmp, _LIB_PATH)
+    with open(stamp, "w") as f:
+        f.write(digest + "\n")
     return _LIB_PATH
 
 
