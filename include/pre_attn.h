@@ -110,9 +110,14 @@ enum pa_flags {
   PA_FLAG_FUSE = 1 << 6,            /* skinny path in one kernel (the row normalisation inside the
                                        GEMV's clusters) where the shape allows; measured slower than
                                        prologue + GEMV at the decode shape, so not the default */
-  PA_FLAG_EXACT_NORM = 1 << 7       /* testing: the many-row prologue computes every activation code
+  PA_FLAG_EXACT_NORM = 1 << 7,      /* testing: the many-row prologue computes every activation code
                                        from the exact normalised value (the fast path's fallback);
                                        results are bitwise the same as without it */
+  PA_FLAG_TEST_WAIT_TIMEOUT = 1 << 8 /* testing: every bounded device wait gives up after 200 us
+                                       instead of about a second, and the main kernel's epilogue
+                                       also waits on a barrier nothing arrives on, so the wait runs
+                                       out: the step's outputs and done words are not written and
+                                       PA_DEV_WAIT_TIMEOUT is raised, as a real timeout would */
 };
 
 /* ----------------------------------------------------------- config */
@@ -181,6 +186,17 @@ typedef struct pa_outputs {
   void *iq;         /* [M, n_iq*128] bf16 index_q */
   void *iq_fp8;     /* [M, n_iq*128] e4m3 index_q, unit scale */
   float q_fp8_scale;/* dequantisation scale of q_fp8 (> 0) */
+  /* Signal mode (pre_attn page, emit_pre_attn.publish_done / emit_k1's done
+   * flags): NULL, or [M, n_heads] uint32 done words (4-byte aligned).  Word
+   * m * n_heads + head is set to done_epoch once that (token, head) row's
+   * outputs and cache bytes are written, with release semantics at GPU
+   * scope: a consumer that reads done_epoch there with an acquire load (as
+   * pre_attn_wait_done does) then sees every byte of the row, and the row's
+   * residual.  The words are never cleared by the library: give each step a
+   * new epoch (a step counter) and the consumer waits for equality.  A row
+   * whose epilogue did not run (a device wait ran out) keeps its old word. */
+  uint32_t *done;
+  uint32_t done_epoch; /* != 0 when done is given */
 } pa_outputs;
 
 /* --------------------------------------------------------- entry points */
@@ -285,6 +301,23 @@ int pre_attn_run_noalloc(pa_handle *h, int M, const pa_step_inputs *in, const pa
  * allocates nothing.  The pages have no counterpart (see
  * pre_attn_run_noalloc).  Errors: PA_ERR_NULL, PA_ERR_CUDA. */
 int pre_attn_noalloc_status(uint32_t *flags, void *stream);
+
+/* The consumer side of signal mode: wait on `stream` until each of the
+ * `count` uint32 words at `done` (device) equals `epoch`, reading them with
+ * acquire loads at GPU scope, then return (a kernel that waits and exits;
+ * work queued behind it on the stream sees the rows those words cover).  It
+ * may be launched with programmatic dependent launch right behind
+ * pre_attn_run on the same stream: then it starts while the step's last
+ * kernel runs (that kernel never waits on it) and follows the rows as they
+ * are published.  Each wait is bounded by timeout_us (1 .. 10^7
+ * microseconds); a word that does not reach `epoch` in time sets
+ * PA_DEV_WAIT_TIMEOUT in the device word *status (device, e.g. a workspace's
+ * status word, read with pre_attn_device_status) and the kernel returns.
+ * Errors (nothing launched): PA_ERR_NULL, PA_ERR_SHAPE (count < 1),
+ * PA_ERR_CONFIG (epoch == 0 or timeout_us out of range), PA_ERR_ALIGN;
+ * PA_ERR_CUDA if the launch fails. */
+int pre_attn_wait_done(const uint32_t *done, int64_t count, uint32_t epoch, uint32_t timeout_us, uint32_t *status,
+                       void *stream);
 
 /* Main kernels a call can run (pre_attn_path). */
 enum {

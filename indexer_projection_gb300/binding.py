@@ -27,6 +27,7 @@ PA_WEIGHT_FP8_PER_CHANNEL, PA_WEIGHT_MXFP8 = 0, 1
 PA_CACHE_FP8, PA_CACHE_NVFP4 = 0, 1
 PA_FLAG_STATIC_KV_SCALE, PA_FLAG_FORCE_GEMV, PA_FLAG_FORCE_GEMM, PA_FLAG_NO_PDL = 1, 2, 4, 8
 PA_FLAG_GEMM_SINGLE, PA_FLAG_GEMM_PAIR, PA_FLAG_FUSE, PA_FLAG_EXACT_NORM = 16, 32, 64, 128
+PA_FLAG_TEST_WAIT_TIMEOUT = 256
 PA_PATH_GEMV, PA_PATH_GEMM_SINGLE, PA_PATH_GEMM_PAIR, PA_PATH_GEMV_FUSED = 0, 1, 2, 3
 
 _vp = ctypes.c_void_p
@@ -61,7 +62,7 @@ class pa_caches(ctypes.Structure):
 
 class pa_outputs(ctypes.Structure):
     _fields_ = [("residual", _vp), ("q", _vp), ("q_fp8", _vp), ("iq", _vp), ("iq_fp8", _vp),
-                ("q_fp8_scale", ctypes.c_float)]
+                ("q_fp8_scale", ctypes.c_float), ("done", _vp), ("done_epoch", ctypes.c_uint32)]
 
 
 class PreAttnError(RuntimeError):
@@ -101,6 +102,7 @@ def load(path: str = LIB_PATH):
         "pre_attn_run_noalloc": (i, [H, i, ctypes.POINTER(pa_step_inputs), ctypes.POINTER(pa_weights),
                                      ctypes.POINTER(pa_caches), ctypes.POINTER(pa_outputs), _vp]),
         "pre_attn_noalloc_status": (i, [u32p, _vp]),
+        "pre_attn_wait_done": (i, [_vp, ctypes.c_int64, ctypes.c_uint32, ctypes.c_uint32, _vp, _vp]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -225,6 +227,13 @@ def pre_attn_set_profile_events(h, before_main=None, after_main=None) -> None:
     st = load().pre_attn_set_profile_events(h, ev(before_main), ev(after_main))
     if st != PA_OK:
         raise PreAttnError(st, "pre_attn_set_profile_events")
+
+
+def pre_attn_wait_done(done, count: int, epoch: int, timeout_us: int, status, stream=None, check: bool = True) -> int:
+    st = load().pre_attn_wait_done(ptr(done), int(count), int(epoch), int(timeout_us), ptr(status), stream_ptr(stream))
+    if check and st != PA_OK:
+        raise PreAttnError(st, "pre_attn_wait_done " + (pre_attn_last_cuda_error() if st == PA_ERR_CUDA else ""))
+    return st
 
 
 def pre_attn_device_status(workspace, stream=None) -> int:

@@ -247,6 +247,8 @@ int pre_attn_run(pa_handle *h, int M, const pa_step_inputs *in, const pa_weights
     if (!(cc->k_global_scale > 0.0f) || !(cc->v_global_scale > 0.0f)) return PA_ERR_CONFIG;
   }
   if (out->q_fp8 && !(out->q_fp8_scale > 0.0f)) return PA_ERR_CONFIG;
+  if (out->done && out->done_epoch == 0) return PA_ERR_CONFIG;
+  if (out->done && !aligned(out->done, 4)) return PA_ERR_ALIGN;
   // alignment (16-byte vector accesses; 256 for the workspace)
   const void *a16[] = {in->ar, in->res, out->residual, wt->w, wt->w_scale, wt->g_in, wt->g_q, wt->g_k,
                        wt->g_iq, wt->g_ik, wt->cos_sin, out->q, out->q_fp8, out->iq, out->iq_fp8,
@@ -333,6 +335,9 @@ int pre_attn_run(pa_handle *h, int M, const pa_step_inputs *in, const pa_weights
   p.q_fp8 = static_cast<uint8_t *>(out->q_fp8);
   p.iq_fp8 = static_cast<uint8_t *>(out->iq_fp8);
   p.q_fp8_inv = out->q_fp8 ? 1.0f / out->q_fp8_scale : 1.0f;
+  p.done = out->done;
+  p.done_epoch = out->done_epoch;
+  p.test_timeout = (c.flags & PA_FLAG_TEST_WAIT_TIMEOUT) ? 1 : 0;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   p.status = reinterpret_cast<uint32_t *>(ws + L.status);
   p.x_scale = reinterpret_cast<float *>(ws + L.x_scale);

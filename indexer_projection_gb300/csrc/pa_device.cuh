@@ -54,6 +54,9 @@ struct Params {
   __nv_bfloat16 *residual, *q, *iq;
   uint8_t *q_fp8, *iq_fp8;
   float q_fp8_inv;           // 1 / q_fp8_scale (f32 reciprocal)
+  uint32_t *done;            // [M, n_heads] done words (NULL: none), set to done_epoch
+  uint32_t done_epoch;
+  int test_timeout;          // testing: a wait that cannot complete, with a short limit
   // workspace
   uint32_t *status;
   uint8_t *xq;               // [M, H] e4m3 activations
@@ -152,15 +155,23 @@ __device__ __forceinline__ uint64_t globaltimer() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// Wait for phase `parity` of an mbarrier, giving up after about a second:
-// the caller's results are then invalid and PA_DEV_WAIT_TIMEOUT is raised.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *status) {
+// Limit of every bounded device wait: about a second; with the testing flag
+// PA_FLAG_TEST_WAIT_TIMEOUT, kTestWaitNs (every wait of the kernels is then
+// short enough for a test to run one out on purpose).
+constexpr uint64_t kWaitNs = 1000000000ull;
+constexpr uint64_t kTestWaitNs = 200000ull;
+__device__ __forceinline__ uint64_t wait_limit(const Params &p) { return p.test_timeout ? kTestWaitNs : kWaitNs; }
+
+// Wait for phase `parity` of an mbarrier, giving up after limit_ns: the
+// caller's results are then invalid and PA_DEV_WAIT_TIMEOUT is raised.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *status,
+                                          uint64_t limit_ns = kWaitNs) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
     if (mbar_try_wait(a, parity)) return true;
-    if (globaltimer() - t0 > 1000000000ull) {
+    if (globaltimer() - t0 > limit_ns) {
       set_status(status, kDevWaitTimeout);
       return false;
     }
@@ -222,9 +233,10 @@ __device__ __forceinline__ void st_async_v4(uint32_t caddr, float4 v, uint32_t c
                : "memory");
 }
 // Wait for phase `parity` of a local mbarrier whose arrivals come from other
-// CTAs of the cluster (acquire at cluster scope), giving up after about a
-// second (PA_DEV_WAIT_TIMEOUT).
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, uint32_t *status) {
+// CTAs of the cluster (acquire at cluster scope), giving up after limit_ns
+// (PA_DEV_WAIT_TIMEOUT).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, uint32_t *status,
+                                                  uint64_t limit_ns = kWaitNs) {
   const uint32_t a = smem_u32(bar);
   auto try_wait = [&]() {
     uint32_t ok;
@@ -237,7 +249,7 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity
   const uint64_t t0 = globaltimer();
   while (true) {
     if (try_wait()) return true;
-    if (globaltimer() - t0 > 1000000000ull) {
+    if (globaltimer() - t0 > limit_ns) {
       set_status(status, kDevWaitTimeout);
       return false;
     }
@@ -403,7 +415,7 @@ __device__ __forceinline__ int64_t load_pos(const Params &p, int m) {
 // CF: the cache format when known at compile time (0 FP8, 1 NVFP4; the other
 // format's code is then left out of the kernel), else -1 (p.cache_fmt).
 template <int E, int CF = -1>
-__device__ __forceinline__ void head_epilogue(const Params &p, const HeadCtx &hc, float (&v)[E], int d0) {
+__device__ __forceinline__ void head_epilogue_stores(const Params &p, const HeadCtx &hc, float (&v)[E], int d0) {
   const int h = hc.head;
   const bool is_q = h < p.k0, is_k = h >= p.k0 && h < p.v0, is_v = h >= p.v0 && h < p.iq0;
   const bool is_iq = h >= p.iq0 && h < p.ik0;
@@ -582,6 +594,34 @@ __device__ __forceinline__ void head_epilogue(const Params &p, const HeadCtx &hc
       slot_base[bs * 64 + off] = sf;
     }
   }
+}
+
+// Signal mode ("vllm.models.minimax_m3.amd.mono.kernels.pre_attn",
+// emit_pre_attn.publish_done and emit_k1's done flags): once the (token,
+// head) row's stores (outputs and cache bytes) are made, its done word
+// done[m * n_heads + head] is set to done_epoch with release semantics at
+// GPU scope, so a consumer that reads the epoch there with an acquire load
+// then sees every byte of that row.  E < 128 (a warp per row): each lane
+// fences its own stores, the warp synchronises, lane 0 releases.  E = 128 (a
+// thread per row): the release orders the thread's own stores.
+template <int E>
+__device__ __forceinline__ void publish_done(const Params &p, const HeadCtx &hc, int d0) {
+  if (!p.done) return;
+  uint32_t *w = p.done + (int64_t)hc.m * p.n_heads + hc.head;
+  if constexpr (E < kHeadDim) {
+    __threadfence();
+    __syncwarp();
+    if (d0 == 0) asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(w), "r"(p.done_epoch) : "memory");
+  } else {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(w), "r"(p.done_epoch) : "memory");
+  }
+}
+
+// The epilogue of one head row, then its done word (when asked for).
+template <int E, int CF = -1>
+__device__ __forceinline__ void head_epilogue(const Params &p, const HeadCtx &hc, float (&v)[E], int d0) {
+  head_epilogue_stores<E, CF>(p, hc, v, d0);
+  publish_done<E>(p, hc, d0);
 }
 
 }  // namespace pa

@@ -50,8 +50,8 @@ struct GemmSmem {  // offsets from the 1024-aligned base
   static constexpr int b = a + kStages * kTileBytes;
   static constexpr int sfa = b + kStages * kTileBytes;
   static constexpr int sfb = sfa + kStages * kSfBytes;
-  static constexpr int bars = sfb + kStages * kSfBytes;  // full[S], empty[S], tfull[2], tempty[2]
-  static constexpr int tmem_addr = bars + (2 * kStages + 4) * 8;
+  static constexpr int bars = sfb + kStages * kSfBytes;  // full[S], empty[S], tfull[2], tempty[2], never, drain
+  static constexpr int tmem_addr = bars + (2 * kStages + 6) * 8;
   static constexpr int ok = tmem_addr + 8;                // 2 x int: tile verdicts
   static constexpr int wscale = ok + 8;                   // 2 x 128 f32: per-channel weight scales of a head
   static constexpr int total = wscale + 2 * kBN * 4;
@@ -78,6 +78,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t *empty = full + kStages;
   uint64_t *tfull = empty + kStages;
   uint64_t *tempty = tfull + 2;
+  uint64_t *never = tempty + 2;  // testing: nothing arrives on it
+  uint64_t *drain = never + 1;   // the MMA issuer's last commit on an abnormal exit
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + GemmSmem::tmem_addr);
   float *ws_s = reinterpret_cast<float *>(smem + GemmSmem::wscale);
   volatile int *ok_s = reinterpret_cast<volatile int *>(smem + GemmSmem::ok);
@@ -98,6 +100,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], kBM / 32);  // one arrival per epilogue warp
     }
+    mbar_init(never, 1);
+    mbar_init(drain, 1);
     fence_mbar_init();
   }
   if (warp == 4 && lane == 0) {
@@ -126,13 +130,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       const uint32_t tx = 2 * kTileBytes + (WFMT == 1 ? 2 * kSfBytes : 0);
       bool ok = true;
+      int last_ph[kStages];  // phase each stage was last loaded with (-1: never)
+#pragma unroll
+      for (int i = 0; i < kStages; ++i) last_ph[i] = -1;
       for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
         const int mt = t / n_tiles, nt = t - mt * n_tiles;
         for (int ks = 0; ks < ksteps; ++ks) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, p.status)) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, p.status, wait_limit(p))) {
             ok = false;
             break;
           }
+          last_ph[stage] = (int)phase;
           mbar_expect_tx(&full[stage], tx);
           tma_2d(smem + GemmSmem::a + stage * kTileBytes, &tmA, ks * kBK, mt * kBM, &full[stage]);
           tma_2d(smem + GemmSmem::b + stage * kTileBytes, &tmB, ks * kBK, nt * kBN, &full[stage]);
@@ -148,6 +156,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
       }
+      // a wait ran out: the copies already issued land before the CTA exits
+      if (!ok)
+#pragma unroll
+        for (int i = 0; i < kStages; ++i)
+          if (last_ph[i] >= 0) mbar_wait(&full[i], (uint32_t)last_ph[i], p.status, wait_limit(p));
     }
   } else if (warp == 5) {
     // --------------------------------------------------------- MMA issuer
@@ -160,11 +173,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t a0 = smem_u32(smem + GemmSmem::a), b0 = smem_u32(smem + GemmSmem::b);
       const uint32_t sfa0 = smem_u32(smem + GemmSmem::sfa), sfb0 = smem_u32(smem + GemmSmem::sfb);
       for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-        if (!mbar_wait(&tempty[abuf], aphase ^ 1, p.status)) break;
+        if (!mbar_wait(&tempty[abuf], aphase ^ 1, p.status, wait_limit(p))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t dacc = tmem + abuf * kBN;
         for (int ks = 0; ks < ksteps; ++ks) {
-          if (!mbar_wait(&full[stage], phase, p.status)) {
+          if (!mbar_wait(&full[stage], phase, p.status, wait_limit(p))) {
             ok = false;
             break;
           }
@@ -198,6 +214,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           aphase ^= 1;
         }
       }
+      if (!ok) {  // a wait ran out: the MMAs already issued complete before the TMEM is freed
+        tc_commit(drain);
+        mbar_wait(drain, 0, p.status, wait_limit(p));
+      }
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -209,7 +229,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int mt = t / n_tiles, nt = t - mt * n_tiles;
       // one thread waits; the verdict and the head's per-channel weight
       // scales are shared through double-buffered shared memory
-      if (row == 0) ok_s[it & 1] = mbar_wait(&tfull[abuf], aphase, p.status) ? 1 : 0;
+      if (row == 0)
+        ok_s[it & 1] = mbar_wait(&tfull[abuf], aphase, p.status, wait_limit(p)) &&
+                               !(p.test_timeout && !mbar_wait(never, 0, p.status, wait_limit(p)))
+                           ? 1
+                           : 0;
       if (WFMT == 0) ws_s[(it & 1) * kBN + row] = __ldg(p.w_scale + nt * kBN + row);
       named_bar(1, kBM);
       if (!ok_s[it & 1]) break;

@@ -50,8 +50,8 @@ struct Smem {  // offsets from the 1024-aligned base
   static constexpr int b = a + kStages * kTile;
   static constexpr int sfa = b + kStages * kTile;
   static constexpr int sfb = sfa + kStages * 1024;          // 1024-aligned slots
-  static constexpr int bars = sfb + kStages * 1024;          // full[S], empty[S], tfull, tempty
-  static constexpr int tmem_addr = bars + (2 * kStages + 2) * 8;
+  static constexpr int bars = sfb + kStages * 1024;          // full[S], empty[S], tfull, tempty, never, drain
+  static constexpr int tmem_addr = bars + (2 * kStages + 4) * 8;
   static constexpr int ok = tmem_addr + 8;                   // 2 x int (+ 8 bytes: keeps wscale 16-aligned)
   static constexpr int wscale = ok + 16;                     // [2 parity][2 heads][128] f32
   static constexpr int total = wscale + 2 * 2 * 128 * 4;
@@ -137,6 +137,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t *empty = full + kStages;
   uint64_t *tfull = empty + kStages;
   uint64_t *tempty = tfull + 1;
+  uint64_t *never = tempty + 1;  // testing: nothing arrives on it
+  uint64_t *drain = never + 1;   // the MMA issuer's last commit on an abnormal exit
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Smem::tmem_addr);
   volatile int *ok_s = reinterpret_cast<volatile int *>(smem + Smem::ok);
   float *ws_s = reinterpret_cast<float *>(smem + Smem::wscale);
@@ -156,6 +158,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     mbar_init(tfull, 1);
     mbar_init(tempty, 4);  // one arrival per epilogue warpgroup of each CTA
+    mbar_init(never, 1);
+    mbar_init(drain, 1);
     fence_mbar_init();
   }
   if (warp == 8 && lane == 0) {
@@ -187,14 +191,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       const uint32_t tx = 2 * kTile + (WFMT == 1 ? 3 * kSf : 0);
       bool ok = true;
+      int last_ph[kStages];  // phase each stage was last armed with (-1: never)
+#pragma unroll
+      for (int i = 0; i < kStages; ++i) last_ph[i] = -1;
       for (Segs sg(cluster, clusters, tiles, ksteps); sg.valid() && ok; sg.next()) {
         const int mp = sg.tile / n_tiles, nt = sg.tile - mp * n_tiles;
         const int m_tile = 2 * mp + (int)rank;
         for (int ks = sg.ks0; ks < sg.ks1; ++ks) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, p.status)) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, p.status, wait_limit(p))) {
             ok = false;
             break;
           }
+          last_ph[stage] = (int)phase;
           const uint32_t fb = full0 + stage * 8;
           // CTA 0 expects both CTAs' bytes on its own barrier (a local
           // arrival); CTA 1's loads just complete their bytes there.  A
@@ -214,6 +222,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
       }
+      // a wait ran out: the copies already issued (both CTAs' bytes count on
+      // CTA 0's stage barriers) land before the pair passes its final cluster
+      // barrier
+      if (!ok && rank == 0)
+#pragma unroll
+        for (int i = 0; i < kStages; ++i)
+          if (last_ph[i] >= 0) mbar_wait(&full[i], (uint32_t)last_ph[i], p.status, wait_limit(p));
     }
   } else if (warp == 9) {
     // -------------------------------------------------- MMA issuer (CTA 0)
@@ -224,10 +239,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t a0 = smem_u32(smem + Smem::a), b0 = smem_u32(smem + Smem::b);
       const uint32_t sfa0 = smem_u32(smem + Smem::sfa), sfb0 = smem_u32(smem + Smem::sfb);
       for (Segs sg(cluster, clusters, tiles, ksteps); sg.valid() && ok; sg.next()) {
-        if (!mbar_wait(tempty, aphase ^ 1, p.status)) break;
+        if (!mbar_wait(tempty, aphase ^ 1, p.status, wait_limit(p))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         for (int ks = sg.ks0; ks < sg.ks1; ++ks) {
-          if (!mbar_wait(&full[stage], phase, p.status)) {
+          if (!mbar_wait(&full[stage], phase, p.status, wait_limit(p))) {
             ok = false;
             break;
           }
@@ -257,6 +275,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_commit_pair(tfull);
         aphase ^= 1;
       }
+      if (!ok) {  // a wait ran out: the MMAs already issued complete before the TMEM is freed
+        tc_commit_pair(drain);
+        mbar_wait(drain, 0, p.status, wait_limit(p));
+      }
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -268,7 +290,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (Segs sg(cluster, clusters, tiles, ksteps); sg.valid(); sg.next(), ++it) {
       const int mp = sg.tile / n_tiles, nt = sg.tile - mp * n_tiles;
       const int head = 2 * nt + wg;
-      if (erow == 0) ok_s[it & 1] = mbar_wait(tfull, aphase, p.status) ? 1 : 0;
+      if (erow == 0)
+        ok_s[it & 1] = mbar_wait(tfull, aphase, p.status, wait_limit(p)) &&
+                               !(p.test_timeout && !mbar_wait(never, 0, p.status, wait_limit(p)))
+                           ? 1
+                           : 0;
       if (WFMT == 0) {
         const int n = head * 128 + row;
         ws_s[((it & 1) * 2 + wg) * 128 + row] = n < p.N ? __ldg(p.w_scale + n) : 0.f;

@@ -117,6 +117,7 @@ struct GvStatic {
   uint64_t mma_bar;              // the MMAs of a batch have completed
   uint64_t recv_bar;             // partial rows received (transaction bytes)
   uint64_t ex1_bar;              // fused: the cluster's norm partials received
+  uint64_t never_bar;            // testing (PA_FLAG_TEST_WAIT_TIMEOUT): nothing arrives on it
   uint32_t tmem;
   int ok;
 };
@@ -182,7 +183,7 @@ __device__ __forceinline__ void fused_norm_quant(const Params &p, int tid, int k
                    "f"(sh), "f"(sl), "r"(mapa(smem_u32(ex1_bar), sub))
                    : "memory");
   }
-  const bool ok1 = mbar_wait_cluster(ex1_bar, 0, p.status);
+  const bool ok1 = mbar_wait_cluster(ex1_bar, 0, p.status, wait_limit(p));
   float rh = 0.f, rl = 0.f;
   if (active && ok1) {
     float th = ex1[m].x, tl = ex1[m].y;  // the 16 K ranges in order: the same sum in every CTA
@@ -263,6 +264,7 @@ __global__ void __launch_bounds__(kGvThreads, 3) pa_skinny_proj_kernel(Params p,
       mbar_init(&ss.ex1_bar, 1);
       mbar_expect_tx(&ss.ex1_bar, (uint32_t)(16 * M * (WFMT == 0 ? 16 : 8)));
     }
+    mbar_init(&ss.never_bar, 1);
     ss.ok = 1;
     fence_mbar_init();
   }
@@ -414,7 +416,7 @@ __global__ void __launch_bounds__(kGvThreads, 3) pa_skinny_proj_kernel(Params p,
       tc_commit(&ss.mma_bar);
     }
     // every thread: the batch's MMAs are done (its stages may be refilled)
-    if (!mbar_wait(&ss.mma_bar, bi & 1, p.status)) ss.ok = 0;
+    if (!mbar_wait(&ss.mma_bar, bi & 1, p.status, wait_limit(p))) ss.ok = 0;
     __syncthreads();
     if (!ss.ok) break;
   }
@@ -466,7 +468,11 @@ __global__ void __launch_bounds__(kGvThreads, 3) pa_skinny_proj_kernel(Params p,
   if (warp >= TS) return;
   const int m = ks + C * warp;
   if (m >= M) return;
-  if (!mbar_wait_cluster(&ss.recv_bar, 0, p.status)) return;
+  if (!mbar_wait_cluster(&ss.recv_bar, 0, p.status, wait_limit(p))) return;
+  // testing: a wait that cannot complete (all partials are in, so nothing of
+  // the cluster writes here any more), run out like a real one: the row's
+  // outputs and done word are skipped and PA_DEV_WAIT_TIMEOUT is raised
+  if (p.test_timeout && !mbar_wait(&ss.never_bar, 0, p.status, wait_limit(p))) return;
   const int d0 = 4 * lane;
   float y[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll

@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(NT) pa_prologue_rows_kernel(Params p, int kc, 
                    "f"(th), "f"(tl), "r"(mapa(smem_u32(&bar1), tid))
                    : "memory");
   }
-  const bool ok1 = mbar_wait_cluster(&bar1, 0, p.status);
+  const bool ok1 = mbar_wait_cluster(&bar1, 0, p.status, wait_limit(p));
   // the C partials combined by a fixed shuffle tree (lane l starts from
   // partial l % C) and taken from lane 0: the same sum and maximum in every
   // warp of every CTA of the cluster

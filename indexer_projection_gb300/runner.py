@@ -61,8 +61,10 @@ class PreAttn:
         return c
 
     @staticmethod
-    def outputs(residual=None, q=None, q_fp8=None, iq=None, iq_fp8=None, q_fp8_scale: float = 1.0) -> B.pa_outputs:
-        return B.pa_outputs(B.ptr(residual), B.ptr(q), B.ptr(q_fp8), B.ptr(iq), B.ptr(iq_fp8), q_fp8_scale)
+    def outputs(residual=None, q=None, q_fp8=None, iq=None, iq_fp8=None, q_fp8_scale: float = 1.0, done=None,
+                done_epoch: int = 0) -> B.pa_outputs:
+        return B.pa_outputs(B.ptr(residual), B.ptr(q), B.ptr(q_fp8), B.ptr(iq), B.ptr(iq_fp8), q_fp8_scale,
+                            B.ptr(done), done_epoch)
 
     def run(self, M: int, ar, res, positions, slot_mapping, weights: B.pa_weights, caches: B.pa_caches,
             outputs: B.pa_outputs, index_slot_mapping=None, stream=None, check: bool = True) -> int:

@@ -246,8 +246,19 @@ class GpuRun:
         else:
             self.caches = PreAttn.nvfp4_caches(d["kv_cache"], wl.kv_pages, wl.kv_page_bytes, d["idx_cache"],
                                                wl.idx_pages, wl.idx_page_bytes, wl.k_global, wl.v_global)
+        self.done = None
+        self.set_done_epoch(0)
+
+    def set_done_epoch(self, epoch: int):
+        """Ask for the step's done words (signal mode) with this epoch (0: none)."""
+        from indexer_projection_gb300.runner import PreAttn
+
+        d, wl = self.d, self.wl
+        if epoch and self.done is None:
+            self.done = self.torch.zeros(max(wl.M, 1) * wl.n_heads, dtype=self.torch.int32, device=self.dev)
         self.outputs = PreAttn.outputs(d.get("residual"), d.get("q_bf16"), d.get("q_fp8"), d.get("iq_bf16"),
-                                       d.get("iq_fp8"), wl.q_fp8_scale)
+                                       d.get("iq_fp8"), wl.q_fp8_scale, done=self.done if epoch else None,
+                                       done_epoch=epoch)
 
     def run(self, M=None, check=True):
         d = self.d

@@ -131,6 +131,17 @@ def test_run_validation_codes(B):
     assert _run(B, h, 4, ins, wt, cc, o3, ws) == B.PA_ERR_NO_IQ_OUTPUT
     o4 = B.pa_outputs(out.residual, out.q, out.q, out.iq, None, 0.0)  # q_fp8 scale 0
     assert _run(B, h, 4, ins, wt, cc, o4, ws) == B.PA_ERR_CONFIG
+    # signal mode: done words need a nonzero epoch and 4-byte alignment
+    o6 = B.pa_outputs(out.residual, out.q, None, out.iq, None, 1.0, (1 << 32) + (1 << 30), 0)
+    assert _run(B, h, 4, ins, wt, cc, o6, ws) == B.PA_ERR_CONFIG
+    o7 = B.pa_outputs(out.residual, out.q, None, out.iq, None, 1.0, (1 << 32) + (1 << 30) + 2, 9)
+    assert _run(B, h, 4, ins, wt, cc, o7, ws) == B.PA_ERR_ALIGN
+    L2 = B.load()
+    assert L2.pre_attn_wait_done(None, 4, 1, 10, (1 << 32), None) == B.PA_ERR_NULL
+    assert L2.pre_attn_wait_done((1 << 32), 0, 1, 10, (1 << 32), None) == B.PA_ERR_SHAPE
+    assert L2.pre_attn_wait_done((1 << 32), 4, 0, 10, (1 << 32), None) == B.PA_ERR_CONFIG
+    assert L2.pre_attn_wait_done((1 << 32), 4, 1, 10**8, (1 << 32), None) == B.PA_ERR_CONFIG
+    assert L2.pre_attn_wait_done((1 << 32) + 2, 4, 1, 10, (1 << 32), None) == B.PA_ERR_ALIGN
     i2, *_ = _run_args(B, ar=(1 << 32) + 8)
     assert _run(B, h, 4, i2, wt, cc, out, ws) == B.PA_ERR_ALIGN
     _, _, _, _, ws_bad = _run_args(B, wk=(1 << 32) + 64)
