@@ -551,6 +551,93 @@ def secondary(args, name, dev, world, peaks, peak_src):
     return out
 
 
+def index_bytes(iw, st, init, local) -> int:
+    """Algorithmic bytes of one indexer-score launch: each scored key block
+    read once (16 KB), the index_q rows, the block table and lengths, and
+    every score column written (4 bytes, -inf included)."""
+    total = iw.M * 128 * 2 + st["block_table"].nbytes + st["seq_lens"].nbytes
+    for r in range(iw.R):
+        seq = int(st["seq_lens"][r])
+        rows_p = [seq - iw.q_len + i for i in range(iw.q_len)]
+        need = set()
+        for p in rows_p:
+            nb = p // 128 + 1
+            total += nb * 128 * 4
+            need |= {b for b in range(nb) if init <= b < nb - local}
+        total += len(need) * 128 * 128
+    return total
+
+
+def index_secondary(args, name, dev, world, peaks):
+    """The indexer scores of a configuration's shape, timed on their own: a
+    CUDA graph of launches over keys larger than L2."""
+    import torch
+
+    from indexer_projection_gb300 import binding as B
+
+    iw = workloads.INDEX_CONFIGS[name]()
+    st = workloads.index_host_state(iw)
+    init, local = iw.init_blocks, iw.local_blocks
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    d = {k: t(st[k].view(np.int16) if k == "iq" else st[k]) for k in ("iq", "index_cache", "block_table", "seq_lens")}
+    cols = iw.bt_width * 128
+    scores = torch.empty(iw.M, cols, dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    scale = B.pre_attn_index_scale_log2e(iw.sm_scale)
+    a = B.pa_index_args(B.ptr(d["iq"]), 128 * iw.n_iq, iw.head, B.ptr(d["index_cache"]), d["index_cache"].numel() // 128,
+                        B.ptr(d["block_table"]), B.ptr(d["seq_lens"]), iw.R, iw.q_len, iw.bt_width, init, local,
+                        scale, B.ptr(scores), cols, B.ptr(status))
+    stream = torch.cuda.Stream(dev)
+    K = max(20, min(args.steps, 200))
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            B.pre_attn_index_scores(a, stream)
+        g = torch.cuda.CUDAGraph()
+    stream.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(K):
+            B.pre_attn_index_scores(a, stream)
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 1
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(200e-6 * 2.1e9))
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    reps = max(1, math.ceil(1.0e3 / max(e0.elapsed_time(e1), 1e-3)))
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(200e-6 * 2.1e9))
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    t1 = time.time()
+    ms = max_over_ranks([e0.elapsed_time(e1)], world, dev)[0] / (reps * K)
+    time.sleep(0.06)
+    clocks = sampler.summary(t0, t1)
+    sampler.stop()
+    nbytes = index_bytes(iw, st, init, local)
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    del g
+    return {"config": {"workload": name, "requests": iw.R, "q_len": iw.q_len, "bt_width": iw.bt_width,
+                       "seq_lens": f"U[{iw.seq_lo}, {iw.seq_hi})", "init_blocks": init, "local_blocks": local},
+            "kernel": "pa_index_scores_kernel (TMA key blocks, ldmatrix + mma.sync bf16)",
+            "us_per_launch": round(ms * 1e3, 3), "launches": reps * K,
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                         "algorithmic_bytes": nbytes},
+            "status": int(status.item()), "clocks": clocks}
+
+
 def run_ours(args, wl, rank, world, local_rank):
     import torch
 
@@ -590,8 +677,11 @@ def run_ours(args, wl, rank, world, local_rank):
     st = m["st"]
     del m
     torch.cuda.empty_cache()
-    if args.also != "none" and args.also != args.workload:
-        line[args.also] = secondary(args, args.also, dev, world, peaks, peak_src)
+    for name in [x for x in args.also.split(",") if x and x != "none" and x != args.workload]:
+        if name in workloads.INDEX_CONFIGS:
+            line[name] = index_secondary(args, name, dev, world, peaks)
+        else:
+            line[name] = secondary(args, name, dev, world, peaks, peak_src)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, st, budget_s=args.cpu_budget)
     return line
@@ -687,8 +777,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference", "ours"])
     ap.add_argument("--workload", default="decode")
-    ap.add_argument("--also", default="prefill",
-                    help="a second workload timed in the same run and reported under its name (none: skip)")
+    ap.add_argument("--also", default="prefill,index_spec_decode",
+                    help="comma-separated workloads also timed in the same run, each reported under its name "
+                         "(the step's configurations, or an indexer-score configuration); none: skip")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--gemm", default="auto", choices=["auto", "single", "pair"],

@@ -319,6 +319,55 @@ int pre_attn_noalloc_status(uint32_t *flags, void *stream);
 int pre_attn_wait_done(const uint32_t *done, int64_t count, uint32_t epoch, uint32_t timeout_us, uint32_t *status,
                        void *stream);
 
+/* ------------------------------------------------------ indexer scores */
+
+/* The indexer scores that follow the step (page "vllm.models.minimax_m3.amd.
+ * mono.kernels.pre_attn", emit_k1: "then every CTA's indexer scores";
+ * build_pre_attn_kernel: index_scale_log2e(sm_scale) and the sparse pinned
+ * init / local blocks).  The pages do not print emit_index_scores' body; this
+ * is the reading: request r (r < R) owns rows m = r * q_len + i (i < q_len) at
+ * positions p = seq_lens[r] - q_len + i; row m's page-128 blocks are
+ * b < nb = p / 128 + 1, of which b < init_blocks and b >= nb - local_blocks
+ * are pinned (attended anyway, no score); key j sits at index slot
+ * block_table[r * bt_width + j / 128] * 128 + j % 128 of the FP8 index cache.
+ * Row m of `scores`, columns j < nb * 128:
+ *   index_scale * sum_d bf16(iq[m][head*128 + d]) * e4m3(key_j[d])  (j <= p, block not pinned)
+ *   -inf                                                              (otherwise)
+ * with f32 accumulation; columns from nb * 128 on are not written.  All
+ * pointers are device pointers owned by the caller. */
+typedef struct pa_index_args {
+  const void *iq;             /* [R * q_len, iq_stride] bf16 (the step's index_q output), 8-byte aligned */
+  int64_t iq_stride;          /* elements a row: a multiple of 4, >= (head + 1) * 128 */
+  int head;                   /* the index_q head scored (128 dims at column head * 128) */
+  const void *index_cache;    /* [num_index_slots, 128] E4M3, unit scale (PA_CACHE_FP8's index cache), 16-byte aligned */
+  int64_t num_index_slots;    /* a multiple of 128 (whole page-128 blocks) */
+  const int32_t *block_table; /* [R, bt_width] page-128 block ids (entries past a request's blocks unused) */
+  const int32_t *seq_lens;    /* [R] tokens of each request, the step's q_len rows included */
+  int R;                      /* requests, 0 .. 65535 */
+  int q_len;                  /* rows a request, 1 .. 16 */
+  int bt_width;               /* block-table width */
+  int init_blocks;            /* pinned first blocks */
+  int local_blocks;           /* pinned last blocks (the local window) */
+  float index_scale;          /* pre_attn_index_scale_log2e(sm_scale) */
+  float *scores;              /* [R * q_len, score_stride] f32 */
+  int64_t score_stride;       /* floats a row: >= bt_width * 128 */
+  uint32_t *status;           /* device status word: PA_DEV_SLOT_RANGE (a block id outside the cache, or a
+                                 request shorter than q_len or longer than its block table: skipped),
+                                 PA_DEV_WAIT_TIMEOUT */
+} pa_index_args;
+
+/* index_scale_log2e(sm_scale) (build_pre_attn_kernel; body not printed):
+ * the reading sm_scale * log2(e), so exp2(score) = exp(sm_scale * q.k). */
+float pre_attn_index_scale_log2e(float sm_scale);
+
+/* Compute the indexer scores on `stream`.  May be launched right behind
+ * pre_attn_run on the same stream: it reads the rows and keys after that
+ * step's kernels complete (programmatic dependent launch).  Allocates
+ * nothing, never synchronises.  Errors (nothing launched): PA_ERR_NULL,
+ * PA_ERR_SHAPE, PA_ERR_CONFIG (negative block counts, NaN scale),
+ * PA_ERR_ALIGN; PA_ERR_CUDA if the launch fails. */
+int pre_attn_index_scores(const pa_index_args *args, void *stream);
+
 /* Main kernels a call can run (pre_attn_path). */
 enum {
   PA_PATH_GEMV = 0,         /* skinny path: prologue, then the FP8 GEMV on one cluster per head */

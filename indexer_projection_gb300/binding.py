@@ -65,6 +65,14 @@ class pa_outputs(ctypes.Structure):
                 ("q_fp8_scale", ctypes.c_float), ("done", _vp), ("done_epoch", ctypes.c_uint32)]
 
 
+class pa_index_args(ctypes.Structure):
+    _fields_ = [("iq", _vp), ("iq_stride", ctypes.c_int64), ("head", ctypes.c_int), ("index_cache", _vp),
+                ("num_index_slots", ctypes.c_int64), ("block_table", _vp), ("seq_lens", _vp), ("R", ctypes.c_int),
+                ("q_len", ctypes.c_int), ("bt_width", ctypes.c_int), ("init_blocks", ctypes.c_int),
+                ("local_blocks", ctypes.c_int), ("index_scale", ctypes.c_float), ("scores", _vp),
+                ("score_stride", ctypes.c_int64), ("status", _vp)]
+
+
 class PreAttnError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
@@ -103,6 +111,8 @@ def load(path: str = LIB_PATH):
                                      ctypes.POINTER(pa_caches), ctypes.POINTER(pa_outputs), _vp]),
         "pre_attn_noalloc_status": (i, [u32p, _vp]),
         "pre_attn_wait_done": (i, [_vp, ctypes.c_int64, ctypes.c_uint32, ctypes.c_uint32, _vp, _vp]),
+        "pre_attn_index_scale_log2e": (ctypes.c_float, [ctypes.c_float]),
+        "pre_attn_index_scores": (i, [ctypes.POINTER(pa_index_args), _vp]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -233,6 +243,17 @@ def pre_attn_wait_done(done, count: int, epoch: int, timeout_us: int, status, st
     st = load().pre_attn_wait_done(ptr(done), int(count), int(epoch), int(timeout_us), ptr(status), stream_ptr(stream))
     if check and st != PA_OK:
         raise PreAttnError(st, "pre_attn_wait_done " + (pre_attn_last_cuda_error() if st == PA_ERR_CUDA else ""))
+    return st
+
+
+def pre_attn_index_scale_log2e(sm_scale: float) -> float:
+    return load().pre_attn_index_scale_log2e(float(sm_scale))
+
+
+def pre_attn_index_scores(args: pa_index_args, stream=None, check: bool = True) -> int:
+    st = load().pre_attn_index_scores(ctypes.byref(args), stream_ptr(stream))
+    if check and st != PA_OK:
+        raise PreAttnError(st, "pre_attn_index_scores " + (pre_attn_last_cuda_error() if st == PA_ERR_CUDA else ""))
     return st
 
 

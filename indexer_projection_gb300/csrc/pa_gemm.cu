@@ -25,12 +25,10 @@
 //
 // Every mbarrier wait is bounded (about a second); a timeout raises
 // PA_DEV_WAIT_TIMEOUT, and the kernel still finishes and frees its TMEM.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include "pa_device.cuh"
 #include "pa_launch.h"
 #include "pa_tc.cuh"
+#include "pa_tma.h"
 
 namespace pa {
 
@@ -287,38 +285,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 // ------------------------------------------------------------------- host
 
-static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void *ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
-// [rows, K] e4m3, K-major: 128 x 128-byte boxes, 128-byte swizzle, rows past
-// the end read as zero.
-static bool make_map(CUtensorMap *map, const void *base, int rows, int K) {
-  auto enc = get_encode();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)K};
-  cuuint32_t box[2] = {kBK, kBM};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 cudaError_t launch_gemm(const Params &p, int num_sms, int grid_override, bool pdl, cudaStream_t stream) {
   if (p.H % kBK || p.N % kBN) return cudaErrorInvalidValue;
   CUtensorMap tmA, tmB;
-  if (!make_map(&tmA, p.xq, p.M, p.H) || !make_map(&tmB, p.w, p.N, p.H)) return cudaErrorInvalidValue;
+  if (!map_rows_sw128(&tmA, p.xq, p.M, p.H, kBK, kBM) || !map_rows_sw128(&tmB, p.w, p.N, p.H, kBK, kBN))
+    return cudaErrorInvalidValue;
   const int tiles = ((p.M + kBM - 1) / kBM) * (p.N / kBN);
   int grid = grid_override > 0 ? grid_override : num_sms;
   if (grid > tiles) grid = tiles;

@@ -26,12 +26,10 @@
 // Every mbarrier wait is bounded (about a second); a timeout raises
 // PA_DEV_WAIT_TIMEOUT and the kernel still reaches its final cluster barrier
 // and frees its TMEM.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include "pa_device.cuh"
 #include "pa_launch.h"
 #include "pa_tc.cuh"
+#include "pa_tma.h"
 
 namespace pa {
 namespace g2 {
@@ -354,54 +352,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------- host
 
-static PFN_cuTensorMapEncodeTiled_v12000 get_encode2() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void *ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
-// [rows, K] e4m3, K-major: 128 x 128-byte boxes, 128-byte swizzle, rows past
-// the end read as zero.
-static bool map_operand(CUtensorMap *map, const void *base, int rows, int K) {
-  auto enc = get_encode2();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)K};
-  cuuint32_t box[2] = {g2::kBK, 128};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// F8_128x4 scale atoms as a [row blocks, ksf*16] int64 grid: one box = one
-// 512-byte atom (128 rows x 4 K-blocks); row blocks past the end read as zero.
-static bool map_scales(CUtensorMap *map, const void *base, int row_blocks, int ksf) {
-  auto enc = get_encode2();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)ksf * 16, (cuuint64_t)row_blocks};
-  cuuint64_t strides[1] = {(cuuint64_t)ksf * 128};
-  cuuint32_t box[2] = {64, 1};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_INT64, 2, const_cast<void *>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 cudaError_t launch_gemm_pair(const Params &p, int num_sms, int grid_override, bool pdl, cudaStream_t stream) {
   if (p.H % g2::kBK || p.N % 128) return cudaErrorInvalidValue;
   CUtensorMap tmA, tmB, tmSFA, tmSFB;
   const int ksf = p.H / 32;
-  if (!map_operand(&tmA, p.xq, p.M, p.H) || !map_operand(&tmB, p.w, p.N, p.H)) return cudaErrorInvalidValue;
+  if (!map_rows_sw128(&tmA, p.xq, p.M, p.H, g2::kBK, 128) || !map_rows_sw128(&tmB, p.w, p.N, p.H, g2::kBK, 128))
+    return cudaErrorInvalidValue;
   if (p.weight_fmt == 1) {
-    if (!map_scales(&tmSFA, p.xsf, p.m_pad / 128, ksf) || !map_scales(&tmSFB, p.wsf, p.N / 128, ksf))
+    if (!map_scale_atoms(&tmSFA, p.xsf, p.m_pad / 128, ksf) || !map_scale_atoms(&tmSFB, p.wsf, p.N / 128, ksf))
       return cudaErrorInvalidValue;
   } else {
     tmSFA = tmA;  // unused by the per-channel kernel

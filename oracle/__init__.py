@@ -119,6 +119,9 @@ def lib():
                 "ora_prologue_row": (ctypes.c_int, [vp] * 8),
                 "ora_project_row": (None, [vp, vp, f, vp, vp, vp, vp, vp]),
                 "ora_pre_attn_rows": (ctypes.c_int, [vp, vp, vp, vp, vp, i64, i64, vp, vp, vp, vp]),
+                "ora_index_scale_log2e": (ctypes.c_double, [ctypes.c_double]),
+                "ora_index_scores": (ctypes.c_int, [vp, i64, vp, i64, vp, ctypes.c_int, vp, ctypes.c_int,
+                                                    ctypes.c_int, ctypes.c_int, ctypes.c_int, f, vp, i64]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -230,6 +233,49 @@ def project_row(cfg: Config, xq, x_scale, xsf, w, w_scale, wsf):
 
 class OracleError(RuntimeError):
     pass
+
+
+def index_scale_log2e(sm_scale: float) -> float:
+    return lib().ora_index_scale_log2e(float(sm_scale))
+
+
+def index_scores(iq, index_cache, block_table, seq_lens, q_len: int, init_blocks: int, local_blocks: int,
+                 index_scale: float, score_cols: int, rows=None, threads: int | None = None):
+    """The indexer scores (see ora_index_scores) of a step's rows.
+
+    iq: [M, >=128] bf16 bits (row stride = its second dim); index_cache:
+    [slots, 128] E4M3 codes; block_table: [R, bt_width] int32 page-128 block
+    ids; seq_lens: [R] int32.  Returns [M, score_cols] float32 with NaN in
+    every column the step does not write.  Requests run concurrently on
+    `threads` host threads (they are independent); `rows` restricts the
+    work to the requests holding those rows."""
+    iq = np.ascontiguousarray(iq, np.uint16)
+    cache = np.ascontiguousarray(index_cache, np.uint8).reshape(-1)
+    bt = np.ascontiguousarray(block_table, np.int32)
+    sl = np.ascontiguousarray(seq_lens, np.int32)
+    R, bt_width = bt.shape
+    M = R * q_len
+    assert iq.shape[0] >= M
+    out = np.full((M, score_cols), np.nan, np.float32)
+    reqs = sorted(set(range(R)) if rows is None else {int(m) // q_len for m in rows})
+    L = lib()
+
+    def work(r):
+        rc = L.ora_index_scores(_p(iq[r * q_len:]), iq.shape[1], _p(cache), cache.size // HEAD_DIM,
+                                _p(bt[r:]), bt_width, _p(sl[r:]), 1, q_len, init_blocks, local_blocks,
+                                float(index_scale), _p(out[r * q_len:]), score_cols)
+        return rc
+
+    nthreads = threads or min(max(1, len(reqs)), os.cpu_count() or 1)
+    if nthreads <= 1:
+        rcs = [work(r) for r in reqs]
+    else:
+        with ThreadPoolExecutor(nthreads) as ex:
+            rcs = list(ex.map(work, reqs))
+    bad = [rc for rc in rcs if rc != 0]
+    if bad:
+        raise OracleError(f"oracle index scores returned {bad[0]}")
+    return out
 
 
 def run_rows(wl, state, rows, want_y: bool = False, threads: int | None = None):

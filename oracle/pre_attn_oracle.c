@@ -556,3 +556,66 @@ int ora_pre_attn_rows(const ora_config *c, const ora_inputs *in, const ora_head_
   free(y);
   return rc;
 }
+
+/* ------------------------------------------------ the indexer scores */
+
+/* index_scale_log2e(sm_scale) ([K1] build_pre_attn_kernel; the body is not
+ * printed).  Reading: the attention scale times log2(e), so that
+ * exp2(score) = exp(sm_scale * q.k), the scale an exp2-based softmax over the
+ * scores takes. */
+double ora_index_scale_log2e(double sm_scale) { return sm_scale * (1.0 / log(2.0)); }
+
+/* The indexer scores of a step's rows ([K1] emit_k1: after the step, every
+ * CTA scores the index keys of its requests against the step's index_q;
+ * emit_index_scores' body is not printed, so this is a reading).
+ * Rows: request r (r < R) has q_len consecutive rows m = r * q_len + i at
+ * positions p = seq_lens[r] - q_len + i (the speculative verify rows).
+ * Keys: key j of request r (j <= p: causal) sits in page-128 block
+ * b = j / 128 at index slot block_table[r * bt_width + b] * 128 + j % 128 of
+ * the FP8 index cache (E4M3, unit scale, 128 bytes a slot).  Row m's blocks
+ * are b < nb = p / 128 + 1; the pinned ones (b < init_blocks, the first
+ * blocks, or b >= nb - local_blocks, the local window) are attended anyway
+ * and get no score.
+ * Output, row m of scores (score_stride floats a row), columns j < nb * 128:
+ *   index_scale * sum_d bf16(iq[m][d]) * e4m3(key_j[d])   j <= p, b not pinned
+ *   -inf                                                    otherwise
+ * The dot product is exact in double, rounded to f32 once after the scale.
+ * Columns from nb * 128 on are not written.  iq row m starts at
+ * iq + m * iq_stride (bf16).  Returns ORA_ERR_ARG for a row before position
+ * 0 or beyond the block table, ORA_ERR_SLOT for a key outside the cache. */
+int ora_index_scores(const uint16_t *iq, int64_t iq_stride, const uint8_t *index_cache,
+                     int64_t num_index_slots, const int32_t *block_table, int bt_width,
+                     const int32_t *seq_lens, int R, int q_len, int init_blocks, int local_blocks,
+                     float index_scale, float *scores, int64_t score_stride) {
+  double lut[256];
+  for (int c = 0; c < 256; ++c) lut[c] = (double)ora_e4m3_decode((uint8_t)c);
+  for (int r = 0; r < R; ++r) {
+    for (int i = 0; i < q_len; ++i) {
+      const int64_t m = (int64_t)r * q_len + i;
+      const int64_t p = (int64_t)seq_lens[r] - q_len + i;
+      if (p < 0) return ORA_ERR_ARG;
+      const int64_t nb = p / 128 + 1;
+      if (nb > bt_width || nb * 128 > score_stride) return ORA_ERR_ARG;
+      double q[HEAD_DIM];
+      for (int d = 0; d < HEAD_DIM; ++d) q[d] = ora_bf16_decode(iq[m * iq_stride + d]);
+      for (int64_t b = 0; b < nb; ++b) {
+        const int pinned = b < init_blocks || b >= nb - local_blocks;
+        const int64_t blk = block_table[(int64_t)r * bt_width + b];
+        for (int jj = 0; jj < 128; ++jj) {
+          const int64_t j = b * 128 + jj;
+          float out = -INFINITY;
+          if (!pinned && j <= p) {
+            const int64_t slot = blk * 128 + jj;
+            if (blk < 0 || slot >= num_index_slots) return ORA_ERR_SLOT;
+            const uint8_t *key = index_cache + slot * HEAD_DIM;
+            double s = 0.0;
+            for (int d = 0; d < HEAD_DIM; ++d) s += q[d] * lut[key[d]];
+            out = (float)(s * (double)index_scale);
+          }
+          scores[m * score_stride + j] = out;
+        }
+      }
+    }
+  }
+  return ORA_OK;
+}

@@ -602,3 +602,57 @@ def test_step_nvfp4_caches_decode_consistently():
                 gmax = np.abs(ref).reshape(8, 16).max(axis=1)
                 tol = np.repeat(gmax, 16) / 6 * 1.07 + 1e-6
                 assert np.all(np.abs(deq - ref) <= tol), (m, h, role)
+
+
+# --------------------------------------------------------- indexer scores
+
+def test_index_scale_is_the_attention_scale_times_log2e():
+    # exp2 of the scaled score is exp of sm_scale * q.k: 2^(x log2 e) = e^x
+    for s in (1.0, 128 ** -0.5, 0.03):
+        v = oracle.index_scale_log2e(s)
+        assert abs(v - s * 1.4426950408889634) <= 1e-15 * v
+        assert abs(2.0 ** v - math.e ** s) <= 1e-14 * math.e ** s
+
+
+def _one_request(seq_len, q_len, bt_width, seed):
+    g = np.random.default_rng(seed)
+    nb = (seq_len + 127) // 128
+    bt = np.full((1, bt_width), -1, np.int32)
+    bt[0, :nb] = g.permutation(nb + 5)[:nb]
+    iq = workloads._bf16_bits(torch.randn(q_len, 128, generator=torch.Generator().manual_seed(seed)))
+    keys = workloads._e4m3_bits(torch.randn((nb + 5) * 128, 128, generator=torch.Generator().manual_seed(seed + 1)))
+    return iq, keys, bt, np.array([seq_len], np.int32)
+
+
+def test_index_score_masks_match_the_hand_worked_patterns():
+    rows = _load_golden("index_masks.txt")
+    for seq_len, q_len, init, local, i, lo, hi, written in rows:
+        iq, keys, bt, sl = _one_request(seq_len, q_len, 16, seq_len)
+        out = oracle.index_scores(iq, keys, bt, sl, q_len, init, local, 0.5, 16 * 128)[i]
+        finite = np.isfinite(out)
+        assert np.array_equal(np.nonzero(finite)[0], np.arange(lo, hi)), (seq_len, q_len, init, local, i)
+        assert np.all(np.isneginf(out[:written][~finite[:written]]))
+        assert np.all(np.isnan(out[written:]))
+
+
+def test_index_scores_equal_a_float64_dot_product_of_the_dequantised_rows():
+    iw = workloads.IndexWorkload("pin", R=3, q_len=3, seq_lo=130, seq_hi=900, bt_width=8, seed=11, n_iq=2, head=1)
+    st = workloads.index_host_state(iw)
+    scale = float(np.float32(oracle.index_scale_log2e(iw.sm_scale)))
+    iq = st["iq"][:, 128:256]  # head 1 of each row
+    out = oracle.index_scores(iq, st["index_cache"], st["block_table"], st["seq_lens"], iw.q_len, 1, 1,
+                              scale, 8 * 128)
+    lut = np.array([oracle.e4m3_decode(c) for c in range(256)], np.float64)
+    keys = lut[st["index_cache"].reshape(-1, 128)]
+    qf = (iq.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    checked = 0
+    for m in range(iw.M):
+        r, i = divmod(m, iw.q_len)
+        p = int(st["seq_lens"][r]) - iw.q_len + i
+        for j in np.nonzero(np.isfinite(out[m]))[0]:
+            slot = int(st["block_table"][r, j // 128]) * 128 + j % 128
+            want = np.float32(np.dot(qf[m], keys[slot]) * scale)
+            assert j <= p
+            assert abs(float(out[m, j]) - float(want)) <= abs(float(want)) * 2.0 ** -23, (m, j)
+            checked += 1
+    assert checked > 1000

@@ -292,3 +292,66 @@ def host_state(wl: Workload, with_outputs: bool = True) -> dict:
 
 CACHE_KEYS = ("k_cache", "v_cache", "k_scale", "v_scale", "index_cache", "kv_cache", "idx_cache")
 OUTPUT_KEYS = ("residual", "q_bf16", "q_fp8", "iq_bf16", "iq_fp8")
+
+
+# ------------------------------------------------------------ indexer scores
+
+@dataclass
+class IndexWorkload:
+    """Inputs of the indexer scores: the step's index_q rows, an FP8 index
+    cache holding every key of the requests, page-128 block tables and
+    sequence lengths."""
+    name: str
+    R: int                 # requests
+    q_len: int             # rows a request (speculative verify rows)
+    seq_lo: int            # seq_lens ~ U[seq_lo, seq_hi)
+    seq_hi: int
+    bt_width: int          # block-table width (page-128 blocks)
+    seed: int
+    init_blocks: int = 1   # pinned first blocks
+    local_blocks: int = 4  # pinned local window (blocks)
+    sm_scale: float = 128 ** -0.5
+    n_iq: int = 1          # index_q heads in the iq rows; the scores use head `head`
+    head: int = 0
+
+    @property
+    def M(self) -> int:
+        return self.R * self.q_len
+
+
+def index_decode() -> IndexWorkload:
+    # the decode configuration's shape: 8 requests, one row each, up to 32768 keys
+    return IndexWorkload("index_decode", R=8, q_len=1, seq_lo=1, seq_hi=32769, bt_width=256, seed=1)
+
+
+def index_spec_decode() -> IndexWorkload:
+    # the speculative-decode configuration's shape: 64 requests x 7 rows, seq_lens U[1024, 32768)
+    return IndexWorkload("index_spec_decode", R=64, q_len=7, seq_lo=1024, seq_hi=32768, bt_width=256, seed=2)
+
+
+INDEX_CONFIGS = {"index_decode": index_decode, "index_spec_decode": index_spec_decode}
+
+
+def index_host_state(iw: IndexWorkload) -> dict:
+    """iq [M, n_iq*128] bf16 bits ~ N(0, 1) (a normed index_q has unit RMS);
+    index_cache [blocks * 128, 128] E4M3 codes of N(0, 1) values (the unit-scale
+    FP8 index keys); block_table [R, bt_width] int32 of distinct random blocks
+    (-1 past a request's last block); seq_lens [R] int32."""
+    g = torch.Generator().manual_seed(iw.seed)
+    seq = torch.randint(iw.seq_lo, iw.seq_hi, (iw.R,), generator=g, dtype=torch.int64)
+    seq = torch.maximum(seq, torch.full_like(seq, iw.q_len))
+    nb = (seq + 127) // 128
+    assert int(nb.max()) <= iw.bt_width
+    pool = int(nb.sum()) + 16
+    perm = torch.randperm(pool, generator=g)
+    bt = torch.full((iw.R, iw.bt_width), -1, dtype=torch.int32)
+    nxt = 0
+    for r in range(iw.R):
+        n = int(nb[r])
+        bt[r, :n] = perm[nxt:nxt + n].to(torch.int32)
+        nxt += n
+    st = {"seq_lens": seq.to(torch.int32).numpy().copy(), "block_table": bt.numpy().copy()}
+    st["iq"] = _bf16_bits(torch.randn(iw.M, iw.n_iq * HEAD_DIM, generator=g))
+    keys = torch.randn(pool * 128, HEAD_DIM, generator=g)
+    st["index_cache"] = _e4m3_bits(keys)
+    return st
