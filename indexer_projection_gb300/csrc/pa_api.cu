@@ -17,6 +17,7 @@ struct pa_handle {
   int n_q, n_kv, n_iq, n_heads, N;
   int device;   // device of the cached SM count (-1: not queried yet)
   int num_sms;
+  int64_t l2_bytes;
   cudaEvent_t prof_before, prof_after;  // optional events around the main kernel
 };
 
@@ -32,11 +33,15 @@ int cuda_fail(cudaError_t e) {
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+bool uses_gemv(const pa_config &c, int M) {
+  return (c.flags & PA_FLAG_FORCE_GEMV) ? true : (c.flags & PA_FLAG_FORCE_GEMM) ? false : M <= 16;
+}
+
 // Workspace layout for M rows.  The status word sits at offset 0 and carries
 // state between calls (PA_DEV_* bits, sticky until read); the rest is
 // scratch: the prologue's quantised activations and their scales.
 struct WsLayout {
-  size_t status, x_scale, xsf, xq, total;
+  size_t status, x_scale, xsf, xq, sk_counter, sk_partial, total;
   int m_pad;
 };
 
@@ -53,6 +58,13 @@ WsLayout ws_layout(const pa_handle *h, int M) {
     off = align_up(off + (size_t)(L.m_pad > 0 ? L.m_pad : 128) * (H / 32), 256);
   L.xq = off;
   off = align_up(off + (size_t)M * H, 256);
+  L.sk_counter = L.sk_partial = 0;
+  if (!uses_gemv(h->cfg, M)) {  // the tensor-core path: the pair GEMM's split region
+    L.sk_counter = off;
+    off = align_up(off + sizeof(uint32_t) * pa::kSplitCounterWords, 256);
+    L.sk_partial = off;
+    off = align_up(off + pa::kSplitPartialBytes, 256);
+  }
   L.total = off;
   return L;
 }
@@ -63,36 +75,31 @@ cudaError_t query_sms(pa_handle *h) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (h->device != dev) {
-    int sms = 0;
+    int sms = 0, l2 = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+    if (e != cudaSuccess) return e;
     h->num_sms = sms;
+    h->l2_bytes = l2;
     h->device = dev;
   }
   return cudaSuccess;
 }
 
-bool uses_gemv(const pa_config &c, int M) {
-  return (c.flags & PA_FLAG_FORCE_GEMV) ? true : (c.flags & PA_FLAG_FORCE_GEMM) ? false : M <= 16;
-}
 
-// Main kernel for M rows (h->num_sms known; the skinny path's fusion
-// check queries the device once).  256 x 256 pair tiles cost
-// about 1.5x a 128 x 128 tile on one SM: the pairs are used unless wave
-// quantisation favours the finer tiles.
+// Main kernel for M rows (h->num_sms known; the skinny path's fusion check
+// queries the device once).  The tensor-core path runs on CTA pairs: their
+// 256 x 256 tiles read half the shared-memory bytes a FLOP of 128 x 128 tiles
+// on single SMs, and the pair kernel splits the tiles of a last, partial wave
+// along K across every cluster, so its waves are never quantised; single-SM
+// tiles only on request.
 int choose_path(const pa_handle *h, int M) {
   const pa_config &c = h->cfg;
   if (uses_gemv(c, M))
     return (c.flags & PA_FLAG_FUSE) && pa::gemv_fuses_prologue(c.hidden, c.weight_format) ? PA_PATH_GEMV_FUSED
                                                                                          : PA_PATH_GEMV;
-  if (c.flags & PA_FLAG_GEMM_SINGLE) return PA_PATH_GEMM_SINGLE;
-  if (c.flags & PA_FLAG_GEMM_PAIR) return PA_PATH_GEMM_PAIR;
-  const int sms = h->num_sms > 1 ? h->num_sms : 2;
-  const int64_t t1 = (int64_t)((M + 127) / 128) * (h->N / 128);
-  const int64_t t2 = (int64_t)((M + 255) / 256) * ((h->N + 255) / 256);
-  const int64_t w1 = (t1 + sms - 1) / sms;
-  const int64_t w2 = (t2 + sms / 2 - 1) / (sms / 2);
-  return 3 * w2 <= 2 * w1 ? PA_PATH_GEMM_PAIR : PA_PATH_GEMM_SINGLE;
+  return (c.flags & PA_FLAG_GEMM_SINGLE) ? PA_PATH_GEMM_SINGLE : PA_PATH_GEMM_PAIR;
 }
 
 bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb) {
@@ -166,6 +173,7 @@ int pre_attn_init(const pa_config *cfg, pa_handle **out) {
   if (h->cfg.kv_page_stride == 0) h->cfg.kv_page_stride = 8;
   h->device = -1;
   h->num_sms = 0;
+  h->l2_bytes = 0;
   h->prof_before = h->prof_after = nullptr;
   *out = h;
   return PA_OK;
@@ -344,6 +352,8 @@ int pre_attn_run(pa_handle *h, int M, const pa_step_inputs *in, const pa_weights
   p.xsf = ws + L.xsf;
   p.xq = ws + L.xq;
   p.m_pad = L.m_pad;
+  p.sk_counter = L.sk_counter ? reinterpret_cast<uint32_t *>(ws + L.sk_counter) : nullptr;
+  p.sk_partial = L.sk_partial ? reinterpret_cast<float *>(ws + L.sk_partial) : nullptr;
 
   const bool pdl = !(c.flags & PA_FLAG_NO_PDL);
   cudaStream_t s = (cudaStream_t)stream;
@@ -360,7 +370,7 @@ int pre_attn_run(pa_handle *h, int M, const pa_step_inputs *in, const pa_weights
   if (gemv) {
     e = pa::launch_gemv(p, fused, pdl, s);
   } else {
-    e = path == PA_PATH_GEMM_PAIR ? pa::launch_gemm_pair(p, h->num_sms, c.gemm_grid, pdl, s)
+    e = path == PA_PATH_GEMM_PAIR ? pa::launch_gemm_pair(p, h->num_sms, h->l2_bytes, c.gemm_grid, pdl, s)
                                   : pa::launch_gemm(p, h->num_sms, c.gemm_grid, pdl, s);
   }
   if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;

@@ -42,6 +42,7 @@ constexpr int kThreads = 320;
 constexpr int kEpiThreads = 256;
 constexpr int kTmemCols = 512;
 constexpr int kSfaCol = 256, kSfbCol = 260;
+constexpr int kMinSplitSteps = 8;  // K steps a cluster takes of the split region, at least
 
 struct Smem {  // offsets from the 1024-aligned base
   static constexpr int a = 0;
@@ -50,7 +51,7 @@ struct Smem {  // offsets from the 1024-aligned base
   static constexpr int sfb = sfa + kStages * 1024;          // 1024-aligned slots
   static constexpr int bars = sfb + kStages * 1024;          // full[S], empty[S], tfull, tempty, never, drain
   static constexpr int tmem_addr = bars + (2 * kStages + 4) * 8;
-  static constexpr int ok = tmem_addr + 8;                   // 2 x int (+ 8 bytes: keeps wscale 16-aligned)
+  static constexpr int ok = tmem_addr + 8;                   // 4 x int: tile verdicts, owner-wait verdicts
   static constexpr int wscale = ok + 16;                     // [2 parity][2 heads][128] f32
   static constexpr int total = wscale + 2 * 2 * 128 * 4;
 };
@@ -98,28 +99,111 @@ __device__ __forceinline__ void tc_commit_pair(uint64_t *bar) {
       : "memory");
 }
 
-// The cluster's tiles, in order: tile c, c + C, ... as a running count of
-// K steps (u = tile * ksteps), each tile's K steps [ks0, ks1) = [0, ksteps).
-// The three roles (TMA producer, MMA issuer, epilogue) walk the same
-// sequence.  (Written this way, rather than as a plain loop over t, the
-// kernel compiled to fewer epilogue spills and ran ~5% faster on prefill.)
-struct Segs {
-  int tile, ks0, ks1;
-  int u, u1, ksteps, step;
-  __device__ Segs(int cluster, int clusters, int tiles, int ks) : ksteps(ks) {
-    u = cluster * ksteps;
-    u1 = tiles * ksteps;
-    step = clusters * ksteps;
+// The schedule (chosen on the host, the same for every CTA).
+//   Raster: tiles are numbered in groups of group_m m-pairs; inside a group
+//   the m-pair runs fastest, then the n tile ("vllm.models.minimax_m3.nvidia.
+//   ops.qkv_index_fused_epilogue", QkvIndexFusedEpilogueKernel.tile_coords /
+//   _group_m), so the clusters of one wave share a few weight tiles and a
+//   group's activations stay in L2 while it walks every weight tile: the
+//   weights are read from HBM once per group, not once per wave.
+//   Whole waves: tile w * C + c for cluster c, w < dp_waves.
+//   The remaining tiles (fewer than a wave) are split along K: their
+//   sk_units = tiles x K steps are cut into sk_clusters equal contiguous
+//   ranges, one per cluster, so no cluster idles while another finishes a
+//   last tile alone.  A range starts and ends anywhere inside a tile: the
+//   cluster whose range holds a tile's last K step owns the tile; the
+//   clusters before it that hold its earlier K steps write their partial
+//   sums to the workspace and count them in the tile's counter; the owner
+//   waits (bounded) for the count, adds the partials and runs the epilogue.
+//   A cluster walks its range from its last segment (where it contributes to
+//   the next cluster's tile) to its first (the tile it owns), so every
+//   partial is produced early and owners seldom wait.
+struct Sched {
+  int m_pairs, n_tiles, ksteps, group_m;
+  int dp_waves;     // whole waves of whole tiles
+  int sk_tile0;     // first tile of the split region: dp_waves * clusters
+  int sk_units;     // K steps of the split region
+  int sk_clusters;  // clusters sharing it (0: none)
+};
+
+__device__ __forceinline__ void tile_coords(const Sched &s, int tile, int &mp, int &nt) {
+  const int per = s.group_m * s.n_tiles;
+  const int g = tile / per, idx = tile - g * per;
+  const int gm = s.m_pairs - g * s.group_m < s.group_m ? s.m_pairs - g * s.group_m : s.group_m;
+  nt = idx / gm;
+  mp = g * s.group_m + (idx - nt * gm);
+}
+__device__ __forceinline__ int sk_begin(const Sched &s, int c) {
+  return (int)((int64_t)c * s.sk_units / s.sk_clusters);
+}
+// The cluster whose split range holds unit u.
+__device__ __forceinline__ int sk_cluster_of(const Sched &s, int u) {
+  int c = (int)((int64_t)u * s.sk_clusters / s.sk_units);
+  while (c + 1 < s.sk_clusters && sk_begin(s, c + 1) <= u) ++c;
+  while (c > 0 && sk_begin(s, c) > u) --c;
+  return c;
+}
+
+// Wait until *count reaches `need` (acquire at GPU scope), giving up after
+// limit_ns (PA_DEV_WAIT_TIMEOUT).
+__device__ __forceinline__ int wait_count(const uint32_t *count, uint32_t need, uint32_t *status, uint64_t limit_ns) {
+  auto ld = [&]() {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(count) : "memory");
+    return v;
+  };
+  if (ld() >= need) return 1;
+  const uint64_t t0 = globaltimer();
+  while (ld() < need) {
+    if (globaltimer() - t0 > limit_ns) {
+      set_status(status, kDevWaitTimeout);
+      return 0;
+    }
+    __nanosleep(32);
+  }
+  return 1;
+}
+
+// A cluster's work items, in order: its whole tiles, then its split segments
+// last to first.  The three roles (TMA producer, MMA issuer, epilogue) walk
+// the same sequence.
+struct Work {
+  int tile, ks0, ks1;  // the current item: K steps [ks0, ks1) of tile
+  bool split;          // from the split region
+  int w, hi, u0;       // whole-tile wave; split range [u0, hi) still to walk
+  int ndp, ksteps, sk_tile0, cluster, clusters;  // ndp: this cluster's whole tiles (below sk_tile0)
+  __device__ Work(const Sched &s, int c, int C) : ksteps(s.ksteps), sk_tile0(s.sk_tile0), cluster(c), clusters(C) {
+    ndp = c < s.sk_tile0 ? (s.sk_tile0 - c + C - 1) / C : 0;
+    if (ndp > s.dp_waves) ndp = s.dp_waves;
+    w = 0;
+    split = false;
+    if (s.sk_clusters > 0 && c < s.sk_clusters) {
+      u0 = sk_begin(s, c);
+      hi = sk_begin(s, c + 1);
+    } else {
+      u0 = hi = 0;
+    }
     set();
   }
-  __device__ bool valid() const { return u < u1; }
+  __device__ bool valid() const { return w < ndp || hi > u0; }
   __device__ void set() {
-    tile = u / ksteps;
-    ks0 = u - tile * ksteps;
-    ks1 = ksteps;
+    if (w < ndp) {
+      tile = w * clusters + cluster;
+      ks0 = 0;
+      ks1 = ksteps;
+      split = false;
+    } else if (hi > u0) {
+      const int t = (hi - 1) / ksteps;  // split-region tile of the segment ending at hi
+      const int lo = t * ksteps > u0 ? t * ksteps : u0;
+      tile = sk_tile0 + t;
+      ks0 = lo - t * ksteps;
+      ks1 = hi - t * ksteps;
+      split = true;
+    }
   }
   __device__ void next() {
-    u += step;
+    if (w < ndp) ++w;
+    else hi = (tile - sk_tile0) * ksteps + ks0;  // the walked segment's start
     set();
   }
 };
@@ -128,7 +212,7 @@ template <int WFMT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     pa_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB, Params p,
-                 int use_pdl) {
+                 Sched sc, int use_pdl) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + Smem::bars);
@@ -144,10 +228,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cta_rank();
   const int M = p.M, K = p.H;
-  const int m_pairs = (M + 255) / 256, n_tiles = (p.N + kBN - 1) / kBN;
-  const int tiles = m_pairs * n_tiles;
   const int cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
-  const int ksteps = K / kBK;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -192,8 +273,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int last_ph[kStages];  // phase each stage was last armed with (-1: never)
 #pragma unroll
       for (int i = 0; i < kStages; ++i) last_ph[i] = -1;
-      for (Segs sg(cluster, clusters, tiles, ksteps); sg.valid() && ok; sg.next()) {
-        const int mp = sg.tile / n_tiles, nt = sg.tile - mp * n_tiles;
+      for (Work sg(sc, cluster, clusters); sg.valid() && ok; sg.next()) {
+        int mp, nt;
+        tile_coords(sc, sg.tile, mp, nt);
         const int m_tile = 2 * mp + (int)rank;
         for (int ks = sg.ks0; ks < sg.ks1; ++ks) {
           if (!mbar_wait(&empty[stage], phase ^ 1, p.status, wait_limit(p))) {
@@ -236,7 +318,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true;
       const uint32_t a0 = smem_u32(smem + Smem::a), b0 = smem_u32(smem + Smem::b);
       const uint32_t sfa0 = smem_u32(smem + Smem::sfa), sfb0 = smem_u32(smem + Smem::sfb);
-      for (Segs sg(cluster, clusters, tiles, ksteps); sg.valid() && ok; sg.next()) {
+      for (Work sg(sc, cluster, clusters); sg.valid() && ok; sg.next()) {
         if (!mbar_wait(tempty, aphase ^ 1, p.status, wait_limit(p))) {
           ok = false;
           break;
@@ -285,8 +367,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int erow = wg * 128 + row;       // 0..255 across both warpgroups
     uint32_t aphase = 0;
     int it = 0;
-    for (Segs sg(cluster, clusters, tiles, ksteps); sg.valid(); sg.next(), ++it) {
-      const int mp = sg.tile / n_tiles, nt = sg.tile - mp * n_tiles;
+    for (Work sg(sc, cluster, clusters); sg.valid(); sg.next(), ++it) {
+      int mp, nt;
+      tile_coords(sc, sg.tile, mp, nt);
       const int head = 2 * nt + wg;
       if (erow == 0)
         ok_s[it & 1] = mbar_wait(tfull, aphase, p.status, wait_limit(p)) &&
@@ -317,6 +400,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       named_bar_sync(2 + wg, 128);
       if ((warp & 3) == 0 && lane == 0) arrive_remote(tempty0);
       aphase ^= 1;
+      if (sg.split) {
+        const int slot = sg.tile - sc.sk_tile0;  // the tile among the split ones
+        uint32_t *count = p.sk_counter + slot * 2 + rank;
+        // partial sums: per CTA 256 columns x 128 rows, column-major (a warp
+        // writes and reads 32 consecutive rows of a column)
+        const size_t part = (size_t)kBN * kBM;
+        if (sg.ks1 < sc.ksteps) {  // a contributor: hand the partial to the owner
+          float *dst = p.sk_partial + (size_t)(cluster * 2 + rank) * part + (size_t)(wg * 128) * kBM + row;
+#pragma unroll
+          for (int i = 0; i < 128; ++i) __stcg(dst + i * kBM, v[i]);
+          __threadfence();
+          named_bar_sync(1, kEpiThreads);
+          if (erow == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(count) : "memory");
+          continue;
+        }
+        if (sg.ks0 > 0) {  // the owner: add the partials of the clusters before it
+          const int c_first = sk_cluster_of(sc, slot * sc.ksteps);
+          if (erow == 0) ok_s[2 + (it & 1)] = wait_count(count, (uint32_t)(cluster - c_first), p.status, wait_limit(p));
+          named_bar_sync(1, kEpiThreads);
+          if (!ok_s[2 + (it & 1)]) continue;
+          for (int c2 = c_first; c2 < cluster; ++c2) {
+            const float *src = p.sk_partial + (size_t)(c2 * 2 + rank) * part + (size_t)(wg * 128) * kBM + row;
+#pragma unroll
+            for (int i = 0; i < 128; ++i) v[i] += __ldcg(src + i * kBM);
+          }
+        }
+      }
       const int m = (2 * mp + (int)rank) * kBM + row;
       if (m >= M || head >= p.n_heads) continue;
       if (WFMT == 0) {
@@ -352,7 +462,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------- host
 
-cudaError_t launch_gemm_pair(const Params &p, int num_sms, int grid_override, bool pdl, cudaStream_t stream) {
+cudaError_t launch_gemm_pair(const Params &p, int num_sms, int64_t l2_bytes, int grid_override, bool pdl,
+                             cudaStream_t stream) {
   if (p.H % g2::kBK || p.N % 128) return cudaErrorInvalidValue;
   CUtensorMap tmA, tmB, tmSFA, tmSFB;
   const int ksf = p.H / 32;
@@ -365,16 +476,42 @@ cudaError_t launch_gemm_pair(const Params &p, int num_sms, int grid_override, bo
     tmSFA = tmA;  // unused by the per-channel kernel
     tmSFB = tmB;
   }
-  const int tiles = ((p.M + 255) / 256) * ((p.N + 255) / 256);
+  g2::Sched sc;
+  sc.m_pairs = (p.M + 255) / 256;
+  sc.n_tiles = (p.N + g2::kBN - 1) / g2::kBN;
+  sc.ksteps = p.H / g2::kBK;
+  const int tiles = sc.m_pairs * sc.n_tiles;
   int clusters = (grid_override > 0 ? grid_override : num_sms) / 2;
   if (clusters < 1) clusters = 1;
-  if (clusters > tiles) clusters = tiles;
+  if (clusters > kMaxSplitClusters) clusters = kMaxSplitClusters;
+  // raster groups: a group's activation rows (256 a pair, K bytes each) take
+  // at most a quarter of the L2
+  const int64_t per_pair = (int64_t)256 * p.H;
+  int gm = (int)((l2_bytes / 4) / (per_pair > 0 ? per_pair : 1));
+  sc.group_m = gm < 1 ? 1 : (gm > sc.m_pairs ? sc.m_pairs : gm);
+  int launch_clusters = clusters;
+  sc.dp_waves = tiles / clusters;
+  sc.sk_tile0 = sc.dp_waves * clusters;
+  const int rem = tiles - sc.sk_tile0;
+  if (rem == 0 || !p.sk_partial || !p.sk_counter) {
+    // whole tiles only (no split region, or no workspace for one)
+    if (launch_clusters > tiles) launch_clusters = tiles;
+    sc.dp_waves = (tiles + launch_clusters - 1) / launch_clusters;
+    sc.sk_tile0 = tiles;
+    sc.sk_units = 0;
+    sc.sk_clusters = 0;
+  } else {
+    sc.sk_units = rem * sc.ksteps;
+    const int by_len = sc.sk_units / g2::kMinSplitSteps;
+    sc.sk_clusters = by_len < 1 ? 1 : (by_len > clusters ? clusters : by_len);
+    if (sc.dp_waves == 0) launch_clusters = sc.sk_clusters;
+  }
   auto kern = p.weight_fmt == 0 ? g2::pa_gemm_pair_kernel<0> : g2::pa_gemm_pair_kernel<1>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), g2::kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  cfg.gridDim = dim3(2 * clusters);
+  cfg.gridDim = dim3(2 * launch_clusters);
   cfg.blockDim = dim3(g2::kThreads);
   cfg.dynamicSmemBytes = g2::kSmemBytes;
   cfg.stream = stream;
@@ -382,7 +519,7 @@ cudaError_t launch_gemm_pair(const Params &p, int num_sms, int grid_override, bo
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmSFA, tmSFB, p, (int)pdl);
+  return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmSFA, tmSFB, p, sc, (int)pdl);
 }
 
 }  // namespace pa

@@ -48,6 +48,7 @@ cudaError_t launch_gemv(const Params &p, bool fused, bool pdl, cudaStream_t stre
 // Tensor-core path: persistent tcgen05 GEMM with the fused head epilogue,
 // on single CTAs (128 x 128 tiles) or on CTA pairs (cta_group::2, 256 x 256).
 cudaError_t launch_gemm(const Params &p, int num_sms, int grid_override, bool pdl, cudaStream_t stream);
-cudaError_t launch_gemm_pair(const Params &p, int num_sms, int grid_override, bool pdl, cudaStream_t stream);
+cudaError_t launch_gemm_pair(const Params &p, int num_sms, int64_t l2_bytes, int grid_override, bool pdl,
+                             cudaStream_t stream);
 
 }  // namespace pa

@@ -32,6 +32,8 @@ __global__ void __launch_bounds__(NTHR) pa_prologue_kernel(Params p, int use_pdl
   }
   const int m = blockIdx.x;
   const int ksf = p.H >> 5;
+  if (m == 0 && p.sk_counter)  // the pair GEMM's split counters start each step at zero
+    for (int i = threadIdx.x; i < kSplitCounterWords; i += NTHR) p.sk_counter[i] = 0;
   if (m >= p.M) {  // MXFP8 padding rows of the tensor-core path: scale 1, codes unused
     if (WFMT == 1)
       for (int kb = threadIdx.x; kb < ksf; kb += NTHR) p.xsf[sf128x4_offset(m, kb, ksf)] = 127;
