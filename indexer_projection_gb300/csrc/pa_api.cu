@@ -41,7 +41,7 @@ bool uses_gemv(const pa_config &c, int M) {
 // state between calls (PA_DEV_* bits, sticky until read); the rest is
 // scratch: the prologue's quantised activations and their scales.
 struct WsLayout {
-  size_t status, x_scale, xsf, xq, sk_counter, sk_partial, total;
+  size_t status, x_scale, xsf, xq, total;
   int m_pad;
 };
 
@@ -58,13 +58,6 @@ WsLayout ws_layout(const pa_handle *h, int M) {
     off = align_up(off + (size_t)(L.m_pad > 0 ? L.m_pad : 128) * (H / 32), 256);
   L.xq = off;
   off = align_up(off + (size_t)M * H, 256);
-  L.sk_counter = L.sk_partial = 0;
-  if (!uses_gemv(h->cfg, M)) {  // the tensor-core path: the pair GEMM's split region
-    L.sk_counter = off;
-    off = align_up(off + sizeof(uint32_t) * pa::kSplitCounterWords, 256);
-    L.sk_partial = off;
-    off = align_up(off + pa::kSplitPartialBytes, 256);
-  }
   L.total = off;
   return L;
 }
@@ -89,17 +82,22 @@ cudaError_t query_sms(pa_handle *h) {
 
 
 // Main kernel for M rows (h->num_sms known; the skinny path's fusion check
-// queries the device once).  The tensor-core path runs on CTA pairs: their
-// 256 x 256 tiles read half the shared-memory bytes a FLOP of 128 x 128 tiles
-// on single SMs, and the pair kernel splits the tiles of a last, partial wave
-// along K across every cluster, so its waves are never quantised; single-SM
-// tiles only on request.
+// queries the device once).  256 x 256 pair tiles cost about 1.5x a
+// 128 x 128 tile on one SM: the pairs are used unless wave quantisation
+// favours the finer tiles.
 int choose_path(const pa_handle *h, int M) {
   const pa_config &c = h->cfg;
   if (uses_gemv(c, M))
     return (c.flags & PA_FLAG_FUSE) && pa::gemv_fuses_prologue(c.hidden, c.weight_format) ? PA_PATH_GEMV_FUSED
                                                                                          : PA_PATH_GEMV;
-  return (c.flags & PA_FLAG_GEMM_SINGLE) ? PA_PATH_GEMM_SINGLE : PA_PATH_GEMM_PAIR;
+  if (c.flags & PA_FLAG_GEMM_SINGLE) return PA_PATH_GEMM_SINGLE;
+  if (c.flags & PA_FLAG_GEMM_PAIR) return PA_PATH_GEMM_PAIR;
+  const int sms = h->num_sms > 1 ? h->num_sms : 2;
+  const int64_t t1 = (int64_t)((M + 127) / 128) * (h->N / 128);
+  const int64_t t2 = (int64_t)((M + 255) / 256) * ((h->N + 255) / 256);
+  const int64_t w1 = (t1 + sms - 1) / sms;
+  const int64_t w2 = (t2 + sms / 2 - 1) / (sms / 2);
+  return 3 * w2 <= 2 * w1 ? PA_PATH_GEMM_PAIR : PA_PATH_GEMM_SINGLE;
 }
 
 bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb) {
@@ -352,8 +350,6 @@ int pre_attn_run(pa_handle *h, int M, const pa_step_inputs *in, const pa_weights
   p.xsf = ws + L.xsf;
   p.xq = ws + L.xq;
   p.m_pad = L.m_pad;
-  p.sk_counter = L.sk_counter ? reinterpret_cast<uint32_t *>(ws + L.sk_counter) : nullptr;
-  p.sk_partial = L.sk_partial ? reinterpret_cast<float *>(ws + L.sk_partial) : nullptr;
 
   const bool pdl = !(c.flags & PA_FLAG_NO_PDL);
   cudaStream_t s = (cudaStream_t)stream;

@@ -22,12 +22,6 @@ constexpr float kFp8Max = 448.0f;
 constexpr uint32_t kDevSlotRange = 1u << 0;
 constexpr uint32_t kDevPosRange = 1u << 1;
 constexpr uint32_t kDevWaitTimeout = 1u << 2;
-// The pair GEMM's split region: at most this many 2-CTA clusters, each with
-// one partial-sum slot of 2 x 128 rows x 256 columns f32 in the workspace,
-// and two counters a split tile.
-constexpr int kMaxSplitClusters = 128;
-constexpr size_t kSplitPartialBytes = (size_t)kMaxSplitClusters * 2 * 128 * 256 * 4;
-constexpr int kSplitCounterWords = kMaxSplitClusters * 2;
 
 // Everything a kernel of the step reads or writes.  Passed by value.
 struct Params {
@@ -69,8 +63,6 @@ struct Params {
   float *x_scale;            // [M] per-token scales (per-channel format)
   uint8_t *xsf;              // MXFP8 activation scales, F8_128x4 of [Mpad, H/32]
   int m_pad;                 // M rounded up to 128 (MXFP8 scale rows)
-  float *sk_partial;         // pair GEMM split region: partial sums (NULL: no split region)
-  uint32_t *sk_counter;      // and its counters, zeroed by the prologue of every step
 };
 
 // ------------------------------------------------------------ small utils

@@ -225,6 +225,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int it = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
       const int mt = t / n_tiles, nt = t - mt * n_tiles;
+      // the row's position, slots and scale, and its cos / sin line, fetched
+      // while the tile's MMAs run (they do not depend on them)
+      const int m = mt * kBM + row;
+      const bool live = m < M;
+      int64_t pos = 0, slot = -1, islot = -1;
+      float xs = 1.0f;
+      if (live) {
+        pos = load_pos(p, m);
+        slot = ld_i64(p.slot + m);
+        islot = ld_i64(p.islot + m);
+        if (WFMT == 0) xs = __ldcg(p.x_scale + m);
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(p.cos_sin + pos * kRotDim));
+      }
       // one thread waits; the verdict and the head's per-channel weight
       // scales are shared through double-buffered shared memory
       if (row == 0)
@@ -253,10 +266,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         abuf = 0;
         aphase ^= 1;
       }
-      const int m = mt * kBM + row;
-      if (m >= M) continue;
+      if (!live) continue;
       if (WFMT == 0) {
-        const float xs = __ldcg(p.x_scale + m);
         const float *wsb = ws_s + (it & 1) * kBN;
 #pragma unroll
         for (int i = 0; i < kBN; ++i) v[i] = v[i] * xs * wsb[i];
@@ -264,9 +275,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       HeadCtx hc;
       hc.m = m;
       hc.head = nt;
-      hc.cs_row = p.cos_sin + load_pos(p, m) * kRotDim;
-      hc.slot = ld_i64(p.slot + m);
-      hc.islot = ld_i64(p.islot + m);
+      hc.cs_row = p.cos_sin + pos * kRotDim;
+      hc.slot = slot;
+      hc.islot = islot;
       hc.g_q = p.g_q;
       hc.g_k = p.g_k;
       hc.g_iq = p.g_iq;

@@ -42,7 +42,6 @@ constexpr int kThreads = 320;
 constexpr int kEpiThreads = 256;
 constexpr int kTmemCols = 512;
 constexpr int kSfaCol = 256, kSfbCol = 260;
-constexpr int kMinSplitSteps = 8;  // K steps a cluster takes of the split region, at least
 
 struct Smem {  // offsets from the 1024-aligned base
   static constexpr int a = 0;
@@ -51,7 +50,7 @@ struct Smem {  // offsets from the 1024-aligned base
   static constexpr int sfb = sfa + kStages * 1024;          // 1024-aligned slots
   static constexpr int bars = sfb + kStages * 1024;          // full[S], empty[S], tfull, tempty, never, drain
   static constexpr int tmem_addr = bars + (2 * kStages + 4) * 8;
-  static constexpr int ok = tmem_addr + 8;                   // 4 x int: tile verdicts, owner-wait verdicts
+  static constexpr int ok = tmem_addr + 8;                   // 2 x int: tile verdicts (+ 8 bytes: wscale 16-aligned)
   static constexpr int wscale = ok + 16;                     // [2 parity][2 heads][128] f32
   static constexpr int total = wscale + 2 * 2 * 128 * 4;
 };
@@ -99,31 +98,15 @@ __device__ __forceinline__ void tc_commit_pair(uint64_t *bar) {
       : "memory");
 }
 
-// The schedule (chosen on the host, the same for every CTA).
-//   Raster: tiles are numbered in groups of group_m m-pairs; inside a group
-//   the m-pair runs fastest, then the n tile ("vllm.models.minimax_m3.nvidia.
-//   ops.qkv_index_fused_epilogue", QkvIndexFusedEpilogueKernel.tile_coords /
-//   _group_m), so the clusters of one wave share a few weight tiles and a
-//   group's activations stay in L2 while it walks every weight tile: the
-//   weights are read from HBM once per group, not once per wave.
-//   Whole waves: tile w * C + c for cluster c, w < dp_waves.
-//   The remaining tiles (fewer than a wave) are split along K: their
-//   sk_units = tiles x K steps are cut into sk_clusters equal contiguous
-//   ranges, one per cluster, so no cluster idles while another finishes a
-//   last tile alone.  A range starts and ends anywhere inside a tile: the
-//   cluster whose range holds a tile's last K step owns the tile; the
-//   clusters before it that hold its earlier K steps write their partial
-//   sums to the workspace and count them in the tile's counter; the owner
-//   waits (bounded) for the count, adds the partials and runs the epilogue.
-//   A cluster walks its range from its last segment (where it contributes to
-//   the next cluster's tile) to its first (the tile it owns), so every
-//   partial is produced early and owners seldom wait.
+// Tile raster (chosen on the host, the same for every CTA): tiles are
+// numbered in groups of group_m m-pairs, the m-pair running fastest inside a
+// group, then the n tile ("vllm.models.minimax_m3.nvidia.ops.
+// qkv_index_fused_epilogue", QkvIndexFusedEpilogueKernel.tile_coords /
+// _group_m).  The clusters of one wave then share a few weight tiles, and a
+// group's activations stay in L2 while it walks every weight tile: the
+// weights are read from HBM about once per group rather than once per wave.
 struct Sched {
   int m_pairs, n_tiles, ksteps, group_m;
-  int dp_waves;     // whole waves of whole tiles
-  int sk_tile0;     // first tile of the split region: dp_waves * clusters
-  int sk_units;     // K steps of the split region
-  int sk_clusters;  // clusters sharing it (0: none)
 };
 
 __device__ __forceinline__ void tile_coords(const Sched &s, int tile, int &mp, int &nt) {
@@ -133,81 +116,31 @@ __device__ __forceinline__ void tile_coords(const Sched &s, int tile, int &mp, i
   nt = idx / gm;
   mp = g * s.group_m + (idx - nt * gm);
 }
-__device__ __forceinline__ int sk_begin(const Sched &s, int c) {
-  return (int)((int64_t)c * s.sk_units / s.sk_clusters);
-}
-// The cluster whose split range holds unit u.
-__device__ __forceinline__ int sk_cluster_of(const Sched &s, int u) {
-  int c = (int)((int64_t)u * s.sk_clusters / s.sk_units);
-  while (c + 1 < s.sk_clusters && sk_begin(s, c + 1) <= u) ++c;
-  while (c > 0 && sk_begin(s, c) > u) --c;
-  return c;
-}
-
-// Wait until *count reaches `need` (acquire at GPU scope), giving up after
-// limit_ns (PA_DEV_WAIT_TIMEOUT).
-__device__ __forceinline__ int wait_count(const uint32_t *count, uint32_t need, uint32_t *status, uint64_t limit_ns) {
-  auto ld = [&]() {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(count) : "memory");
-    return v;
-  };
-  if (ld() >= need) return 1;
-  const uint64_t t0 = globaltimer();
-  while (ld() < need) {
-    if (globaltimer() - t0 > limit_ns) {
-      set_status(status, kDevWaitTimeout);
-      return 0;
-    }
-    __nanosleep(32);
-  }
-  return 1;
-}
-
-// A cluster's work items, in order: its whole tiles, then its split segments
-// last to first.  The three roles (TMA producer, MMA issuer, epilogue) walk
-// the same sequence.
-struct Work {
-  int tile, ks0, ks1;  // the current item: K steps [ks0, ks1) of tile
-  bool split;          // from the split region
-  int w, hi, u0;       // whole-tile wave; split range [u0, hi) still to walk
-  int ndp, ksteps, sk_tile0, cluster, clusters;  // ndp: this cluster's whole tiles (below sk_tile0)
-  __device__ Work(const Sched &s, int c, int C) : ksteps(s.ksteps), sk_tile0(s.sk_tile0), cluster(c), clusters(C) {
-    ndp = c < s.sk_tile0 ? (s.sk_tile0 - c + C - 1) / C : 0;
-    if (ndp > s.dp_waves) ndp = s.dp_waves;
-    w = 0;
-    split = false;
-    if (s.sk_clusters > 0 && c < s.sk_clusters) {
-      u0 = sk_begin(s, c);
-      hi = sk_begin(s, c + 1);
-    } else {
-      u0 = hi = 0;
-    }
+// The cluster's tiles, in order: tile c, c + C, ..., K steps [0, ksteps)
+// each, as a running count of K steps.  The three roles (TMA producer, MMA
+// issuer, epilogue) walk the same sequence.  (Written this way, rather than
+// as a plain loop over tiles, the kernel compiled to fewer epilogue spills
+// and ran ~5% faster on prefill.)
+struct Segs {
+  int tile, ks0, ks1;
+  int u, u1, ksteps, step;
+  __device__ Segs(const Sched &s, int c, int C) : ksteps(s.ksteps) {
+    u = c * ksteps;
+    u1 = s.m_pairs * s.n_tiles * ksteps;
+    step = C * ksteps;
     set();
   }
-  __device__ bool valid() const { return w < ndp || hi > u0; }
+  __device__ bool valid() const { return u < u1; }
   __device__ void set() {
-    if (w < ndp) {
-      tile = w * clusters + cluster;
-      ks0 = 0;
-      ks1 = ksteps;
-      split = false;
-    } else if (hi > u0) {
-      const int t = (hi - 1) / ksteps;  // split-region tile of the segment ending at hi
-      const int lo = t * ksteps > u0 ? t * ksteps : u0;
-      tile = sk_tile0 + t;
-      ks0 = lo - t * ksteps;
-      ks1 = hi - t * ksteps;
-      split = true;
-    }
+    tile = u / ksteps;
+    ks0 = u - tile * ksteps;
+    ks1 = ksteps;
   }
   __device__ void next() {
-    if (w < ndp) ++w;
-    else hi = (tile - sk_tile0) * ksteps + ks0;  // the walked segment's start
+    u += step;
     set();
   }
 };
-
 template <int WFMT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     pa_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -273,7 +206,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int last_ph[kStages];  // phase each stage was last armed with (-1: never)
 #pragma unroll
       for (int i = 0; i < kStages; ++i) last_ph[i] = -1;
-      for (Work sg(sc, cluster, clusters); sg.valid() && ok; sg.next()) {
+      for (Segs sg(sc, cluster, clusters); sg.valid() && ok; sg.next()) {
         int mp, nt;
         tile_coords(sc, sg.tile, mp, nt);
         const int m_tile = 2 * mp + (int)rank;
@@ -318,7 +251,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true;
       const uint32_t a0 = smem_u32(smem + Smem::a), b0 = smem_u32(smem + Smem::b);
       const uint32_t sfa0 = smem_u32(smem + Smem::sfa), sfb0 = smem_u32(smem + Smem::sfb);
-      for (Work sg(sc, cluster, clusters); sg.valid() && ok; sg.next()) {
+      for (Segs sg(sc, cluster, clusters); sg.valid() && ok; sg.next()) {
         if (!mbar_wait(tempty, aphase ^ 1, p.status, wait_limit(p))) {
           ok = false;
           break;
@@ -367,10 +300,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int erow = wg * 128 + row;       // 0..255 across both warpgroups
     uint32_t aphase = 0;
     int it = 0;
-    for (Work sg(sc, cluster, clusters); sg.valid(); sg.next(), ++it) {
+    for (Segs sg(sc, cluster, clusters); sg.valid(); sg.next(), ++it) {
       int mp, nt;
       tile_coords(sc, sg.tile, mp, nt);
       const int head = 2 * nt + wg;
+      // the row's position, slots and scale, and its cos / sin line, fetched
+      // while the tile's MMAs run (they do not depend on them)
+      const int m = (2 * mp + (int)rank) * kBM + row;
+      const bool live = m < M && head < p.n_heads;
+      int64_t pos = 0, slot = -1, islot = -1;
+      float xs = 1.0f;
+      if (live) {
+        pos = load_pos(p, m);
+        slot = ld_i64(p.slot + m);
+        islot = ld_i64(p.islot + m);
+        if (WFMT == 0) xs = __ldcg(p.x_scale + m);
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(p.cos_sin + pos * kRotDim));
+      }
       if (erow == 0)
         ok_s[it & 1] = mbar_wait(tfull, aphase, p.status, wait_limit(p)) &&
                                !(p.test_timeout && !mbar_wait(never, 0, p.status, wait_limit(p)))
@@ -400,37 +346,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       named_bar_sync(2 + wg, 128);
       if ((warp & 3) == 0 && lane == 0) arrive_remote(tempty0);
       aphase ^= 1;
-      if (sg.split) {
-        const int slot = sg.tile - sc.sk_tile0;  // the tile among the split ones
-        uint32_t *count = p.sk_counter + slot * 2 + rank;
-        // partial sums: per CTA 256 columns x 128 rows, column-major (a warp
-        // writes and reads 32 consecutive rows of a column)
-        const size_t part = (size_t)kBN * kBM;
-        if (sg.ks1 < sc.ksteps) {  // a contributor: hand the partial to the owner
-          float *dst = p.sk_partial + (size_t)(cluster * 2 + rank) * part + (size_t)(wg * 128) * kBM + row;
-#pragma unroll
-          for (int i = 0; i < 128; ++i) __stcg(dst + i * kBM, v[i]);
-          __threadfence();
-          named_bar_sync(1, kEpiThreads);
-          if (erow == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(count) : "memory");
-          continue;
-        }
-        if (sg.ks0 > 0) {  // the owner: add the partials of the clusters before it
-          const int c_first = sk_cluster_of(sc, slot * sc.ksteps);
-          if (erow == 0) ok_s[2 + (it & 1)] = wait_count(count, (uint32_t)(cluster - c_first), p.status, wait_limit(p));
-          named_bar_sync(1, kEpiThreads);
-          if (!ok_s[2 + (it & 1)]) continue;
-          for (int c2 = c_first; c2 < cluster; ++c2) {
-            const float *src = p.sk_partial + (size_t)(c2 * 2 + rank) * part + (size_t)(wg * 128) * kBM + row;
-#pragma unroll
-            for (int i = 0; i < 128; ++i) v[i] += __ldcg(src + i * kBM);
-          }
-        }
-      }
-      const int m = (2 * mp + (int)rank) * kBM + row;
-      if (m >= M || head >= p.n_heads) continue;
+      if (!live) continue;
       if (WFMT == 0) {
-        const float xs = __ldcg(p.x_scale + m);
         const float *wsb = ws_s + ((it & 1) * 2 + wg) * 128;
 #pragma unroll
         for (int i = 0; i < 128; ++i) v[i] = v[i] * xs * wsb[i];
@@ -438,9 +355,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       HeadCtx hc;
       hc.m = m;
       hc.head = head;
-      hc.cs_row = p.cos_sin + load_pos(p, m) * kRotDim;
-      hc.slot = ld_i64(p.slot + m);
-      hc.islot = ld_i64(p.islot + m);
+      hc.cs_row = p.cos_sin + pos * kRotDim;
+      hc.slot = slot;
+      hc.islot = islot;
       hc.g_q = p.g_q;
       hc.g_k = p.g_k;
       hc.g_iq = p.g_iq;
@@ -483,35 +400,18 @@ cudaError_t launch_gemm_pair(const Params &p, int num_sms, int64_t l2_bytes, int
   const int tiles = sc.m_pairs * sc.n_tiles;
   int clusters = (grid_override > 0 ? grid_override : num_sms) / 2;
   if (clusters < 1) clusters = 1;
-  if (clusters > kMaxSplitClusters) clusters = kMaxSplitClusters;
+  if (clusters > tiles) clusters = tiles;
   // raster groups: a group's activation rows (256 a pair, K bytes each) take
   // at most a quarter of the L2
   const int64_t per_pair = (int64_t)256 * p.H;
-  int gm = (int)((l2_bytes / 4) / (per_pair > 0 ? per_pair : 1));
-  sc.group_m = gm < 1 ? 1 : (gm > sc.m_pairs ? sc.m_pairs : gm);
-  int launch_clusters = clusters;
-  sc.dp_waves = tiles / clusters;
-  sc.sk_tile0 = sc.dp_waves * clusters;
-  const int rem = tiles - sc.sk_tile0;
-  if (rem == 0 || !p.sk_partial || !p.sk_counter) {
-    // whole tiles only (no split region, or no workspace for one)
-    if (launch_clusters > tiles) launch_clusters = tiles;
-    sc.dp_waves = (tiles + launch_clusters - 1) / launch_clusters;
-    sc.sk_tile0 = tiles;
-    sc.sk_units = 0;
-    sc.sk_clusters = 0;
-  } else {
-    sc.sk_units = rem * sc.ksteps;
-    const int by_len = sc.sk_units / g2::kMinSplitSteps;
-    sc.sk_clusters = by_len < 1 ? 1 : (by_len > clusters ? clusters : by_len);
-    if (sc.dp_waves == 0) launch_clusters = sc.sk_clusters;
-  }
+  const int64_t gm = (l2_bytes / 4) / (per_pair > 0 ? per_pair : 1);
+  sc.group_m = gm < 1 ? 1 : (gm > sc.m_pairs ? sc.m_pairs : (int)gm);
   auto kern = p.weight_fmt == 0 ? g2::pa_gemm_pair_kernel<0> : g2::pa_gemm_pair_kernel<1>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), g2::kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  cfg.gridDim = dim3(2 * launch_clusters);
+  cfg.gridDim = dim3(2 * clusters);
   cfg.blockDim = dim3(g2::kThreads);
   cfg.dynamicSmemBytes = g2::kSmemBytes;
   cfg.stream = stream;

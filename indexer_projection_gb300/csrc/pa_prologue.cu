@@ -23,23 +23,24 @@ namespace pa {
 // rows (the skinny path, which waits on this kernel): 1024 threads a row, so
 // the per-element work of the correctly rounded norm is spread 4x wider and
 // the row is done sooner.
+// The tensor-core kernel that follows is launched when every CTA of this
+// grid has passed its trigger, and it takes a whole SM's registers and
+// shared memory for its CTA: the trigger comes after the row's work, so its
+// CTAs do not take SMs this grid's remaining rows still need (a trigger at
+// the start let them do that and stretched a 448-row prologue fourfold).
 template <int WFMT, int NTHR, int MAXC>
 __global__ void __launch_bounds__(NTHR) pa_prologue_kernel(Params p, int use_pdl) {
   __shared__ float2 red2[NTHR / 32];
-  if (use_pdl) {
-    pdl_trigger();
-    pdl_wait();
-  }
+  if (use_pdl) pdl_wait();
   const int m = blockIdx.x;
   const int ksf = p.H >> 5;
-  if (m == 0 && p.sk_counter)  // the pair GEMM's split counters start each step at zero
-    for (int i = threadIdx.x; i < kSplitCounterWords; i += NTHR) p.sk_counter[i] = 0;
   if (m >= p.M) {  // MXFP8 padding rows of the tensor-core path: scale 1, codes unused
     if (WFMT == 1)
       for (int kb = threadIdx.x; kb < ksf; kb += NTHR) p.xsf[sf128x4_offset(m, kb, ksf)] = 127;
-    return;
+  } else {
+    norm_quant_row<WFMT, NTHR, MAXC>(p, m, red2);
   }
-  norm_quant_row<WFMT, NTHR, MAXC>(p, m, red2);
+  if (use_pdl) pdl_trigger();
 }
 
 // One cluster of C CTAs per token row (blockIdx.x / C); CTA r takes the
