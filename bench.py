@@ -539,11 +539,20 @@ def secondary(args, name, dev, world, peaks, peak_src):
     m = measure(args, wl, dev, world, K2, max(3, args.warmup), min_seconds=1.0)
     kname, desc, _ = path_info(B, m["path"])
     ms = m["ms"]
-    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    # a region of over half a second runs at the power-capped sustained
+    # clock: its steps are compared with the sustained peak (the burst one
+    # is reported beside it)
+    region_s = ms * 1e-3 * K2 * m["reps"]
+    burst = peaks["bf16_tflops"] * FP8_OVER_BF16
+    sustained = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * FP8_OVER_BF16
+    fp8_peak = sustained if region_s >= 0.5 else burst
     out = {"config": workload_config(name, wl, world), "path": desc, "steps": K2 * m["reps"],
-           "timed_as": f"{m['reps']} replays of a CUDA graph of {K2} steps",
+           "timed_as": f"{m['reps']} replays of a CUDA graph of {K2} steps ({region_s:.2f} s)",
            "us_per_layer": round(ms * 1e3, 3), "tokens_per_s": round(tokens_per_second(world, wl.M, ms), 1),
            "step_fp8_frac": round(step_flops(wl) / (ms * 1e-3) / 1e12 / fp8_peak, 4),
+           "step_fp8_peak": {"value": round(fp8_peak, 1),
+                             "source": ("sustained" if region_s >= 0.5 else "burst") + " bf16 of measured x 2"},
+           "step_fp8_frac_of_burst": round(step_flops(wl) / (ms * 1e-3) / 1e12 / burst, 4),
            "step_hbm_frac": round(step_bytes(wl)["step"] / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
            "roofline": roofline(B, wl, kname, m, peaks, peak_src, name), "clocks": m["clocks"]}
     del m
