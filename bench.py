@@ -3,7 +3,7 @@
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
                   [--workload decode|spec_decode|prefill|tiny|sweep_m<M>]
-                  [--also prefill|none]
+                  [--also prefill,spec_decode,index_spec_decode|none]
 
 A step is one pre_attn_run() (prologue + skinny GEMV or tcgen05 GEMM with the
 fused head epilogue) over one batch of the workload's synthetic inputs.  The
@@ -11,8 +11,10 @@ timed region is a CUDA graph of exactly K steps; step i uses the i-th of C
 rotating copies of the layer weights and inputs (C chosen so the copies
 exceed twice the L2), so weights stream from HBM as they would across layers.
 Rank 0 prints one JSON line: the headline workload (decode by default) and,
-under "prefill", the prefill configuration timed in the same run (its own
-graph of steps, at least a second of them, with its own clock record).
+under their names, the workloads of --also timed in the same run (prefill
+and speculative decode: their own graphs of steps, at least a second of
+them, each with its own clock record; the indexer scores of the
+speculative-decode shape: a graph of pre_attn_index_scores launches).
 Under torchrun each rank runs an independent replica (the step has no
 cross-GPU exchange) and the slowest rank's time sets the aggregate tokens/s.
 
@@ -95,7 +97,8 @@ def step_flops(wl) -> int:
 KERNEL_SOURCES = {"skinny": ("pa_gemv.cu", "pa_device.cuh", "pa_tc.cuh", "pa_norm.cuh"),
                   "gemm": ("pa_gemm.cu", "pa_device.cuh", "pa_tc.cuh"),
                   "gemm_pair": ("pa_gemm2.cu", "pa_device.cuh", "pa_tc.cuh"),
-                  "prologue": ("pa_prologue.cu", "pa_device.cuh", "pa_norm.cuh")}
+                  "prologue": ("pa_prologue.cu", "pa_device.cuh", "pa_norm.cuh"),
+                  "index_scores": ("pa_index.cu", "pa_device.cuh", "pa_tma.h")}
 
 
 def kernel_sha(kernel: str) -> str:
@@ -518,8 +521,11 @@ def roofline(B, wl, name, m, peaks, peak_src, workload_name):
                 "peak_source": f"{peak_src} bf16 x nominal FP8/BF16 ratio 2 (of measured)"}
     achieved = nb["step"] / (ms_step * 1e-3) / 1e9
     peak = peaks["hbm_gbs"]
+    # the step's DRAM bytes: the GEMV's and its row prologue's captures
+    t_main, t_pro = ncu_traffic(name, workload_name), ncu_traffic("prologue", workload_name + "_rows")
+    traffic = t_main + t_pro if t_main is not None and t_pro is not None else None
     return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": ncu_traffic(name, workload_name),
+            "frac": round(achieved / peak, 4), "traffic": traffic,
             "kernel": f"whole step ({desc}): {nb['step']} algorithmic bytes over {ms_step * 1e3:.3f} us",
             "main_kernel_alone": {"us": round(main_ms * 1e3, 3), "frac": round(nb["main"] / (main_ms * 1e-3) / 1e9 / peak, 4),
                                   "note": "the GEMV timed with events around it, which stops its overlap with the "
@@ -642,7 +648,7 @@ def index_secondary(args, name, dev, world, peaks):
             "kernel": "pa_index_scores_kernel (TMA key blocks, ldmatrix + mma.sync bf16)",
             "us_per_launch": round(ms * 1e3, 3), "launches": reps * K,
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                         "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": ncu_traffic("index_scores", name),
                          "algorithmic_bytes": nbytes},
             "status": int(status.item()), "clocks": clocks}
 
