@@ -6,8 +6,9 @@ and its binding) never touches it, and it never touches the product path.
 
 The oracle restates the MiniMax-M3 sparse-layer pre-attention step from the
 pages "vllm.models.minimax_m3.amd.mono.kernels.pre_attn" (K1 mono_pre) and
-"vllm.models.minimax_m3.nvidia.ops.qkv_index_fused_epilogue"; each C function
-cites the symbol it follows.
+"vllm.models.minimax_m3.nvidia.ops.qkv_index_fused_epilogue", and the DSpark
+drafter's attention from "vllm.models.minimax_m3.amd.mono.drafter.attention";
+each C function cites the symbol it follows.
 """
 
 from __future__ import annotations
@@ -78,6 +79,12 @@ class Outputs(ctypes.Structure):
                 ("iq_fp8", ctypes.c_void_p), ("q_fp8_scale", ctypes.c_float)]
 
 
+class DattnConfig(ctypes.Structure):
+    _fields_ = [("R", ctypes.c_int), ("q_len", ctypes.c_int), ("bt_width", ctypes.c_int),
+                ("window", ctypes.c_int), ("max_blocks", ctypes.c_int), ("part_blocks", ctypes.c_int),
+                ("sm_scale", ctypes.c_double)]
+
+
 class HeadParams(ctypes.Structure):
     _fields_ = [("g_q", ctypes.c_void_p), ("g_k", ctypes.c_void_p), ("g_iq", ctypes.c_void_p),
                 ("g_ik", ctypes.c_void_p), ("cos_sin", ctypes.c_void_p),
@@ -122,6 +129,9 @@ def lib():
                 "ora_index_scale_log2e": (ctypes.c_double, [ctypes.c_double]),
                 "ora_index_scores": (ctypes.c_int, [vp, i64, vp, i64, vp, ctypes.c_int, vp, ctypes.c_int,
                                                     ctypes.c_int, ctypes.c_int, ctypes.c_int, f, vp, i64]),
+                "ora_drafter_qkv": (ctypes.c_int, [vp, i64, i64, vp, vp, f, vp, i64, vp, vp, vp, i64, vp]),
+                "ora_drafter_window": (None, [i64, i64, ctypes.c_int, ctypes.c_int, vp, vp]),
+                "ora_drafter_attention": (ctypes.c_int, [vp, vp, vp, i64, vp, vp, vp, vp, vp, vp]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -276,6 +286,75 @@ def index_scores(iq, index_cache, block_table, seq_lens, q_len: int, init_blocks
     if bad:
         raise OracleError(f"oracle index scores returned {bad[0]}")
     return out
+
+
+def drafter_qkv(qkv, qn, kn, eps: float, cos_sin, positions, slot_mapping, cache):
+    """The drafter's q / k head norms, RoPE and FP8 (see ora_drafter_qkv).
+
+    qkv: [M, >=18*128] bf16 bits; qn, kn: [128] bf16 bits; cos_sin:
+    [max_pos, 64] bf16 bits; positions, slot_mapping: [M] int64; cache:
+    [blocks, 128, 256] uint8, updated in place.  Returns q8 [M * 16, 128]
+    E4M3 codes."""
+    qkv = np.ascontiguousarray(qkv, np.uint16)
+    M = qkv.shape[0]
+    q8 = np.zeros((M * 16, HEAD_DIM), np.uint8)
+    assert cache.flags.c_contiguous and cache.dtype == np.uint8
+    rc = lib().ora_drafter_qkv(_p(qkv), qkv.shape[1], M, _p(np.ascontiguousarray(qn, np.uint16)),
+                               _p(np.ascontiguousarray(kn, np.uint16)), float(eps),
+                               _p(np.ascontiguousarray(cos_sin, np.uint16)), cos_sin.shape[0],
+                               _p(np.ascontiguousarray(positions, np.int64)),
+                               _p(np.ascontiguousarray(slot_mapping, np.int64)), _p(cache),
+                               cache.size // (128 * 256), _p(q8))
+    if rc != 0:
+        raise OracleError(f"oracle drafter qkv returned {rc}")
+    return q8
+
+
+def drafter_window(p0: int, seq_len: int, window: int, max_blocks: int):
+    lo, hi = ctypes.c_int64(), ctypes.c_int64()
+    lib().ora_drafter_window(p0, seq_len, window, max_blocks, ctypes.byref(lo), ctypes.byref(hi))
+    return lo.value, hi.value
+
+
+def drafter_attention(q8, cache, block_table, seq_lens, positions, q_len: int, window: int, max_blocks: int,
+                      part_blocks: int, sm_scale: float, rows=None, threads: int | None = None):
+    """The drafter's split-KV attention and MXFP8 merge (see
+    ora_drafter_attention).  q8: [M * 16, 128] E4M3; cache: [blocks, 128, 256]
+    uint8; block_table [R, bt_width] int32; seq_lens [R] int32; positions [M]
+    int64.  Returns (out_bf16 [M, 2048] uint16 bits, codes [M, 2048] uint8,
+    scales [M, 64] uint8); rows of requests outside `rows` (when given) are
+    left zero.  Requests run concurrently on `threads` host threads."""
+    q8 = np.ascontiguousarray(q8, np.uint8)
+    cache = np.ascontiguousarray(cache, np.uint8)
+    bt = np.ascontiguousarray(block_table, np.int32)
+    sl = np.ascontiguousarray(seq_lens, np.int32)
+    pos = np.ascontiguousarray(positions, np.int64)
+    R, bt_width = bt.shape
+    M = R * q_len
+    assert q8.shape[0] >= M * 16 and pos.shape[0] >= M
+    out = np.zeros((M, 2048), np.uint16)
+    codes = np.zeros((M, 2048), np.uint8)
+    scales = np.zeros((M, 64), np.uint8)
+    reqs = sorted(set(range(R)) if rows is None else {int(m) // q_len for m in rows})
+    L = lib()
+    nblocks = cache.size // (128 * 256)
+
+    def work(r):
+        cfg = DattnConfig(1, q_len, bt_width, window, max_blocks, part_blocks, float(sm_scale))
+        a = r * q_len
+        return L.ora_drafter_attention(ctypes.byref(cfg), _p(q8[a * 16:]), _p(cache), nblocks, _p(bt[r:]),
+                                       _p(sl[r:]), _p(pos[a:]), _p(out[a:]), _p(codes[a:]), _p(scales[a:]))
+
+    nthreads = threads or min(max(1, len(reqs)), os.cpu_count() or 1)
+    if nthreads <= 1:
+        rcs = [work(r) for r in reqs]
+    else:
+        with ThreadPoolExecutor(nthreads) as ex:
+            rcs = list(ex.map(work, reqs))
+    bad = [rc for rc in rcs if rc != 0]
+    if bad:
+        raise OracleError(f"oracle drafter attention returned {bad[0]}")
+    return out, codes, scales
 
 
 def run_rows(wl, state, rows, want_y: bool = False, threads: int | None = None):

@@ -17,6 +17,9 @@
  *         roles), prepare_SF (F8_128x4 scale layout), _nvfp4_cache_views,
  *         _nvfp4_quant32, _rms_norm, _rope64,
  *         minimax_m3_qkv_index_fused_epilogue (argument contract).
+ *   [DA]  "vllm.models.minimax_m3.amd.mono.drafter.attention" (the DSpark
+ *         drafter's attention): module summary, qkv_rows, window, kv_load,
+ *         block_math, block_acc, store_partial, merge_task.
  *
  * Precision: where the pages fix f32 (the residual sum, the per-token and
  * per-group quantiser arithmetic) the oracle does the same f32 operation;
@@ -618,4 +621,200 @@ int ora_index_scores(const uint16_t *iq, int64_t iq_stride, const uint8_t *index
     }
   }
   return ORA_OK;
+}
+
+
+/* --------------------------------------------- the drafter's attention */
+
+/* [DA] "vllm.models.minimax_m3.amd.mono.drafter.attention": the DSpark
+ * drafter's attention over its own FP8 KV cache, one KV head of 128 dims, 16
+ * query heads, up to 8 rows a request (7 on the page).  The drafter cache
+ * holds page-128 blocks of 128 keys, 256 bytes a key: the key's 128 E4M3 K
+ * bytes, then its 128 E4M3 V bytes (kv_load); q, K and V are unit-scale FP8
+ * (module summary: "FP8 q"). */
+#define DA_HEADS 16
+#define DA_BLOCK 128
+#define DA_KEY_BYTES 256
+
+/* The drafter's q / k head norms, RoPE and FP8 (qkv_rows: "head norm, RoPE,
+ * FP8"; its new K / V rows go to the cache).  Row m of qkv (qkv_stride bf16
+ * values) holds 16 q heads, then k, then v, 128 each.  q and k take the
+ * step's head norm (ora_head_rmsnorm with gamma qn / kn) and its partial NeoX
+ * RoPE at positions[m] (a reading: the page names the steps, not their
+ * form); v is taken as is.  q8 row (m * 16 + h) gets E4M3(f32(z)) of head h;
+ * the key at slot slot_mapping[m] (slot < 0: none) gets E4M3(f32(k)) and
+ * E4M3(v) at cache byte slot * 256 and slot * 256 + 128.  Returns
+ * ORA_ERR_POS for a position outside [0, max_pos), ORA_ERR_SLOT for a slot
+ * past the cache, before anything of that row is written. */
+int ora_drafter_qkv(const uint16_t *qkv, int64_t qkv_stride, int64_t M, const uint16_t *qn,
+                    const uint16_t *kn, float eps, const uint16_t *cos_sin, int64_t max_pos,
+                    const int64_t *positions, const int64_t *slot_mapping, uint8_t *cache,
+                    int64_t num_blocks, uint8_t *q8) {
+  float y[HEAD_DIM];
+  double z[HEAD_DIM];
+  for (int64_t m = 0; m < M; ++m) {
+    const int64_t pos = positions[m], slot = slot_mapping[m];
+    if (pos < 0 || pos >= max_pos) return ORA_ERR_POS;
+    if (slot >= num_blocks * DA_BLOCK) return ORA_ERR_SLOT;
+    const uint16_t *cs = cos_sin + pos * ROT_DIM;
+    for (int h = 0; h < DA_HEADS + 2; ++h) {
+      const uint16_t *src = qkv + m * qkv_stride + (int64_t)h * HEAD_DIM;
+      for (int d = 0; d < HEAD_DIM; ++d) y[d] = ora_bf16_decode(src[d]);
+      if (h <= DA_HEADS) {
+        ora_head_rmsnorm(y, h < DA_HEADS ? qn : kn, eps, z);
+        ora_rope_neox(z, cs);
+        for (int d = 0; d < HEAD_DIM; ++d) y[d] = (float)z[d];
+      }
+      uint8_t *dst = h < DA_HEADS ? q8 + (m * DA_HEADS + h) * HEAD_DIM
+                   : slot < 0     ? NULL
+                   : cache + slot * DA_KEY_BYTES + (h - DA_HEADS) * HEAD_DIM;
+      if (!dst) continue;
+      for (int d = 0; d < HEAD_DIM; ++d) dst[d] = ora_e4m3_encode(y[d]);
+    }
+  }
+  return ORA_OK;
+}
+
+/* Request r's key window ([DA] window): rows r * q_len .. + q_len - 1 sit at
+ * p0 + j with p0 = positions[r * q_len]; the keys lo .. hi with
+ * lo = max(p0 - (window - 1), 0) and hi = min(seq_len - 1,
+ * (lo / 128 + max_blocks) * 128 - 1), blocks lo / 128 .. hi / 128.  Key kp
+ * counts for row j when lo <= kp <= hi and kp > p0 + j - window
+ * (block_math's mask): the rows see each other's keys, non-causally. */
+void ora_drafter_window(int64_t p0, int64_t seq, int window, int max_blocks, int64_t *lo,
+                        int64_t *hi) {
+  int64_t a = p0 - (window - 1);
+  if (a < 0) a = 0;
+  int64_t b = (a / DA_BLOCK + max_blocks) * DA_BLOCK - 1;
+  if (seq - 1 < b) b = seq - 1;
+  *lo = a;
+  *hi = b;
+}
+
+/* The split-KV attention and its merge ([DA] module summary, block_acc,
+ * block_math, store_partial, merge_task), for R requests of q_len rows.
+ *   Partitions: the window's blocks, from lo / 128 on, in runs of
+ *     part_blocks blocks (the page fixes the partition's math, not its
+ *     length: a reading; the GPU path takes the same argument).  Each is an
+ *     online softmax over its blocks in order: with C = sm_scale * log2(e)
+ *     and m = -inf, l = 0, o = 0 to start, a block's valid scores s = q . k
+ *     (raw units) give m' = max(m, max s), ms = (m' == -inf ? 0 : m'),
+ *     alpha = exp2((m - ms) C), p = f32(exp2(s C - (ms C - 8))) (P x 256 at
+ *     m'), l = l alpha + sum p, o = o alpha + sum E4M3(p) v.  l sums the
+ *     unquantised p, o the E4M3 ones (block_acc).
+ *   Merge, in partition order (merge_task): m* = max m_i, w_i =
+ *     exp2((m_i - m*) C) (0 for a partition that saw no valid key), out =
+ *     (sum w_i o_i) / (sum w_i l_i); a row with no valid key at all gives 0.
+ *     out is rounded to bf16, then quantised to MXFP8 over the row's 16 * 128
+ *     values: 32-value blocks, ora_mx_exponent's E8M0 exponent e, codes
+ *     E4M3(x * 2^-e), scale byte e + 127.
+ * Sums and products are exact or in double.  q8 row (m * 16 + h) holds head
+ * h of row m; out_bf16 (optional) [R * q_len, 2048]; out_codes likewise
+ * (bytes); out_scales [R * q_len, 64].  A request whose window is empty
+ * (hi < lo) gets zero rows.  Returns ORA_ERR_ARG when a window block lies
+ * past the block table, ORA_ERR_SLOT for a block id outside the cache. */
+typedef struct {
+  int R, q_len, bt_width;
+  int window, max_blocks, part_blocks;
+  double sm_scale;
+} ora_dattn_cfg;
+
+int ora_drafter_attention(const ora_dattn_cfg *c, const uint8_t *q8, const uint8_t *cache,
+                          int64_t num_blocks, const int32_t *block_table, const int32_t *seq_lens,
+                          const int64_t *positions, uint16_t *out_bf16, uint8_t *out_codes,
+                          uint8_t *out_scales) {
+  const double C = c->sm_scale / log(2.0);
+  const int D = HEAD_DIM, W = DA_HEADS * HEAD_DIM;
+  double lut[256];
+  for (int i = 0; i < 256; ++i) lut[i] = (double)ora_e4m3_decode((uint8_t)i);
+  const int maxp = (c->max_blocks + c->part_blocks - 1) / c->part_blocks + 1;
+  double *pm = (double *)malloc(sizeof(double) * maxp);
+  double *pl = (double *)malloc(sizeof(double) * maxp);
+  double *po = (double *)malloc(sizeof(double) * maxp * D);
+  float *row = (float *)malloc(sizeof(float) * W);
+  if (!pm || !pl || !po || !row) {
+    free(pm); free(pl); free(po); free(row);
+    return ORA_ERR_ARG;
+  }
+  int rc = ORA_OK;
+  for (int r = 0; r < c->R && rc == ORA_OK; ++r) {
+    const int64_t p0 = positions[(int64_t)r * c->q_len];
+    int64_t lo, hi;
+    ora_drafter_window(p0, seq_lens[r], c->window, c->max_blocks, &lo, &hi);
+    const int64_t b_lo = lo / DA_BLOCK, b_hi = hi < lo ? b_lo - 1 : hi / DA_BLOCK;
+    const int64_t nparts = (b_hi - b_lo + c->part_blocks) / c->part_blocks;
+    if (b_hi >= b_lo && b_hi >= c->bt_width) { rc = ORA_ERR_ARG; break; }
+    for (int64_t b = b_lo; b <= b_hi; ++b) {
+      const int64_t phys = block_table[(int64_t)r * c->bt_width + b];
+      if (phys < 0 || phys >= num_blocks) rc = ORA_ERR_SLOT;
+    }
+    if (rc) break;
+    for (int j = 0; j < c->q_len; ++j) {
+      const int64_t m_row = (int64_t)r * c->q_len + j;
+      const int64_t qp = p0 + j;
+      for (int h = 0; h < DA_HEADS; ++h) {
+        const uint8_t *qv = q8 + (m_row * DA_HEADS + h) * D;
+        double mst = -INFINITY;
+        for (int64_t i = 0; i < nparts; ++i) {
+          double m = -INFINITY, l = 0.0, *o = po + i * D;
+          for (int d = 0; d < D; ++d) o[d] = 0.0;
+          const int64_t b_end = b_lo + (i + 1) * c->part_blocks;
+          for (int64_t b = b_lo + i * c->part_blocks; b < b_end && b <= b_hi; ++b) {
+            const uint8_t *blk = cache + (int64_t)block_table[(int64_t)r * c->bt_width + b] *
+                                             DA_BLOCK * DA_KEY_BYTES;
+            double s[DA_BLOCK], mb = -INFINITY;
+            for (int k = 0; k < DA_BLOCK; ++k) {
+              const int64_t kp = b * DA_BLOCK + k;
+              s[k] = -INFINITY;
+              if (kp < lo || kp > hi || kp <= qp - c->window) continue;
+              double acc = 0.0;
+              for (int d = 0; d < D; ++d) acc += lut[qv[d]] * lut[blk[k * DA_KEY_BYTES + d]];
+              s[k] = acc;
+              if (acc > mb) mb = acc;
+            }
+            const double mn = m > mb ? m : mb;
+            const double ms = mn == -INFINITY ? 0.0 : mn;
+            const double alpha = exp2((m - ms) * C);
+            const double off = ms * C - 8.0;
+            double psum = 0.0;
+            for (int d = 0; d < D; ++d) o[d] *= alpha;
+            for (int k = 0; k < DA_BLOCK; ++k) {
+              if (s[k] == -INFINITY) continue;
+              const float p = (float)exp2(s[k] * C - off);
+              const double pq = lut[ora_e4m3_encode(p)];
+              const uint8_t *v = blk + k * DA_KEY_BYTES + D;
+              psum += (double)p;
+              for (int d = 0; d < D; ++d) o[d] += pq * lut[v[d]];
+            }
+            l = l * alpha + psum;
+            m = mn;
+          }
+          pm[i] = m;
+          pl[i] = l;
+          if (m > mst) mst = m;
+        }
+        double L = 0.0, acc[HEAD_DIM];
+        for (int d = 0; d < D; ++d) acc[d] = 0.0;
+        for (int64_t i = 0; i < nparts; ++i) {
+          if (pm[i] == -INFINITY) continue;
+          const double w = exp2((pm[i] - mst) * C);
+          L += w * pl[i];
+          for (int d = 0; d < D; ++d) acc[d] += w * po[i * D + d];
+        }
+        for (int d = 0; d < D; ++d) row[h * D + d] = L > 0.0 ? ora_bf16_round((float)(acc[d] / L)) : 0.0f;
+      }
+      for (int k = 0; k < W; ++k)
+        if (out_bf16) out_bf16[m_row * W + k] = ora_bf16_encode(row[k]);
+      for (int bk = 0; bk < W / 32; ++bk) {
+        float amax = 0.0f;
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(row[32 * bk + i]));
+        const int e = ora_mx_exponent(amax);
+        for (int i = 0; i < 32; ++i)
+          out_codes[m_row * W + 32 * bk + i] = ora_e4m3_encode((float)ldexp((double)row[32 * bk + i], -e));
+        out_scales[m_row * (W / 32) + bk] = (uint8_t)(e + 127);
+      }
+    }
+  }
+  free(pm); free(pl); free(po); free(row);
+  return rc;
 }

@@ -355,3 +355,100 @@ def index_host_state(iw: IndexWorkload) -> dict:
     keys = torch.randn(pool * 128, HEAD_DIM, generator=g)
     st["index_cache"] = _e4m3_bits(keys)
     return st
+
+
+@dataclass
+class DrafterWorkload:
+    """Inputs of the drafter's attention: the drafter's projection rows (16 q
+    heads, k, v; bf16), its q / k head-norm gammas, the RoPE table, R
+    requests of q_len consecutive rows whose last row is the request's last
+    key (positions seq_len - q_len .. seq_len - 1), page-128 block tables and
+    a drafter KV cache of 256-byte key records (K then V, E4M3).
+
+    Only the blocks from (seq_len - q_len - window) / 128 on are given
+    physical blocks (a superset of what the key window can touch); the rest
+    of a block-table row is -1.  Keys below seq_len - q_len hold E4M3 codes
+    of N(0, 1) values (a normed key has unit RMS; V likewise); every other
+    byte of the cache (the new rows' slots before the call, keys past
+    seq_len, unused blocks) holds `stale`: "nan" fills them with E4M3 NaN
+    codes (0x7f / 0xff), "random" with random bytes."""
+    name: str
+    R: int
+    q_len: int
+    seq_lo: int            # seq_lens ~ U[seq_lo, seq_hi)
+    seq_hi: int
+    seed: int
+    window: int = 4096
+    max_blocks: int = 34   # 4096 keys + 6 rows from any offset in a block
+    part_blocks: int = 0   # 0: the library's choice for the device
+    sm_scale: float = 128 ** -0.5
+    eps: float = 1e-6
+    stale: str = "nan"
+    spare_blocks: int = 8
+
+    @property
+    def M(self) -> int:
+        return self.R * self.q_len
+
+    @property
+    def bt_width(self) -> int:
+        return (self.seq_hi + 127) // 128
+
+
+def drafter_spec_decode() -> DrafterWorkload:
+    # the speculative-decode configuration's shape: 64 requests x 7 rows, seq_lens U[1024, 32768)
+    return DrafterWorkload("drafter_spec_decode", R=64, q_len=7, seq_lo=1024, seq_hi=32768, seed=2)
+
+
+DRAFTER_CONFIGS = {"drafter_spec_decode": drafter_spec_decode}
+
+
+def drafter_host_state(dw: DrafterWorkload) -> dict:
+    """qkv [M, 18 * 128] bf16 bits ~ N(0, 1); qn, kn [128] bf16 bits ~ N(0, 0.1);
+    cos_sin [seq_hi, 64] bf16 bits; positions, slot_mapping [M] int64;
+    seq_lens [R] int32; block_table [R, bt_width] int32; cache [blocks, 128,
+    256] uint8 (see DrafterWorkload)."""
+    g = torch.Generator().manual_seed(dw.seed)
+    seq = torch.randint(dw.seq_lo, dw.seq_hi, (dw.R,), generator=g, dtype=torch.int64)
+    seq = torch.maximum(seq, torch.full_like(seq, dw.q_len))
+    nb = (seq + 127) // 128
+    first = torch.clamp((seq - dw.q_len - dw.window) // 128, min=0)
+    counts = nb - first
+    pool = int(counts.sum()) + dw.spare_blocks
+    perm = torch.randperm(pool, generator=g)
+    bt = torch.full((dw.R, dw.bt_width), -1, dtype=torch.int32)
+    nxt = 0
+    for r in range(dw.R):
+        a, b = int(first[r]), int(nb[r])
+        bt[r, a:b] = perm[nxt:nxt + b - a].to(torch.int32)
+        nxt += b - a
+    M = dw.M
+    pos = (seq.repeat_interleave(dw.q_len) - dw.q_len + torch.arange(dw.q_len).repeat(dw.R)).to(torch.int64)
+    blk = bt[torch.arange(dw.R).repeat_interleave(dw.q_len), pos // 128].to(torch.int64)
+    slots = blk * 128 + pos % 128
+    if dw.stale == "nan":
+        cache = torch.where(torch.rand(pool, 128, 256, generator=g) < 0.5, 0x7F, 0xFF).to(torch.uint8)
+    else:
+        cache = torch.randint(0, 256, (pool, 128, 256), generator=g, dtype=torch.uint8)
+    # the keys already in the cache: below seq_len - q_len
+    kv = _e4m3_bits(torch.randn(pool * 128, 256, generator=g)).reshape(pool, 128, 256)
+    written = torch.zeros(pool, 128, dtype=torch.bool)
+    for r in range(dw.R):
+        a, b = int(first[r]), int(nb[r])
+        n_old = int(seq[r]) - dw.q_len
+        for c in range(a, b):
+            k = torch.arange(128) + c * 128
+            written[int(bt[r, c])] = k < n_old
+    cache[written] = torch.from_numpy(kv)[written]
+    st = {
+        "seq_lens": seq.to(torch.int32).numpy().copy(),
+        "block_table": bt.numpy().copy(),
+        "positions": pos.numpy().copy(),
+        "slot_mapping": slots.numpy().copy(),
+        "cache": cache.numpy().copy(),
+        "qkv": _bf16_bits(torch.randn(M, 18 * HEAD_DIM, generator=g)),
+        "qn": _bf16_bits(torch.randn(HEAD_DIM, generator=g) * 0.1),
+        "kn": _bf16_bits(torch.randn(HEAD_DIM, generator=g) * 0.1),
+        "cos_sin": cos_sin_table(dw.seq_hi),
+    }
+    return st
