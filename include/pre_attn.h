@@ -368,6 +368,89 @@ float pre_attn_index_scale_log2e(float sm_scale);
  * PA_ERR_ALIGN; PA_ERR_CUDA if the launch fails. */
 int pre_attn_index_scores(const pa_index_args *args, void *stream);
 
+/* ------------------------------------------------ the drafter's attention
+ *
+ * The DSpark drafter's attention (page "vllm.models.minimax_m3.amd.mono.
+ * drafter.attention": module summary, qkv_rows, window, block_math /
+ * block_acc, store_partial, merge_task), as two kernels on `stream`:
+ *   1. q / k head norms and RoPE (qkv_rows): for each of M = R * q_len rows
+ *      of the drafter's projection (16 q heads, then k, then v, 128 bf16
+ *      each), q and k get the step's Gemma head RMSNorm (gammas qn, kn) and
+ *      partial NeoX RoPE at positions[m]; q becomes E4M3 into q8 row
+ *      m * 16 + h, k and v become E4M3 at the row's slot of the drafter
+ *      cache (slot_mapping[m] < 0: not stored).  All unit scale.
+ *   2. split-KV attention and merge: request r's rows sit at p0 + j
+ *      (p0 = positions[r * q_len], j < q_len) and see keys kp with
+ *      lo <= kp <= hi and kp > p0 + j - window, where lo = max(p0 - window
+ *      + 1, 0) and hi = min(seq_lens[r] - 1, (lo / 128 + max_blocks) * 128
+ *      - 1) (window); rows see each other's keys (non-causal).  The blocks
+ *      lo / 128 .. hi / 128 are cut into partitions of part_blocks blocks;
+ *      each partition runs an online softmax over its blocks with scores
+ *      s = q . k, P = exp2(s C - (m C - 8)) (C = sm_scale * log2(e), m the
+ *      running maximum), l summing P and o summing E4M3(P) V (block_acc);
+ *      the partitions are merged in order, out = sum w_i o_i / sum w_i l_i
+ *      with w_i = exp2((m_i - max m) C), rounded to bf16 and quantised to
+ *      MXFP8 (32-value blocks along the row's 16 * 128 values, the smallest
+ *      power-of-two E8M0 scale under which no value exceeds 448).  A row
+ *      with no valid key gets zeros.
+ * The drafter cache is page-128 blocks of 128 keys x 256 bytes (the key's
+ * 128 E4M3 K bytes, then its 128 E4M3 V bytes); slot s is byte s * 256 of
+ * it, block b of request r is block_table[r * bt_width + b].
+ * With qkv == NULL the first kernel is skipped: q8 and the cache are taken
+ * as they are.  All pointers are device pointers owned by the caller. */
+typedef struct pa_drafter_args {
+  const void *qkv;             /* [M, qkv_stride] bf16, or NULL; 16-byte aligned */
+  int64_t qkv_stride;          /* elements a row: a multiple of 8, >= 18 * 128 */
+  const void *qn, *kn;         /* [128] bf16 head-norm gammas of q and k, 16-byte aligned */
+  float eps;                   /* head RMSNorm epsilon */
+  const void *cos_sin;         /* [max_pos, 64] bf16 (cos of the 32 rotary pairs, then sin), 16-byte aligned */
+  int64_t max_pos;             /* positions outside [0, max_pos) are clamped and flagged */
+  const int64_t *positions;    /* [M]: request r's rows at positions[r * q_len] + j */
+  const int64_t *slot_mapping; /* [M] drafter-cache slots of the new keys (< 0: none) */
+  void *cache;                 /* [num_blocks, 128, 256] bytes, 16-byte aligned */
+  int64_t num_blocks;          /* 1 .. 2^24 - 1 */
+  const int32_t *block_table;  /* [R, bt_width] page-128 block ids */
+  int bt_width;
+  const int32_t *seq_lens;     /* [R] keys of each request, its q_len new ones included */
+  int R;                       /* requests, 0 .. 65535 */
+  int q_len;                   /* rows a request, 1 .. 8 (7 on the page) */
+  int window;                  /* sliding window in keys (4096 on the page), >= 1 */
+  int max_blocks;              /* blocks of a window at most (34 covers 4096 keys and 7 rows), >= 1 */
+  int part_blocks;             /* blocks a partition: >= 1, or 0 for pre_attn_drafter_part_blocks' choice */
+  float sm_scale;              /* 1 / sqrt(128) on the page */
+  void *q8;                    /* [M * 16, 128] E4M3: written by kernel 1 (or given), read by kernel 2;
+                                  16-byte aligned */
+  void *out_bf16;              /* [M, 2048] bf16 or NULL, 16-byte aligned */
+  void *out_codes;             /* [M, 2048] E4M3 MXFP8 codes, 16-byte aligned */
+  void *out_scales;            /* [M, 64] E8M0 scale bytes (row-major: scale k covers columns 32k .. 32k + 31) */
+  void *workspace;             /* pre_attn_drafter_workspace_bytes(); zero it once before its first use: every
+                                  call leaves its counters at zero again. 256-byte aligned */
+  size_t workspace_bytes;
+  uint32_t *status;            /* device status word: PA_DEV_POS_RANGE, PA_DEV_SLOT_RANGE (a slot or block id
+                                  outside the cache, or a window block past the block table: that key's store
+                                  or that block skipped), PA_DEV_WAIT_TIMEOUT */
+  uint32_t flags;              /* PA_FLAG_NO_PDL, PA_FLAG_TEST_WAIT_TIMEOUT */
+} pa_drafter_args;
+
+/* The partition length pre_attn_drafter_attention picks for part_blocks = 0:
+ * about two partitions of every request resident on each of num_sms SMs
+ * (the kernel runs two CTAs an SM), at least one block, at most max_blocks.
+ * Pure host arithmetic; returns -PA_ERR_SHAPE for non-positive arguments. */
+int pre_attn_drafter_part_blocks(int R, int max_blocks, int num_sms);
+
+/* Workspace bytes of a call with these sizes (part_blocks >= 1): a counter
+ * per request and one partial (m, l, o) of 128 rows per partition.  Returns
+ * 0 for non-positive arguments. */
+size_t pre_attn_drafter_workspace_bytes(int R, int max_blocks, int part_blocks);
+
+/* Run the drafter's attention on `stream` (see above).  Allocates nothing,
+ * never synchronises; kernel 2 waits for kernel 1 (and kernel 1 for the
+ * previous kernel on the stream) through programmatic dependent launch.
+ * Errors (nothing launched): PA_ERR_NULL, PA_ERR_SHAPE, PA_ERR_CONFIG
+ * (window, max_blocks or part_blocks < 0 / 0, a NaN scale), PA_ERR_ALIGN,
+ * PA_ERR_WORKSPACE; PA_ERR_CUDA if a launch fails. */
+int pre_attn_drafter_attention(const pa_drafter_args *args, void *stream);
+
 /* Main kernels a call can run (pre_attn_path). */
 enum {
   PA_PATH_GEMV = 0,         /* skinny path: prologue, then the FP8 GEMV on one cluster per head */

@@ -73,6 +73,16 @@ class pa_index_args(ctypes.Structure):
                 ("score_stride", ctypes.c_int64), ("status", _vp)]
 
 
+class pa_drafter_args(ctypes.Structure):
+    _fields_ = [("qkv", _vp), ("qkv_stride", ctypes.c_int64), ("qn", _vp), ("kn", _vp), ("eps", ctypes.c_float),
+                ("cos_sin", _vp), ("max_pos", ctypes.c_int64), ("positions", _vp), ("slot_mapping", _vp),
+                ("cache", _vp), ("num_blocks", ctypes.c_int64), ("block_table", _vp), ("bt_width", ctypes.c_int),
+                ("seq_lens", _vp), ("R", ctypes.c_int), ("q_len", ctypes.c_int), ("window", ctypes.c_int),
+                ("max_blocks", ctypes.c_int), ("part_blocks", ctypes.c_int), ("sm_scale", ctypes.c_float),
+                ("q8", _vp), ("out_bf16", _vp), ("out_codes", _vp), ("out_scales", _vp), ("workspace", _vp),
+                ("workspace_bytes", ctypes.c_size_t), ("status", _vp), ("flags", ctypes.c_uint32)]
+
+
 class PreAttnError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
@@ -113,6 +123,9 @@ def load(path: str = LIB_PATH):
         "pre_attn_wait_done": (i, [_vp, ctypes.c_int64, ctypes.c_uint32, ctypes.c_uint32, _vp, _vp]),
         "pre_attn_index_scale_log2e": (ctypes.c_float, [ctypes.c_float]),
         "pre_attn_index_scores": (i, [ctypes.POINTER(pa_index_args), _vp]),
+        "pre_attn_drafter_part_blocks": (i, [i, i, i]),
+        "pre_attn_drafter_workspace_bytes": (sz, [i, i, i]),
+        "pre_attn_drafter_attention": (i, [ctypes.POINTER(pa_drafter_args), _vp]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -254,6 +267,22 @@ def pre_attn_index_scores(args: pa_index_args, stream=None, check: bool = True) 
     st = load().pre_attn_index_scores(ctypes.byref(args), stream_ptr(stream))
     if check and st != PA_OK:
         raise PreAttnError(st, "pre_attn_index_scores " + (pre_attn_last_cuda_error() if st == PA_ERR_CUDA else ""))
+    return st
+
+
+def pre_attn_drafter_part_blocks(R: int, max_blocks: int, num_sms: int) -> int:
+    return int(load().pre_attn_drafter_part_blocks(int(R), int(max_blocks), int(num_sms)))
+
+
+def pre_attn_drafter_workspace_bytes(R: int, max_blocks: int, part_blocks: int) -> int:
+    return int(load().pre_attn_drafter_workspace_bytes(int(R), int(max_blocks), int(part_blocks)))
+
+
+def pre_attn_drafter_attention(args: pa_drafter_args, stream=None, check: bool = True) -> int:
+    st = load().pre_attn_drafter_attention(ctypes.byref(args), stream_ptr(stream))
+    if check and st != PA_OK:
+        raise PreAttnError(st, "pre_attn_drafter_attention " +
+                           (pre_attn_last_cuda_error() if st == PA_ERR_CUDA else ""))
     return st
 
 

@@ -211,3 +211,56 @@ def test_harness_masks_match_oracle_offsets():
                 f = L.ora_nvfp4_sf_vswz_offset if sl % 2 else L.ora_nvfp4_sf_linear_offset
                 wf[base + f(16, sl, s % 16, g)] = True
     assert np.array_equal(dm, wd) and np.array_equal(fm, wf)
+
+
+def test_drafter_partition_choice_and_workspace(B):
+    # about two resident partitions of every request an SM, at least one block
+    assert B.pre_attn_drafter_part_blocks(64, 34, 152) == 9   # 304 / 64 -> 4 partitions of <= 9 blocks
+    assert B.pre_attn_drafter_part_blocks(1, 34, 152) == 1
+    assert B.pre_attn_drafter_part_blocks(1000, 34, 152) == 34
+    assert B.pre_attn_drafter_part_blocks(152, 34, 152) == 17
+    assert B.pre_attn_drafter_part_blocks(0, 34, 152) < 0
+    # a counter per request (256-byte rounded), then ceil(34 / 9) = 4 partials of
+    # 128 m + 128 l + 128 x 128 o f32 per request
+    assert B.pre_attn_drafter_workspace_bytes(64, 34, 9) == 256 + 64 * 4 * (1024 + 65536)
+    assert B.pre_attn_drafter_workspace_bytes(65, 34, 34) == 512 + 65 * (1024 + 65536)
+    assert B.pre_attn_drafter_workspace_bytes(0, 34, 9) == 0
+
+
+def _drafter_args(B, bufs, **kw):
+    a = B.pa_drafter_args()
+    for k in ("positions", "cache", "block_table", "seq_lens", "q8", "out_codes", "out_scales", "workspace",
+              "status"):
+        setattr(a, k, bufs[k])
+    a.num_blocks, a.bt_width, a.R, a.q_len = 16, 8, 2, 7
+    a.window, a.max_blocks, a.part_blocks, a.sm_scale = 4096, 34, 4, 128 ** -0.5
+    a.workspace_bytes = B.pre_attn_drafter_workspace_bytes(2, 34, 4)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_drafter_validation_codes(B):
+    # fake, aligned "device" addresses: every case returns before any launch
+    base = 1 << 40
+    bufs = {k: base + i * (1 << 24) for i, k in enumerate(
+        ("positions", "cache", "block_table", "seq_lens", "q8", "out_codes", "out_scales", "workspace", "status"))}
+    run = lambda **kw: B.pre_attn_drafter_attention(_drafter_args(B, bufs, **kw), None, check=False)  # noqa: E731
+    assert B.load().pre_attn_drafter_attention(None, None) == B.PA_ERR_NULL
+    for k in ("positions", "cache", "block_table", "seq_lens", "q8", "out_codes", "out_scales", "workspace", "status"):
+        assert run(**{k: None}) == B.PA_ERR_NULL, k
+    assert run(qkv=base) == B.PA_ERR_NULL  # qkv without its gammas, table and slots
+    for bad in (dict(R=-1), dict(R=65536), dict(q_len=0), dict(q_len=9), dict(bt_width=0), dict(num_blocks=0),
+                dict(num_blocks=1 << 24)):
+        assert run(**bad) == B.PA_ERR_SHAPE, bad
+    q = dict(qkv=base, qn=base, kn=base, cos_sin=base, slot_mapping=base, max_pos=64)
+    assert run(**q, qkv_stride=18 * 128 - 8) == B.PA_ERR_SHAPE
+    assert run(**q, qkv_stride=18 * 128 + 4) == B.PA_ERR_SHAPE
+    for bad in (dict(window=0), dict(max_blocks=0), dict(part_blocks=-1), dict(sm_scale=float("nan"))):
+        assert run(**bad) == B.PA_ERR_CONFIG, bad
+    assert run(**q, qkv_stride=18 * 128, eps=-1.0) == B.PA_ERR_CONFIG
+    for k, off in (("cache", 8), ("q8", 4), ("out_codes", 8), ("workspace", 128), ("status", 2), ("positions", 4)):
+        assert run(**{k: bufs[k] + off}) == B.PA_ERR_ALIGN, k
+    assert run(out_bf16=base + 8) == B.PA_ERR_ALIGN
+    assert run(workspace_bytes=100) == B.PA_ERR_WORKSPACE
+    assert run(R=0) == B.PA_OK  # nothing to do: nothing launched

@@ -1,0 +1,266 @@
+"""GPU parity of the drafter's attention (pre_attn_drafter_attention) against
+the CPU oracle, through the C-ABI.
+
+Both sides take the same seeded inputs and the same partition length.
+Where they may differ, and the bounds used:
+  - q8 and the new K codes (head norm in f32 on the GPU, in double in the
+    oracle): one E4M3 step at most, in at most 0.1% of the codes; V codes
+    and every cache byte the call must not touch: exactly.
+  - the bf16 output: the scores are f32 sums of exact FP8 products on the
+    tensor cores, the exponentials the SFU's ex2 (a few ulp), and P's E4M3
+    code can flip where p sits on a rounding boundary; each flip moves the
+    output by one P step x |v| / l, far below one bf16 step of a typical
+    output.  The bound is the step's bf16 tolerance, 1e-2 + 2e-2 |oracle|.
+    Measured: 99.9% of the bf16 outputs are bit-identical to the oracle's
+    and the largest difference is a few bf16 steps; the test also requires
+    at least 99% to be identical.
+  - MXFP8: a code is a function of its 32-value bf16 block, so every block
+    whose bf16 values equal the oracle's must carry the oracle's scale and
+    codes exactly; and, as a property of the GPU's own output, every scale
+    and code must be the MXFP8 encoding (smallest power-of-two scale with
+    no value above 448, torch's E4M3 cast) of the GPU's bf16 values.  (A
+    one-step code bound would be stricter than the bf16 tolerance for values
+    far below their block's maximum, where one E4M3 step is a tiny amount.)
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+def _dev(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).to("cuda")
+
+
+def gpu_run(dw, st, part_blocks, with_qkv=True, flags=0, bf16=True, reps=1):
+    import torch
+
+    from indexer_projection_gb300 import binding as B
+
+    M = dw.M
+    d = {k: _dev(v) for k, v in st.items() if k not in ("q8", "qkv", "qn", "kn", "cos_sin")}
+    d["qkv"] = _dev(st["qkv"].view(np.int16))
+    d["qn"], d["kn"] = _dev(st["qn"].view(np.int16)), _dev(st["kn"].view(np.int16))
+    d["cos_sin"] = _dev(st["cos_sin"].view(np.int16))
+    q8 = _dev(st["q8"]) if not with_qkv else torch.full((M * 16, 128), 0xA5, dtype=torch.uint8, device="cuda")
+    out = torch.full((M, 2048), -1, dtype=torch.int16, device="cuda")
+    codes = torch.full((M, 2048), 0xA5, dtype=torch.uint8, device="cuda")
+    scales = torch.full((M, 64), 0xA5, dtype=torch.uint8, device="cuda")
+    pb = part_blocks
+    if pb == 0:
+        pb = B.pre_attn_drafter_part_blocks(dw.R, dw.max_blocks, torch.cuda.get_device_properties(0).multi_processor_count)
+    wsb = B.pre_attn_drafter_workspace_bytes(dw.R, dw.max_blocks, pb)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    a = B.pa_drafter_args()
+    if with_qkv:
+        a.qkv, a.qkv_stride = B.ptr(d["qkv"]), d["qkv"].shape[1]
+        a.qn, a.kn, a.eps = B.ptr(d["qn"]), B.ptr(d["kn"]), dw.eps
+        a.cos_sin, a.max_pos = B.ptr(d["cos_sin"]), d["cos_sin"].shape[0]
+        a.slot_mapping = B.ptr(d["slot_mapping"])
+    a.positions = B.ptr(d["positions"])
+    a.cache, a.num_blocks = B.ptr(d["cache"]), d["cache"].shape[0]
+    a.block_table, a.bt_width = B.ptr(d["block_table"]), d["block_table"].shape[1]
+    a.seq_lens, a.R, a.q_len = B.ptr(d["seq_lens"]), dw.R, dw.q_len
+    a.window, a.max_blocks, a.part_blocks, a.sm_scale = dw.window, dw.max_blocks, part_blocks, dw.sm_scale
+    a.q8 = B.ptr(q8)
+    a.out_bf16 = B.ptr(out) if bf16 else None
+    a.out_codes, a.out_scales = B.ptr(codes), B.ptr(scales)
+    a.workspace, a.workspace_bytes = B.ptr(ws), wsb
+    a.status, a.flags = B.ptr(status), flags
+    for _ in range(reps):
+        B.pre_attn_drafter_attention(a, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    return {"q8": q8.cpu().numpy(), "out": out.cpu().numpy().view(np.uint16), "codes": codes.cpu().numpy(),
+            "scales": scales.cpu().numpy(), "cache": d["cache"].cpu().numpy(), "status": int(status.item()),
+            "ws": ws, "pb": pb}
+
+
+def oracle_run(dw, st, pb, with_qkv=True):
+    cache = st["cache"].copy()
+    if with_qkv:
+        q8 = oracle.drafter_qkv(st["qkv"], st["qn"], st["kn"], dw.eps, st["cos_sin"], st["positions"],
+                                st["slot_mapping"], cache)
+    else:
+        q8 = st["q8"]
+    out, codes, scales = oracle.drafter_attention(q8, cache, st["block_table"], st["seq_lens"], st["positions"],
+                                                  dw.q_len, dw.window, dw.max_blocks, pb, dw.sm_scale)
+    return {"q8": q8, "cache": cache, "out": out, "codes": codes, "scales": scales}
+
+
+def _e4m3_rank(c):
+    """E4M3 codes -> signed rank (adjacent values differ by 1; +0 and -0 both 0)."""
+    c = np.asarray(c, np.int64)
+    mag = c & 0x7F
+    return np.where(c & 0x80, -mag, mag)
+
+
+def check_codes_close(got, want, what, frac=1e-3):
+    d = np.abs(_e4m3_rank(got) - _e4m3_rank(want))
+    assert d.max(initial=0) <= 1, f"{what}: a code {d.max()} steps off"
+    n = int((d > 0).sum())
+    assert n <= max(1, frac * d.size), f"{what}: {n} of {d.size} codes differ"
+    return n
+
+
+def _bf16(bits):
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def mx_encode(bits):
+    """MXFP8 of bf16 rows [M, 2048]: (codes, scale bytes) with the smallest
+    e such that 448 * 2^e >= the block's amax, codes = torch's E4M3 cast."""
+    import torch
+    x = _bf16(bits).reshape(bits.shape[0], -1, 32)
+    amax = np.abs(x).max(axis=2)
+    e = np.zeros(amax.shape, np.int64)
+    nz = amax > 0
+    e[nz] = np.ceil(np.log2(amax[nz] / 448.0)).astype(np.int64)
+    e = np.where(448.0 * np.ldexp(1.0, e - 1) >= amax, e - 1, e)  # log2 rounding either way
+    e = np.where(448.0 * np.ldexp(1.0, e) < amax, e + 1, e)
+    e = np.where(nz, np.clip(e, -127, 127), 0)
+    y = (x * np.ldexp(1.0, -e)[:, :, None]).astype(np.float32)
+    codes = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy().reshape(bits.shape[0], -1)
+    return codes, (e + 127).astype(np.uint8)
+
+
+def check_outputs(dw, g, o):
+    x, y = _bf16(g["out"]), _bf16(o["out"])
+    assert np.all(np.isfinite(x)), "non-finite output"
+    err = np.abs(x - y) - (1e-2 + 2e-2 * np.abs(y))
+    assert err.max() <= 0, f"bf16 out: max excess {err.max():.3g} (max |diff| {np.abs(x - y).max():.3g})"
+    differ = float((g["out"] != o["out"]).mean())
+    assert differ <= 1e-2, f"bf16 out: {differ:.4f} of the values differ from the oracle's"
+    # blocks with the oracle's bf16 values: the oracle's scale and codes
+    same = np.all((g["out"] == o["out"]).reshape(g["out"].shape[0], -1, 32), axis=2)
+    assert np.array_equal(g["scales"][same], o["scales"][same]), "MXFP8 scales of identical blocks"
+    sc = np.repeat(same, 32, axis=1)
+    assert np.array_equal(g["codes"][sc], o["codes"][sc]), "MXFP8 codes of identical blocks"
+    # every block: the MXFP8 encoding of the GPU's own bf16 values
+    codes, scales = mx_encode(g["out"])
+    assert np.array_equal(g["scales"], scales), "MXFP8 scales are not the encoding of the bf16 output"
+    assert np.array_equal(g["codes"], codes), "MXFP8 codes are not the encoding of the bf16 output"
+
+
+def check_cache(dw, st, g, o):
+    """K codes within a step, V exact, everything else untouched."""
+    gc, oc = g["cache"].reshape(-1, 256), o["cache"].reshape(-1, 256)
+    slots = st["slot_mapping"][st["slot_mapping"] >= 0]
+    check_codes_close(gc[slots, :128], oc[slots, :128], "K cache")
+    assert np.array_equal(gc[slots, 128:], oc[slots, 128:]), "V cache"
+    rest = np.ones(gc.shape[0], bool)
+    rest[slots] = False
+    assert np.array_equal(gc[rest], st["cache"].reshape(-1, 256)[rest]), "bytes outside the new slots changed"
+
+
+def full_check(dw, part_blocks=3, with_qkv=True):
+    st = workloads.drafter_host_state(dw)
+    g = gpu_run(dw, st, part_blocks, with_qkv=with_qkv)
+    assert g["status"] == 0
+    o = oracle_run(dw, st, g["pb"], with_qkv=with_qkv)
+    if with_qkv:
+        check_codes_close(g["q8"], o["q8"], "q8")
+        check_cache(dw, st, g, o)
+    check_outputs(dw, g, o)
+    return g, o
+
+
+def test_attention_alone_matches_the_oracle():
+    dw = workloads.DrafterWorkload("da", R=6, q_len=7, seq_lo=200, seq_hi=9000, seed=31, prefilled=True)
+    full_check(dw, 3, with_qkv=False)
+
+
+def test_full_path_matches_the_oracle():
+    dw = workloads.DrafterWorkload("df", R=6, q_len=7, seq_lo=200, seq_hi=9000, seed=32)
+    full_check(dw, 4)
+
+
+@pytest.mark.parametrize("pb", [1, 2, 5, 34, 0])
+def test_partition_lengths(pb):
+    dw = workloads.DrafterWorkload(f"dp{pb}", R=4, q_len=7, seq_lo=3000, seq_hi=9000, seed=40 + pb)
+    full_check(dw, pb)
+
+
+@pytest.mark.parametrize("q_len,window,seq_lo,seq_hi,maxb", [
+    (1, 4096, 1, 5000, 33),     # one row a request; requests shorter than a block
+    (8, 4096, 8, 9000, 34),     # the 128-row tile full
+    (7, 100, 7, 3000, 34),      # a window inside one or two blocks: rows masked apart
+    (7, 4096, 7, 600, 34),      # lo = 0 everywhere
+    (7, 4096, 2000, 9000, 3),   # max_blocks clips the window
+    (3, 129, 300, 2000, 34),    # a window one key over a block
+])
+def test_shapes_and_windows(q_len, window, seq_lo, seq_hi, maxb):
+    dw = workloads.DrafterWorkload("ds", R=5, q_len=q_len, seq_lo=seq_lo, seq_hi=seq_hi, seed=q_len * 7 + window,
+                                   window=window, max_blocks=maxb)
+    full_check(dw, 2)
+
+
+def test_stale_bytes_random_instead_of_nan():
+    dw = workloads.DrafterWorkload("dr", R=4, q_len=7, seq_lo=100, seq_hi=5000, seed=51, stale="random")
+    full_check(dw, 3)
+
+
+def test_spec_decode_configuration_every_row():
+    # the full speculative-decode shape in the launch configuration the
+    # benchmark times (the library's partition length), every row compared
+    dw = workloads.drafter_spec_decode()
+    full_check(dw, 0)
+
+
+def test_repeated_calls_are_identical_and_leave_counters_zero():
+    dw = workloads.DrafterWorkload("drep", R=5, q_len=7, seq_lo=2000, seq_hi=9000, seed=61, prefilled=True)
+    st = workloads.drafter_host_state(dw)
+    g1 = gpu_run(dw, st, 2, with_qkv=False)
+    g3 = gpu_run(dw, st, 2, with_qkv=False, reps=3)
+    for k in ("out", "codes", "scales"):
+        assert np.array_equal(g1[k], g3[k]), k
+    assert not g3["ws"][: 4 * dw.R].cpu().numpy().any()  # the per-request counters
+
+
+def test_empty_window_rows_are_zero():
+    dw = workloads.DrafterWorkload("de", R=3, q_len=7, seq_lo=3000, seq_hi=5000, seed=71, prefilled=True)
+    st = workloads.drafter_host_state(dw)
+    st["seq_lens"][1] = 1  # request 1 ends before its window starts: no key at all
+    g = gpu_run(dw, st, 2, with_qkv=False)
+    o = oracle_run(dw, st, 2, with_qkv=False)
+    assert g["status"] == 0
+    assert not g["codes"][7:14].any() and np.all(g["scales"][7:14] == 127) and not g["out"][7:14].any()
+    check_outputs(dw, g, o)
+
+
+def test_bad_block_ids_are_flagged_and_other_requests_exact():
+    from indexer_projection_gb300 import binding as B
+
+    dw = workloads.DrafterWorkload("db", R=3, q_len=7, seq_lo=3000, seq_hi=5000, seed=81, prefilled=True)
+    st = workloads.drafter_host_state(dw)
+    lo, hi = oracle.drafter_window(int(st["positions"][7]), int(st["seq_lens"][1]), dw.window, dw.max_blocks)
+    st["block_table"][1, lo // 128 + 1] = st["cache"].shape[0] + 5  # request 1: a block id past the cache
+    g = gpu_run(dw, st, 2, with_qkv=False)
+    assert g["status"] & B.PA_DEV_SLOT_RANGE
+    good = dict(st)
+    keep = [0, 2]
+    good["block_table"] = st["block_table"][keep]
+    good["seq_lens"] = st["seq_lens"][keep]
+    good["positions"] = st["positions"].reshape(3, 7)[keep].reshape(-1)
+    good["q8"] = st["q8"].reshape(3, 7 * 16, 128)[keep].reshape(-1, 128)
+    o = oracle_run(workloads.DrafterWorkload("db2", R=2, q_len=7, seq_lo=1, seq_hi=2, seed=0), good, 2,
+                   with_qkv=False)
+    sub = {k: g[k].reshape(3, 7, -1)[keep].reshape(14, -1) for k in ("out", "codes", "scales")}
+    check_outputs(dw, sub, o)
+
+
+def test_a_wait_that_runs_out_is_reported_and_the_next_call_is_clean():
+    from indexer_projection_gb300 import binding as B
+
+    dw = workloads.DrafterWorkload("dt", R=2, q_len=7, seq_lo=2000, seq_hi=5000, seed=91, prefilled=True)
+    st = workloads.drafter_host_state(dw)
+    g = gpu_run(dw, st, 2, with_qkv=False, flags=B.PA_FLAG_TEST_WAIT_TIMEOUT)
+    assert g["status"] & B.PA_DEV_WAIT_TIMEOUT
+    g2 = gpu_run(dw, st, 2, with_qkv=False)
+    assert g2["status"] == 0
+    check_outputs(dw, g2, oracle_run(dw, st, 2, with_qkv=False))

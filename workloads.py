@@ -385,6 +385,7 @@ class DrafterWorkload:
     eps: float = 1e-6
     stale: str = "nan"
     spare_blocks: int = 8
+    prefilled: bool = False  # the new rows' keys already in the cache, q8 given (attention alone)
 
     @property
     def M(self) -> int:
@@ -407,7 +408,8 @@ def drafter_host_state(dw: DrafterWorkload) -> dict:
     """qkv [M, 18 * 128] bf16 bits ~ N(0, 1); qn, kn [128] bf16 bits ~ N(0, 0.1);
     cos_sin [seq_hi, 64] bf16 bits; positions, slot_mapping [M] int64;
     seq_lens [R] int32; block_table [R, bt_width] int32; cache [blocks, 128,
-    256] uint8 (see DrafterWorkload)."""
+    256] uint8 (see DrafterWorkload); with `prefilled`, q8 [M * 16, 128]
+    E4M3 codes."""
     g = torch.Generator().manual_seed(dw.seed)
     seq = torch.randint(dw.seq_lo, dw.seq_hi, (dw.R,), generator=g, dtype=torch.int64)
     seq = torch.maximum(seq, torch.full_like(seq, dw.q_len))
@@ -430,12 +432,12 @@ def drafter_host_state(dw: DrafterWorkload) -> dict:
         cache = torch.where(torch.rand(pool, 128, 256, generator=g) < 0.5, 0x7F, 0xFF).to(torch.uint8)
     else:
         cache = torch.randint(0, 256, (pool, 128, 256), generator=g, dtype=torch.uint8)
-    # the keys already in the cache: below seq_len - q_len
+    # the keys already in the cache: below seq_len - q_len (below seq_len when prefilled)
     kv = _e4m3_bits(torch.randn(pool * 128, 256, generator=g)).reshape(pool, 128, 256)
     written = torch.zeros(pool, 128, dtype=torch.bool)
     for r in range(dw.R):
         a, b = int(first[r]), int(nb[r])
-        n_old = int(seq[r]) - dw.q_len
+        n_old = int(seq[r]) - (0 if dw.prefilled else dw.q_len)
         for c in range(a, b):
             k = torch.arange(128) + c * 128
             written[int(bt[r, c])] = k < n_old
@@ -451,4 +453,6 @@ def drafter_host_state(dw: DrafterWorkload) -> dict:
         "kn": _bf16_bits(torch.randn(HEAD_DIM, generator=g) * 0.1),
         "cos_sin": cos_sin_table(dw.seq_hi),
     }
+    if dw.prefilled:  # E4M3 codes of N(0, 1) q rows (a normed q has unit RMS)
+        st["q8"] = _e4m3_bits(torch.randn(M * 16, HEAD_DIM, generator=g))
     return st
