@@ -3,7 +3,7 @@
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
                   [--workload decode|spec_decode|prefill|tiny|sweep_m<M>]
-                  [--also prefill,spec_decode,index_spec_decode|none]
+                  [--also prefill,spec_decode,index_spec_decode,drafter_spec_decode|none]
 
 A step is one pre_attn_run() (prologue + skinny GEMV or tcgen05 GEMM with the
 fused head epilogue) over one batch of the workload's synthetic inputs.  The
@@ -14,7 +14,9 @@ Rank 0 prints one JSON line: the headline workload (decode by default) and,
 under their names, the workloads of --also timed in the same run (prefill
 and speculative decode: their own graphs of steps, at least a second of
 them, each with its own clock record; the indexer scores of the
-speculative-decode shape: a graph of pre_attn_index_scores launches).
+speculative-decode shape: a graph of pre_attn_index_scores launches; the
+drafter's attention at that shape: graphs of pre_attn_drafter_attention
+calls).
 Under torchrun each rank runs an independent replica (the step has no
 cross-GPU exchange) and the slowest rank's time sets the aggregate tokens/s.
 
@@ -98,7 +100,8 @@ KERNEL_SOURCES = {"skinny": ("pa_gemv.cu", "pa_device.cuh", "pa_tc.cuh", "pa_nor
                   "gemm": ("pa_gemm.cu", "pa_device.cuh", "pa_tc.cuh"),
                   "gemm_pair": ("pa_gemm2.cu", "pa_device.cuh", "pa_tc.cuh"),
                   "prologue": ("pa_prologue.cu", "pa_device.cuh", "pa_norm.cuh"),
-                  "index_scores": ("pa_index.cu", "pa_device.cuh", "pa_tma.h")}
+                  "index_scores": ("pa_index.cu", "pa_device.cuh", "pa_tma.h"),
+                  "drafter_attn": ("pa_drafter.cu", "pa_device.cuh", "pa_tc.cuh", "pa_tma.h")}
 
 
 def kernel_sha(kernel: str) -> str:
@@ -653,6 +656,170 @@ def index_secondary(args, name, dev, world, peaks):
             "status": int(status.item()), "clocks": clocks}
 
 
+def drafter_windows(dw, st):
+    """Keys lo .. hi of each request's window (first row's window start,
+    below seq_len, at most max_blocks blocks from lo's block)."""
+    out = []
+    for r in range(dw.R):
+        p0 = int(st["positions"][r * dw.q_len])
+        lo = max(p0 - (dw.window - 1), 0)
+        hi = min(int(st["seq_lens"][r]) - 1, (lo // 128 + dw.max_blocks) * 128 - 1)
+        out.append((lo, hi))
+    return out
+
+
+def drafter_accounting(dw, st) -> dict:
+    """Algorithmic bytes and tensor FLOPs of one drafter call: the window's
+    K and V bytes read once, the projection rows read, the new keys written,
+    the MXFP8 output and scales written, the metadata read; QK^T and PV over
+    every (row, head, window key)."""
+    keys = sum(hi - lo + 1 for lo, hi in drafter_windows(dw, st) if hi >= lo)
+    blocks = sum(hi // 128 - lo // 128 + 1 for lo, hi in drafter_windows(dw, st) if hi >= lo)
+    M = dw.M
+    attn = keys * 256 + blocks * 4 + dw.R * 4 + M * 8 + M * 2048 + M * 64
+    qkv = M * 18 * 128 * 2 + M * 256 + M * 16 + M * 64 * 2 + 2 * 128 * 2
+    flops = 2 * 2 * 16 * dw.q_len * keys * 128
+    return {"keys": keys, "attn_bytes": attn, "call_bytes": attn + qkv, "flops": flops}
+
+
+def drafter_secondary(args, name, dev, world, peaks, peak_src):
+    """The drafter's attention at a configuration's shape: a CUDA graph of
+    whole calls (both kernels) rotating over copies of the drafter cache and
+    inputs larger than twice the L2, and a graph of the attention kernel
+    alone (its q8 rows and new keys already in place) for its roofline."""
+    import torch
+
+    from indexer_projection_gb300 import binding as B
+
+    dw = workloads.DRAFTER_CONFIGS[name]()
+    st = workloads.drafter_host_state(dw)
+    acc = drafter_accounting(dw, st)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    per_copy = st["cache"].nbytes + st["qkv"].nbytes
+    copies = max(2, math.ceil(2 * l2 / per_copy) + 1)
+    shared = {k: t(st[k]) for k in ("positions", "slot_mapping", "block_table", "seq_lens")}
+    shared["qn"], shared["kn"] = t(st["qn"].view(np.int16)), t(st["kn"].view(np.int16))
+    shared["cos_sin"] = t(st["cos_sin"].view(np.int16))
+    M = dw.M
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    pb = B.pre_attn_drafter_part_blocks(dw.R, dw.max_blocks, sms)
+    wsb = B.pre_attn_drafter_workspace_bytes(dw.R, dw.max_blocks, pb)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    codes = torch.empty(M, 2048, dtype=torch.uint8, device=dev)
+    scales = torch.empty(M, 64, dtype=torch.uint8, device=dev)
+    bufs, args_full, args_attn = [], [], []
+    for c in range(copies):
+        cache, qkv = t(st["cache"]), t(st["qkv"].view(np.int16))
+        q8 = torch.empty(M * 16, 128, dtype=torch.uint8, device=dev)
+        bufs.append((cache, qkv, q8))
+        for with_qkv, lst in ((True, args_full), (False, args_attn)):
+            a = B.pa_drafter_args()
+            if with_qkv:
+                a.qkv, a.qkv_stride = B.ptr(qkv), qkv.shape[1]
+                a.qn, a.kn, a.eps = B.ptr(shared["qn"]), B.ptr(shared["kn"]), dw.eps
+                a.cos_sin, a.max_pos = B.ptr(shared["cos_sin"]), shared["cos_sin"].shape[0]
+                a.slot_mapping = B.ptr(shared["slot_mapping"])
+            a.positions = B.ptr(shared["positions"])
+            a.cache, a.num_blocks = B.ptr(cache), cache.shape[0]
+            a.block_table, a.bt_width = B.ptr(shared["block_table"]), shared["block_table"].shape[1]
+            a.seq_lens, a.R, a.q_len = B.ptr(shared["seq_lens"]), dw.R, dw.q_len
+            a.window, a.max_blocks, a.part_blocks, a.sm_scale = dw.window, dw.max_blocks, pb, dw.sm_scale
+            a.q8, a.out_codes, a.out_scales = B.ptr(q8), B.ptr(codes), B.ptr(scales)
+            a.workspace, a.workspace_bytes, a.status = B.ptr(ws), wsb, B.ptr(status)
+            lst.append(a)
+    stream = torch.cuda.Stream(dev)
+    K = max(20, min(args.steps, 200))
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+
+    def timed(arg_list):
+        with torch.cuda.stream(stream):
+            for i in range(5):
+                B.pre_attn_drafter_attention(arg_list[i % copies], stream)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(K):
+                B.pre_attn_drafter_attention(arg_list[i % copies], stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        stream.synchronize()
+        reps = max(1, math.ceil(0.5e3 / max(e0.elapsed_time(e1), 1e-3)))
+        t0 = time.time()
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(int(200e-6 * 2.1e9))
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        stream.synchronize()
+        t1 = time.time()
+        ms = max_over_ranks([e0.elapsed_time(e1)], world, dev)[0] / (reps * K)
+        del g
+        return ms, reps * K, t0, t1
+
+    # the full calls first: they write every copy's q8 rows and new keys,
+    # which the attention-only graph then reads
+    ms_call, n_call, t0, _ = timed(args_full)
+    ms_att3, n_attn, _, t1 = timed(args_attn)
+    # the attention kernel alone: events recorded around it, calls queued
+    # behind a GPU sleep so the host never starves the GPU between them
+    P = 64
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(P)]
+    with torch.cuda.stream(stream):
+        for e0, e1 in evs:
+            e0.record(stream)
+            e1.record(stream)
+    stream.synchronize()
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(2e-3 * 2.1e9))
+        for i, (e0, e1) in enumerate(evs):
+            a = args_attn[i % copies]
+            a.prof_before, a.prof_after = e0.cuda_event, e1.cuda_event
+            B.pre_attn_drafter_attention(a, stream)
+            a.prof_before, a.prof_after = None, None
+    stream.synchronize()
+    ms_attn = max_over_ranks([statistics.median(e0.elapsed_time(e1) for e0, e1 in evs[P // 4:])], world, dev)[0]
+    time.sleep(0.06)
+    clocks = sampler.summary(t0, t1)
+    sampler.stop()
+    hbm = peaks["hbm_gbs"]
+    fp8 = peaks["bf16_tflops"] * FP8_OVER_BF16
+    a_gbs = acc["attn_bytes"] / (ms_attn * 1e-3) / 1e9
+    c_gbs = acc["call_bytes"] / (ms_call * 1e-3) / 1e9
+    out = {"config": {"workload": name, "requests": dw.R, "q_len": dw.q_len, "window": dw.window,
+                      "max_blocks": dw.max_blocks, "part_blocks": pb, "seq_lens": f"U[{dw.seq_lo}, {dw.seq_hi})",
+                      "window_keys": acc["keys"]},
+           "kernels": "pa_drafter_qkv_kernel (head norm, RoPE, FP8, cache insert) + pa_drafter_attn_kernel "
+                      "(tcgen05 S = QK^T, O += PV in TMEM, TMA K/V from the cache) + pa_drafter_merge_kernel "
+                      "(ordered merge, bf16, MXFP8)",
+           "l2": f"{copies} rotating cache + input copies ({copies * per_copy / 1e6:.0f} MB > 2x L2)",
+           "us_per_call": round(ms_call * 1e3, 3), "calls": n_call,
+           "rows_per_s": round(M / (ms_call * 1e-3), 1),
+           "call_hbm_frac": round(c_gbs / hbm, 4),
+           "us_attention_and_merge": round(ms_att3 * 1e3, 3),
+           "us_attention_kernel": round(ms_attn * 1e3, 3), "attention_timing": "median of 48 launches, "
+                                  "CUDA events around the kernel on its stream",
+           "roofline": {"bound": "hbm", "achieved": round(a_gbs, 1), "peak": hbm, "unit": "GB/s",
+                        "frac": round(a_gbs / hbm, 4), "traffic": ncu_traffic("drafter_attn", name),
+                        "algorithmic_bytes": acc["attn_bytes"], "peak_source": f"{peak_src} copy"},
+           "tensor": {"achieved_tflops": round(acc["flops"] / (ms_attn * 1e-3) / 1e12, 1),
+                      "peak_tflops": round(fp8, 1),
+                      "frac": round(acc["flops"] / (ms_attn * 1e-3) / 1e12 / fp8, 4),
+                      "peak_source": f"burst bf16 of {peak_src} x {FP8_OVER_BF16:g}"},
+           "gpu_launches": 3 * n_call + 2 * n_attn + 2 * P,
+           "status": int(status.item()), "clocks": clocks}
+    del bufs, args_full, args_attn
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, wl, rank, world, local_rank):
     import torch
 
@@ -695,6 +862,8 @@ def run_ours(args, wl, rank, world, local_rank):
     for name in [x for x in args.also.split(",") if x and x != "none" and x != args.workload]:
         if name in workloads.INDEX_CONFIGS:
             line[name] = index_secondary(args, name, dev, world, peaks)
+        elif name in workloads.DRAFTER_CONFIGS:
+            line[name] = drafter_secondary(args, name, dev, world, peaks, peak_src)
         else:
             line[name] = secondary(args, name, dev, world, peaks, peak_src)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -792,7 +961,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference", "ours"])
     ap.add_argument("--workload", default="decode")
-    ap.add_argument("--also", default="prefill,spec_decode,index_spec_decode",
+    ap.add_argument("--also", default="prefill,spec_decode,index_spec_decode,drafter_spec_decode",
                     help="comma-separated workloads also timed in the same run, each reported under its name "
                          "(the step's configurations, or an indexer-score configuration); none: skip")
     ap.add_argument("--no-cpu-baseline", action="store_true")

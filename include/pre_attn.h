@@ -372,14 +372,14 @@ int pre_attn_index_scores(const pa_index_args *args, void *stream);
  *
  * The DSpark drafter's attention (page "vllm.models.minimax_m3.amd.mono.
  * drafter.attention": module summary, qkv_rows, window, block_math /
- * block_acc, store_partial, merge_task), as two kernels on `stream`:
+ * block_acc, store_partial, merge_task), as three kernels on `stream`:
  *   1. q / k head norms and RoPE (qkv_rows): for each of M = R * q_len rows
  *      of the drafter's projection (16 q heads, then k, then v, 128 bf16
  *      each), q and k get the step's Gemma head RMSNorm (gammas qn, kn) and
  *      partial NeoX RoPE at positions[m]; q becomes E4M3 into q8 row
  *      m * 16 + h, k and v become E4M3 at the row's slot of the drafter
  *      cache (slot_mapping[m] < 0: not stored).  All unit scale.
- *   2. split-KV attention and merge: request r's rows sit at p0 + j
+ *   2. split-KV attention (3. and its merge): request r's rows sit at p0 + j
  *      (p0 = positions[r * q_len], j < q_len) and see keys kp with
  *      lo <= kp <= hi and kp > p0 + j - window, where lo = max(p0 - window
  *      + 1, 0) and hi = min(seq_lens[r] - 1, (lo / 128 + max_blocks) * 128
@@ -417,37 +417,43 @@ typedef struct pa_drafter_args {
   int window;                  /* sliding window in keys (4096 on the page), >= 1 */
   int max_blocks;              /* blocks of a window at most (34 covers 4096 keys and 7 rows), >= 1 */
   int part_blocks;             /* blocks a partition: >= 1, or 0 for pre_attn_drafter_part_blocks' choice */
-  float sm_scale;              /* 1 / sqrt(128) on the page */
+  float sm_scale;              /* > 0, finite: 1 / sqrt(128) on the page */
   void *q8;                    /* [M * 16, 128] E4M3: written by kernel 1 (or given), read by kernel 2;
                                   16-byte aligned */
   void *out_bf16;              /* [M, 2048] bf16 or NULL, 16-byte aligned */
   void *out_codes;             /* [M, 2048] E4M3 MXFP8 codes, 16-byte aligned */
   void *out_scales;            /* [M, 64] E8M0 scale bytes (row-major: scale k covers columns 32k .. 32k + 31) */
-  void *workspace;             /* pre_attn_drafter_workspace_bytes(); zero it once before its first use: every
-                                  call leaves its counters at zero again. 256-byte aligned */
+  void *workspace;             /* pre_attn_drafter_workspace_bytes() of scratch (the partitions' partial
+                                  results), 256-byte aligned; no initial contents needed */
   size_t workspace_bytes;
   uint32_t *status;            /* device status word: PA_DEV_POS_RANGE, PA_DEV_SLOT_RANGE (a slot or block id
                                   outside the cache, or a window block past the block table: that key's store
                                   or that block skipped), PA_DEV_WAIT_TIMEOUT */
   uint32_t flags;              /* PA_FLAG_NO_PDL, PA_FLAG_TEST_WAIT_TIMEOUT */
+  void *prof_before;           /* optional cudaEvent_t recorded on the stream just before the attention
+                                  kernel (kernel 2), or NULL; profiling only: the record keeps kernel 2
+                                  from overlapping kernel 1 */
+  void *prof_after;            /* optional cudaEvent_t recorded just after kernel 2, or NULL */
 } pa_drafter_args;
 
 /* The partition length pre_attn_drafter_attention picks for part_blocks = 0:
- * about two partitions of every request resident on each of num_sms SMs
- * (the kernel runs two CTAs an SM), at least one block, at most max_blocks.
- * Pure host arithmetic; returns -PA_ERR_SHAPE for non-positive arguments. */
+ * max(1, floor(2 * num_sms / R)) partitions of a full window (the kernel runs
+ * two CTAs an SM, so every partition of every request fits one wave),
+ * max_blocks cut evenly between them: ceil(max_blocks / that).  Pure host
+ * arithmetic; returns -PA_ERR_SHAPE for non-positive arguments. */
 int pre_attn_drafter_part_blocks(int R, int max_blocks, int num_sms);
 
-/* Workspace bytes of a call with these sizes (part_blocks >= 1): a counter
- * per request and one partial (m, l, o) of 128 rows per partition.  Returns
- * 0 for non-positive arguments. */
+/* Workspace bytes of a call with these sizes (part_blocks >= 1): one
+ * partial (m, l, o) of 128 rows, f32, per partition of every request.
+ * Returns 0 for non-positive arguments. */
 size_t pre_attn_drafter_workspace_bytes(int R, int max_blocks, int part_blocks);
 
 /* Run the drafter's attention on `stream` (see above).  Allocates nothing,
- * never synchronises; kernel 2 waits for kernel 1 (and kernel 1 for the
- * previous kernel on the stream) through programmatic dependent launch.
+ * never synchronises; each kernel waits for the one before it (kernel 1
+ * for the previous kernel on the stream) through programmatic dependent
+ * launch.
  * Errors (nothing launched): PA_ERR_NULL, PA_ERR_SHAPE, PA_ERR_CONFIG
- * (window, max_blocks or part_blocks < 0 / 0, a NaN scale), PA_ERR_ALIGN,
+ * (window, max_blocks or part_blocks out of range, sm_scale not positive and finite), PA_ERR_ALIGN,
  * PA_ERR_WORKSPACE; PA_ERR_CUDA if a launch fails. */
 int pre_attn_drafter_attention(const pa_drafter_args *args, void *stream);
 

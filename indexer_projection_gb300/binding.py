@@ -80,7 +80,8 @@ class pa_drafter_args(ctypes.Structure):
                 ("seq_lens", _vp), ("R", ctypes.c_int), ("q_len", ctypes.c_int), ("window", ctypes.c_int),
                 ("max_blocks", ctypes.c_int), ("part_blocks", ctypes.c_int), ("sm_scale", ctypes.c_float),
                 ("q8", _vp), ("out_bf16", _vp), ("out_codes", _vp), ("out_scales", _vp), ("workspace", _vp),
-                ("workspace_bytes", ctypes.c_size_t), ("status", _vp), ("flags", ctypes.c_uint32)]
+                ("workspace_bytes", ctypes.c_size_t), ("status", _vp), ("flags", ctypes.c_uint32),
+                ("prof_before", _vp), ("prof_after", _vp)]
 
 
 class PreAttnError(RuntimeError):

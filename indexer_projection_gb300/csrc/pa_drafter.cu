@@ -1,6 +1,6 @@
 // The DSpark drafter's attention ("vllm.models.minimax_m3.amd.mono.drafter.
 // attention": module summary, qkv_rows, window, kv_load, block_math /
-// block_acc, store_partial, merge_task), as two kernels.
+// block_acc, store_partial, merge_task), as three kernels.
 //
 // pa_drafter_qkv_kernel (qkv_rows): a warp a (row, head) of the drafter's
 // projection rows: Gemma head RMSNorm and partial NeoX RoPE for the 16 q heads
@@ -19,20 +19,24 @@
 //               shared tile, B: the block's V bytes as loaded, i.e. MN-major:
 //               a key's 128 dims are contiguous)
 // with S and O in tensor memory (256 columns, two CTAs an SM).  Four softmax
-// warps own a row each per thread (TMEM lane = row): the block's masked row
-// maximum, alpha, P = exp2(s C - (m C - 8)) (P x 256 at the new maximum), l,
-// the E4M3 codes of P, and O's rescale by alpha in tensor memory between the
-// block's PV MMA and the previous one.  One thread issues the TMA copies (two
-// stages of K + V), one the MMAs; S of the next block is issued as soon as the
-// softmax threads have read S, so it overlaps their exponentials.
+// warps own a row each per thread (TMEM lane = row): they read the row's 128
+// scores in one round trip (S is then free, so the next block's QK^T runs
+// while they work), take the block's masked row maximum, alpha, P = exp2(s C
+// - (m C - 8)) (P x 256 at the new maximum), l, the E4M3 codes of P (written
+// straight into the P tile once the previous PV is done), and rescale O by
+// alpha in tensor memory before this block's PV.  One thread issues the TMA
+// copies (two stages of K + V), one the MMAs.
 // Keys outside [lo, hi] of a window-edge block hold whatever the cache held
 // (stale or never written bytes, possibly E4M3 NaN codes): their scores are
 // masked and their V rows zeroed in shared memory before the PV MMA, as the
 // page's kv_load zeroes them.
-// Each partition stores (m, l, o) of its rows (store_partial); the last CTA of
-// a request to finish (a counter per request) merges the partitions in order,
-// rounds to bf16 and quantises to MXFP8 (merge_task), a thread per (row, head,
-// 32-dim block), so each MXFP8 block is one thread's.
+// Each partition stores (m, l, o) of its rows (store_partial).
+//
+// pa_drafter_merge_kernel (merge_task): a CTA a query row, a thread a (head,
+// 16 dims): the request's partitions merged in order, rounded to bf16 and
+// quantised to MXFP8 (a 32-dim block is two neighbouring threads).  It waits
+// for the attention kernel through programmatic dependent launch, so the
+// whole merge runs spread over the GPU instead of on one CTA a request.
 //
 // Every wait is bounded (PA_DEV_WAIT_TIMEOUT); a block id outside the cache,
 // or a window block past the block table, is read as zeros, masked and
@@ -111,7 +115,6 @@ struct AttnParams {
   int64_t num_blocks;
   int R, q_len, bt_width, window, max_blocks, part_blocks, maxp;
   float C;  // sm_scale * log2(e)
-  uint32_t *counters;
   uint8_t *parts;
   __nv_bfloat16 *out_bf16;
   uint8_t *out_codes, *out_scales;
@@ -217,7 +220,6 @@ __global__ void __launch_bounds__(kDaThreads, 2)
   uint64_t *never = o_done + 1;    // testing: nothing arrives on it
   uint64_t *drain = never + 1;     // the MMA issuer's last commit on an abnormal exit
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
-  int *last_s = reinterpret_cast<int *>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int part = blockIdx.x, r = blockIdx.y;
@@ -244,19 +246,7 @@ __global__ void __launch_bounds__(kDaThreads, 2)
   if (use_pdl) pdl_wait();  // q8 and the new keys come from the previous kernel
   const Window win = request_window(a, r);
   const int na = (win.nblk + a.part_blocks - 1) / a.part_blocks;
-  if (win.nblk > 0 && part >= na) return;  // no partition here
-  if (win.nblk <= 0) {
-    // no key at all: partition 0 writes the request's zero rows
-    if (part != 0) return;
-    const int n = a.q_len * 2048;
-    uint8_t *codes = a.out_codes + (int64_t)r * n;
-    for (int i = tid; i < n / 16; i += kDaThreads) reinterpret_cast<uint4 *>(codes)[i] = make_uint4(0, 0, 0, 0);
-    for (int i = tid; i < a.q_len * 64; i += kDaThreads) a.out_scales[(int64_t)r * a.q_len * 64 + i] = 127;
-    if (a.out_bf16)
-      for (int i = tid; i < n / 8; i += kDaThreads)
-        reinterpret_cast<uint4 *>(a.out_bf16 + (int64_t)r * n)[i] = make_uint4(0, 0, 0, 0);
-    return;
-  }
+  if (part >= na) return;  // no partition here (no key at all: the merge writes zero rows)
   const int b0 = win.b_lo + part * a.part_blocks;
   const int nb = min(a.part_blocks, win.nblk - part * a.part_blocks);
 
@@ -298,6 +288,8 @@ __global__ void __launch_bounds__(kDaThreads, 2)
     }
   } else if (warp == 1) {
     // --------------------------------------------------------- MMA issuer
+    // S of the next block as soon as the softmax threads have read this one
+    // (it runs while they work), then this block's PV once its P is written
     if (lane == 0) {
       bool ok = mbar_wait(q_full, 0, a.status, lim) && mbar_wait(&kv_full[0], 0, a.status, lim);
       const uint64_t qd = sdesc_sw128(smem_u32(smem + kSmQ));
@@ -311,7 +303,7 @@ __global__ void __launch_bounds__(kDaThreads, 2)
       }
       for (int t = 0; t < nb && ok; ++t) {
         const int s = t % kDaStages;
-        if (t + 1 < nb) {  // S of the next block once the softmax threads have read this one
+        if (t + 1 < nb) {
           const int s1 = (t + 1) % kDaStages;
           if (!mbar_wait(&kv_full[s1], (uint32_t)((t + 1) / kDaStages) & 1, a.status, lim) ||
               !mbar_wait(s_free, (uint32_t)t & 1, a.status, lim)) {
@@ -360,7 +352,9 @@ __global__ void __launch_bounds__(kDaThreads, 2)
       const int64_t kb = (int64_t)(b0 + t) * 128;
       const bool bad = phys_block(a, r, b0 + t) < 0;
       int kmin = 128, kmax = -1;  // valid keys kb + kmin .. kb + kmax of this row
-      if (live && !bad) {
+      if (!live) {
+        kmin = 0, kmax = 127;  // padding rows: computed, never used
+      } else if (!bad) {
         const int64_t x = klo - kb, y = win.hi - kb;
         kmin = x < 0 ? 0 : x > 128 ? 128 : (int)x;
         kmax = y > 127 ? 127 : y < -1 ? -1 : (int)y;
@@ -371,55 +365,29 @@ __global__ void __launch_bounds__(kDaThreads, 2)
         break;
       }
       tc_fence_after();
-      // pass 1: the block's row maximum over the valid keys
-      float mb = -INFINITY;
+      // the row's 128 scores in one round trip; S is then free for the next
+      // block's QK^T, which runs while this block's exponentials do
+      float x[128];
+      tc_ld64(trow, *reinterpret_cast<float(*)[64]>(&x[0]));
+      tc_ld64(trow + 64, *reinterpret_cast<float(*)[64]>(&x[64]));
+      tc_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free);
+      // window-edge blocks (some row of the warp has keys outside its range):
+      // those scores become -inf (P = 2^-inf = 0); the branch is warp-uniform
+      if (__any_sync(0xffffffffu, !full)) {
 #pragma unroll
-      for (int c = 0; c < 4; c += 2) {
-        float x0[32], x1[32];
-        tc_ld32(trow + 32 * c, x0);
-        tc_ld32(trow + 32 * (c + 1), x1);
-        tc_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int k0 = 32 * c + e, k1 = k0 + 32;
-          mb = fmaxf(mb, (full || (k0 >= kmin && k0 <= kmax)) ? x0[e] : -INFINITY);
-          mb = fmaxf(mb, (full || (k1 >= kmin && k1 <= kmax)) ? x1[e] : -INFINITY);
-        }
+        for (int k = 0; k < 128; ++k) x[k] = ((k >= kmin) & (k <= kmax)) ? x[k] : -INFINITY;
       }
+      float m4[4] = {x[0], x[1], x[2], x[3]};
+#pragma unroll
+      for (int k = 4; k < 128; ++k) m4[k & 3] = fmaxf(m4[k & 3], x[k]);
+      const float mb = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       const float mn = fmaxf(m_run, mb);
       const float ms = mn == -INFINITY ? 0.f : mn;
       const float alpha = live ? ex2((m_run - ms) * C) : 1.0f;  // padding rows: no rescale
       const float off = ms * C - 8.0f;
-      // pass 2: P (x 256 at the new maximum), its sum and its E4M3 codes
-      uint32_t pw[32];
-      float psum = 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; c += 2) {
-        float x0[32], x1[32];
-        tc_ld32(trow + 32 * c, x0);
-        tc_ld32(trow + 32 * (c + 1), x1);
-        tc_wait_ld();
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const float *x = h ? x1 : x0;
-#pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            float p[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int k = 32 * (c + h) + e + u;
-              p[u] = (full || (k >= kmin && k <= kmax)) ? ex2(fmaf(x[e + u], C, -off)) : 0.f;
-              psum += p[u];
-            }
-            pw[(32 * (c + h) + e) >> 2] = e4m3x4(p[0], p[1], p[2], p[3]);
-          }
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_free);
-      l_run = fmaf(l_run, alpha, psum);
-      m_run = mn;
       // the previous block's PV is done: P's tile and O are free
       if (t > 0) {
         if (!mbar_wait(o_done, (uint32_t)(t - 1) & 1, a.status, lim)) {
@@ -427,18 +395,39 @@ __global__ void __launch_bounds__(kDaThreads, 2)
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            float o[32];
-            tc_ld32(trow + kDaOCol + 32 * c, o);
-            tc_wait_ld();
+      }
+      // P (x 256 at the new maximum), its sum, and its E4M3 codes straight
+      // into the swizzled P tile, 16 keys a 16-byte chunk
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
+      uint8_t *prow = smem + kSmP + row * 128;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] *= alpha;
-            tc_st32(trow + kDaOCol + 32 * c, o);
+      for (int c = 0; c < 8; ++c) {
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float pq[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            pq[u] = ex2(fmaf(x[16 * c + 4 * q + u], C, -off));
+            s4[u] += pq[u];
           }
-          tc_wait_st();
+          w[q] = e4m3x4(pq[0], pq[1], pq[2], pq[3]);
         }
+        if (live) *reinterpret_cast<uint4 *>(prow + ((c ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      l_run = fmaf(l_run, alpha, (s4[0] + s4[1]) + (s4[2] + s4[3]));
+      m_run = mn;
+      // O rescaled by alpha before this block's PV accumulates into it
+      if (t > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {  // one round trip
+        float o[128];
+        tc_ld64(trow + kDaOCol, *reinterpret_cast<float(*)[64]>(&o[0]));
+        tc_ld64(trow + kDaOCol + 64, *reinterpret_cast<float(*)[64]>(&o[64]));
+        tc_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 128; ++e) o[e] *= alpha;
+        tc_st64(trow + kDaOCol, *reinterpret_cast<const float(*)[64]>(&o[0]));
+        tc_st64(trow + kDaOCol + 64, *reinterpret_cast<const float(*)[64]>(&o[64]));
+        tc_wait_st();
       }
       // keys of the block outside [lo, hi]: their V rows to zero
       const int64_t key = kb + row;
@@ -451,13 +440,6 @@ __global__ void __launch_bounds__(kDaThreads, 2)
 #pragma unroll
         for (int c = 0; c < 8; ++c) vrow[c] = make_uint4(0, 0, 0, 0);
       }
-      if (live) {
-        uint8_t *prow = smem + kSmP + row * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4 *>(prow + ((c ^ (row & 7)) << 4)) =
-              make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
-      }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -468,14 +450,14 @@ __global__ void __launch_bounds__(kDaThreads, 2)
     tc_fence_after();
     uint8_t *pp = a.parts + ((int64_t)r * a.maxp + part) * kDaPartBytes;
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-      float o[32];
-      tc_ld32(trow + kDaOCol + 32 * c, o);
+    for (int hf = 0; hf < 2; ++hf) {
+      float o[64];
+      tc_ld64(trow + kDaOCol + 64 * hf, o);
       tc_wait_ld();
       if (live) {
-        float4 *dst = reinterpret_cast<float4 *>(pp + 1024 + row * 512 + c * 128);
+        float4 *dst = reinterpret_cast<float4 *>(pp + 1024 + row * 512 + hf * 256);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+        for (int q = 0; q < 16; ++q) dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
       }
     }
     if (live) {
@@ -490,75 +472,97 @@ __global__ void __launch_bounds__(kDaThreads, 2)
     tc_fence_after();
     tc_dealloc(tmem, kDaTmemCols);
   }
-  // -------------------------------------------- the last partition merges
-  if (tid == 0) {
-    __threadfence();
-    const uint32_t old = atomicAdd(a.counters + r, 1u);
-    const int last = old + 1 == (uint32_t)na;
-    if (last) {
-      a.counters[r] = 0;  // ready for the next call
-      __threadfence();
-    }
-    *last_s = last;
-  }
-  __syncthreads();
-  if (!*last_s) return;
+}
+
+// ------------------------------------------------------------ kernel 3
+// The merge (merge_task): a CTA a query row m = r * q_len + j, a thread a
+// (head h, 16 dims); the request's partitions are merged in order:
+//   m* = max m_i, w_i = 2^((m_i - m*) C) (0 for a partition without a valid
+//   key of the row), out = sum w_i o_i / sum w_i l_i (0 if that sum is 0),
+// rounded to bf16, then MXFP8: each 32-dim block (two neighbouring threads)
+// takes the smallest E8M0 scale 2^e with 448 * 2^e >= its amax, codes
+// E4M3(x * 2^-e).  A request without keys gets zero rows.
+constexpr int kDaMergeThreads = 128;
+constexpr int kDaMergeBatch = 4;  // partitions whose loads are in flight together
+
+__global__ void __launch_bounds__(kDaMergeThreads) pa_drafter_merge_kernel(AttnParams a, int use_pdl) {
+  const int tid = threadIdx.x;
+  const int m_row = blockIdx.x;
+  const int r = m_row / a.q_len, j = m_row - r * a.q_len;
+  const int h = tid >> 3, piece = tid & 7;
+  const int row = kDaHeads * j + h;  // the partials' row
+  if (use_pdl) pdl_wait();           // the partials come from the attention kernel
+  const Window win = request_window(a, r);
+  const int na = win.nblk > 0 ? (win.nblk + a.part_blocks - 1) / a.part_blocks : 0;
   const uint8_t *pr = a.parts + (int64_t)r * a.maxp * kDaPartBytes;
-  const int rows = kDaHeads * a.q_len;
-  for (int task = tid; task < rows * 4; task += kDaThreads) {
-    const int row = task >> 2, c = task & 3;
-    float mst = -INFINITY;
-    for (int i = 0; i < na; ++i) mst = fmaxf(mst, __ldcg(reinterpret_cast<const float *>(pr + i * kDaPartBytes) + row));
-    float L = 0.f, acc[32];
+  float mst = -INFINITY;
+  for (int i0 = 0; i0 < na; i0 += 8) {
+    float mi[8];
 #pragma unroll
-    for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-#pragma unroll 2
-    for (int i = 0; i < na; ++i) {
-      const uint8_t *pi = pr + i * kDaPartBytes;
-      const float mi = __ldcg(reinterpret_cast<const float *>(pi) + row);
-      if (mi == -INFINITY) continue;  // no valid key in this partition
-      const float w = ex2((mi - mst) * a.C);
-      L = fmaf(w, __ldcg(reinterpret_cast<const float *>(pi + 512) + row), L);
-      const float4 *o = reinterpret_cast<const float4 *>(pi + 1024 + row * 512 + c * 128);
+    for (int u = 0; u < 8; ++u)
+      mi[u] = i0 + u < na ? __ldcg(reinterpret_cast<const float *>(pr + (int64_t)(i0 + u) * kDaPartBytes) + row)
+                          : -INFINITY;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float4 x = __ldcg(o + q);
-        acc[4 * q] = fmaf(w, x.x, acc[4 * q]);
-        acc[4 * q + 1] = fmaf(w, x.y, acc[4 * q + 1]);
-        acc[4 * q + 2] = fmaf(w, x.z, acc[4 * q + 2]);
-        acc[4 * q + 3] = fmaf(w, x.w, acc[4 * q + 3]);
+    for (int u = 0; u < 8; ++u) mst = fmaxf(mst, mi[u]);
+  }
+  float L = 0.f, acc[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+  for (int i0 = 0; i0 < na; i0 += kDaMergeBatch) {
+    float mi[kDaMergeBatch], li[kDaMergeBatch];
+    float4 oi[kDaMergeBatch][4];
+#pragma unroll
+    for (int u = 0; u < kDaMergeBatch; ++u) {
+      const bool in = i0 + u < na;
+      const uint8_t *pi = pr + (int64_t)(in ? i0 + u : 0) * kDaPartBytes;
+      mi[u] = in ? __ldcg(reinterpret_cast<const float *>(pi) + row) : -INFINITY;
+      li[u] = in ? __ldcg(reinterpret_cast<const float *>(pi + 512) + row) : 0.f;
+      const float4 *o = reinterpret_cast<const float4 *>(pi + 1024 + row * 512 + piece * 64);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) oi[u][q] = in ? __ldcg(o + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kDaMergeBatch; ++u) {  // in partition order
+      if (mi[u] == -INFINITY) continue;          // no valid key of this row there
+      const float w = ex2((mi[u] - mst) * a.C);
+      L = fmaf(w, li[u], L);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[4 * q] = fmaf(w, oi[u][q].x, acc[4 * q]);
+        acc[4 * q + 1] = fmaf(w, oi[u][q].y, acc[4 * q + 1]);
+        acc[4 * q + 2] = fmaf(w, oi[u][q].z, acc[4 * q + 2]);
+        acc[4 * q + 3] = fmaf(w, oi[u][q].w, acc[4 * q + 3]);
       }
     }
-    // out = o / l, bf16, then the 32-value MXFP8 block
-    float amax = 0.f;
-    uint32_t bw[16];
-#pragma unroll
-    for (int e = 0; e < 32; e += 2) {
-      const float x0 = L > 0.f ? acc[e] / L : 0.f, x1 = L > 0.f ? acc[e + 1] / L : 0.f;
-      const uint16_t h0 = f32_to_bf16_bits(x0), h1 = f32_to_bf16_bits(x1);
-      acc[e] = bf16_to_f32(h0);
-      acc[e + 1] = bf16_to_f32(h1);
-      amax = fmaxf(amax, fmaxf(fabsf(acc[e]), fabsf(acc[e + 1])));
-      bw[e >> 1] = (uint32_t)h0 | ((uint32_t)h1 << 16);
-    }
-    const int e = mx_exponent(amax);
-    const float inv = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e (e <= 126 for a bf16 amax)
-    uint32_t cw[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-      cw[q] = e4m3x4(acc[4 * q] * inv, acc[4 * q + 1] * inv, acc[4 * q + 2] * inv, acc[4 * q + 3] * inv);
-    const int64_t m_row = (int64_t)r * a.q_len + (row >> 4);
-    const int col = (row & 15) * kHeadDim + 32 * c;
-    uint4 *cd = reinterpret_cast<uint4 *>(a.out_codes + m_row * 2048 + col);
-    cd[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-    cd[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-    a.out_scales[m_row * 64 + (col >> 5)] = (uint8_t)(e + 127);
-    if (a.out_bf16) {
-      uint4 *bd = reinterpret_cast<uint4 *>(a.out_bf16 + m_row * 2048 + col);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) bd[q] = make_uint4(bw[4 * q], bw[4 * q + 1], bw[4 * q + 2], bw[4 * q + 3]);
-    }
   }
+  // out = o / l in bf16, then the MXFP8 block of this thread and its neighbour
+  float amax = 0.f;
+  uint32_t bw[8];
+#pragma unroll
+  for (int e = 0; e < 16; e += 2) {
+    const float x0 = L > 0.f ? acc[e] / L : 0.f, x1 = L > 0.f ? acc[e + 1] / L : 0.f;
+    const uint16_t h0 = f32_to_bf16_bits(x0), h1 = f32_to_bf16_bits(x1);
+    acc[e] = bf16_to_f32(h0);
+    acc[e + 1] = bf16_to_f32(h1);
+    amax = fmaxf(amax, fmaxf(fabsf(acc[e]), fabsf(acc[e + 1])));
+    bw[e >> 1] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+  }
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  const int e = mx_exponent(amax);
+  const float inv = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e (e <= 126 for a bf16 amax)
+  uint32_t cw[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    cw[q] = e4m3x4(acc[4 * q] * inv, acc[4 * q + 1] * inv, acc[4 * q + 2] * inv, acc[4 * q + 3] * inv);
+  const int col = h * kHeadDim + 16 * piece;
+  *reinterpret_cast<uint4 *>(a.out_codes + (int64_t)m_row * 2048 + col) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+  if ((piece & 1) == 0) a.out_scales[(int64_t)m_row * 64 + (col >> 5)] = (uint8_t)(e + 127);
+  if (a.out_bf16) {
+    uint4 *bd = reinterpret_cast<uint4 *>(a.out_bf16 + (int64_t)m_row * 2048 + col);
+    bd[0] = make_uint4(bw[0], bw[1], bw[2], bw[3]);
+    bd[1] = make_uint4(bw[4], bw[5], bw[6], bw[7]);
+  }
+  if (use_pdl) pdl_trigger();
 }
 
 int device_sms() {
@@ -573,23 +577,24 @@ int device_sms() {
   return sms[dev];
 }
 
-int64_t counter_bytes(int R) { return ((int64_t)R * 4 + 255) / 256 * 256; }
 
 }  // namespace
 }  // namespace pa
 
 extern "C" int pre_attn_drafter_part_blocks(int R, int max_blocks, int num_sms) {
   if (R < 1 || max_blocks < 1 || num_sms < 1) return -PA_ERR_SHAPE;
-  int per = 2 * num_sms / R;  // partitions of a request that keep one wave of two CTAs an SM
+  // as many partitions a request as keep every partition of every request
+  // in one wave of two CTAs an SM, cut evenly
+  int per = 2 * num_sms / R;
   if (per < 1) per = 1;
-  int pb = (max_blocks + per - 1) / per;
+  const int pb = (max_blocks + per - 1) / per;
   return pb < 1 ? 1 : pb > max_blocks ? max_blocks : pb;
 }
 
 extern "C" size_t pre_attn_drafter_workspace_bytes(int R, int max_blocks, int part_blocks) {
   if (R < 1 || max_blocks < 1 || part_blocks < 1) return 0;
   const int64_t maxp = (max_blocks + part_blocks - 1) / part_blocks;
-  return (size_t)(pa::counter_bytes(R) + (int64_t)R * maxp * pa::kDaPartBytes);
+  return (size_t)((int64_t)R * maxp * pa::kDaPartBytes);
 }
 
 extern "C" int pre_attn_drafter_attention(const pa_drafter_args *in, void *stream) {
@@ -605,7 +610,7 @@ extern "C" int pre_attn_drafter_attention(const pa_drafter_args *in, void *strea
     return PA_ERR_SHAPE;
   if (x.qkv && (x.qkv_stride < (kDaHeads + 2) * kHeadDim || x.qkv_stride % 8 || x.max_pos < 1)) return PA_ERR_SHAPE;
   if (x.window < 1 || x.max_blocks < 1 || x.max_blocks > 65535 || x.part_blocks < 0 ||
-      !(x.sm_scale == x.sm_scale) || (x.qkv && !(x.eps >= 0.f)))
+      !(x.sm_scale > 0.f && x.sm_scale < INFINITY) || (x.qkv && !(x.eps >= 0.f)))
     return PA_ERR_CONFIG;
   const uintptr_t a16 = 15;
   auto mis = [](const void *p, uintptr_t m) { return (reinterpret_cast<uintptr_t>(p) & m) != 0; };
@@ -674,8 +679,7 @@ extern "C" int pre_attn_drafter_attention(const pa_drafter_args *in, void *strea
   p.part_blocks = pb;
   p.maxp = (x.max_blocks + pb - 1) / pb;
   p.C = (float)((double)x.sm_scale * 1.4426950408889634);  // log2(e)
-  p.counters = static_cast<uint32_t *>(x.workspace);
-  p.parts = static_cast<uint8_t *>(x.workspace) + counter_bytes(x.R);
+  p.parts = static_cast<uint8_t *>(x.workspace);
   p.out_bf16 = static_cast<__nv_bfloat16 *>(x.out_bf16);
   p.out_codes = static_cast<uint8_t *>(x.out_codes);
   p.out_scales = static_cast<uint8_t *>(x.out_scales);
@@ -690,6 +694,18 @@ extern "C" int pre_attn_drafter_attention(const pa_drafter_args *in, void *strea
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
+  if (x.prof_before && (e = cudaEventRecord(static_cast<cudaEvent_t>(x.prof_before), s)) != cudaSuccess)
+    return record_cuda_error(e);
   e = cudaLaunchKernelEx(&cfg, pa_drafter_attn_kernel, tmQ, tmKV, p, pdl ? 1 : 0);
+  if (e != cudaSuccess) return record_cuda_error(e);
+  if (x.prof_after && (e = cudaEventRecord(static_cast<cudaEvent_t>(x.prof_after), s)) != cudaSuccess)
+    return record_cuda_error(e);
+  cudaLaunchConfig_t mcfg = {};
+  mcfg.gridDim = dim3((unsigned)M);
+  mcfg.blockDim = dim3(kDaMergeThreads);
+  mcfg.stream = s;
+  mcfg.attrs = attr;
+  mcfg.numAttrs = pdl ? 1 : 0;
+  e = cudaLaunchKernelEx(&mcfg, pa_drafter_merge_kernel, p, pdl ? 1 : 0);
   return e == cudaSuccess ? PA_OK : record_cuda_error(e);
 }

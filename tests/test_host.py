@@ -214,16 +214,16 @@ def test_harness_masks_match_oracle_offsets():
 
 
 def test_drafter_partition_choice_and_workspace(B):
-    # about two resident partitions of every request an SM, at least one block
-    assert B.pre_attn_drafter_part_blocks(64, 34, 152) == 9   # 304 / 64 -> 4 partitions of <= 9 blocks
+    # floor(2 * SMs / R) partitions of a full window (one wave), cut evenly
+    assert B.pre_attn_drafter_part_blocks(64, 34, 152) == 9   # 304 // 64 = 4 partitions of <= 9 blocks
     assert B.pre_attn_drafter_part_blocks(1, 34, 152) == 1
     assert B.pre_attn_drafter_part_blocks(1000, 34, 152) == 34
     assert B.pre_attn_drafter_part_blocks(152, 34, 152) == 17
+    assert B.pre_attn_drafter_part_blocks(100, 34, 152) == 12  # 304 // 100 = 3 partitions of <= 12 blocks
     assert B.pre_attn_drafter_part_blocks(0, 34, 152) < 0
-    # a counter per request (256-byte rounded), then ceil(34 / 9) = 4 partials of
-    # 128 m + 128 l + 128 x 128 o f32 per request
-    assert B.pre_attn_drafter_workspace_bytes(64, 34, 9) == 256 + 64 * 4 * (1024 + 65536)
-    assert B.pre_attn_drafter_workspace_bytes(65, 34, 34) == 512 + 65 * (1024 + 65536)
+    # ceil(34 / 9) = 4 partials of 128 m + 128 l + 128 x 128 o f32 per request
+    assert B.pre_attn_drafter_workspace_bytes(64, 34, 9) == 64 * 4 * (1024 + 65536)
+    assert B.pre_attn_drafter_workspace_bytes(65, 34, 34) == 65 * (1024 + 65536)
     assert B.pre_attn_drafter_workspace_bytes(0, 34, 9) == 0
 
 
@@ -256,7 +256,8 @@ def test_drafter_validation_codes(B):
     q = dict(qkv=base, qn=base, kn=base, cos_sin=base, slot_mapping=base, max_pos=64)
     assert run(**q, qkv_stride=18 * 128 - 8) == B.PA_ERR_SHAPE
     assert run(**q, qkv_stride=18 * 128 + 4) == B.PA_ERR_SHAPE
-    for bad in (dict(window=0), dict(max_blocks=0), dict(part_blocks=-1), dict(sm_scale=float("nan"))):
+    for bad in (dict(window=0), dict(max_blocks=0), dict(part_blocks=-1), dict(sm_scale=float("nan")),
+                dict(sm_scale=-0.1), dict(sm_scale=0.0), dict(sm_scale=float("inf"))):
         assert run(**bad) == B.PA_ERR_CONFIG, bad
     assert run(**q, qkv_stride=18 * 128, eps=-1.0) == B.PA_ERR_CONFIG
     for k, off in (("cache", 8), ("q8", 4), ("out_codes", 8), ("workspace", 128), ("status", 2), ("positions", 4)):

@@ -212,14 +212,13 @@ def test_spec_decode_configuration_every_row():
     full_check(dw, 0)
 
 
-def test_repeated_calls_are_identical_and_leave_counters_zero():
+def test_repeated_calls_are_identical():
     dw = workloads.DrafterWorkload("drep", R=5, q_len=7, seq_lo=2000, seq_hi=9000, seed=61, prefilled=True)
     st = workloads.drafter_host_state(dw)
     g1 = gpu_run(dw, st, 2, with_qkv=False)
     g3 = gpu_run(dw, st, 2, with_qkv=False, reps=3)
     for k in ("out", "codes", "scales"):
         assert np.array_equal(g1[k], g3[k]), k
-    assert not g3["ws"][: 4 * dw.R].cpu().numpy().any()  # the per-request counters
 
 
 def test_empty_window_rows_are_zero():
