@@ -565,19 +565,6 @@ __global__ void __launch_bounds__(kDaMergeThreads) pa_drafter_merge_kernel(AttnP
   if (use_pdl) pdl_trigger();
 }
 
-int device_sms() {
-  static int sms[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
-  if (sms[dev] <= 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
-    sms[dev] = n;
-  }
-  return sms[dev];
-}
-
-
 }  // namespace
 }  // namespace pa
 
@@ -623,7 +610,7 @@ extern "C" int pre_attn_drafter_attention(const pa_drafter_args *in, void *strea
   if (x.R == 0) return PA_OK;
   int pb = x.part_blocks;
   if (pb == 0) {
-    const int sms = device_sms();
+    const int sms = current_device_sms();
     if (sms < 1) return record_cuda_error(cudaGetLastError());
     pb = pre_attn_drafter_part_blocks(x.R, x.max_blocks, sms);
   }

@@ -11,11 +11,14 @@
 //   or -inf (j > p); columns from nb * 128 on are not written.
 //
 // The work is a skinny contraction (128 keys x 128 dims by up to 16 query
-// rows per block) over a key stream that HBM bounds.  A CTA takes up to four
-// blocks of one request (strided, for balance across the request's blocks),
-// loads each block's 16 KB of keys with one TMA copy (128-byte swizzle, so
-// the fragment loads below hit distinct banks), and its 8 warps take 16 keys
-// each: ldmatrix reads a warp's 16 keys x 32 dims of E4M3 as four 8 x 8
+// rows per block) over a key stream that HBM bounds.  Up to 512 requests, a
+// persistent grid (three CTAs an SM) walks the list of (request, block)
+// items in even contiguous slices, a producer warp keeping four key blocks
+// in flight a CTA (pa_index_scores_persist_kernel); beyond that, a CTA takes
+// up to four blocks of one request (strided, for balance across the
+// request's blocks; pa_index_scores_kernel).  Each block's 16 KB of keys
+// arrives by one TMA copy (128-byte swizzle, so the fragment loads below hit
+// distinct banks), and 8 warps take 16 keys each: ldmatrix reads a warp's 16 keys x 32 dims of E4M3 as four 8 x 8
 // b16 tiles (2 E4M3 per b16), each thread converts its 4-code pieces to
 // bf16 (exact: every E4M3 value is a bf16 value) and feeds
 // mma.sync m16n8k16 bf16 with the query rows as B.  A thread's 4 codes of a
@@ -224,23 +227,256 @@ __global__ void __launch_bounds__(kIdxThreads) pa_index_scores_kernel(const __gr
   }
 }
 
+// ------------------------------------------------------ persistent variant
+// Up to kIxPersistMaxR requests: a grid of three CTAs an SM walks the global
+// list of (request, block) items, request by request, each CTA an even
+// contiguous slice of it, so the key stream does not stop at CTA
+// boundaries.  A producer warp keeps kIxStages key blocks in flight through
+// a TMA ring; the eight compute warps score each block as the kernel above
+// (the same fragments, the same masks and stores) and reload the query
+// fragments only when the request changes.  Every CTA derives the item list
+// itself: each request's block count from seq_lens, then a prefix sum.
+constexpr int kIxStages = 4;
+constexpr int kIxComputeWarps = 8;
+constexpr int kIxPersistThreads = 32 * (kIxComputeWarps + 1);
+constexpr int kIxPersistMaxR = 512;
+constexpr int kIxPersistSmem = kIxStages * kKeyBlockBytes + 1024;  // + alignment slack
+
+// Blocks of request r's score rows; 0 for a request without rows, and 0 with
+// *bad set for one shorter than q_len or longer than its block table.
+__device__ __forceinline__ int request_blocks(const IndexParams &a, int r, bool *bad) {
+  const int seq = __ldg(a.seq_lens + r);
+  if (seq < 1) return 0;
+  const int nb = (seq - 1) / 128 + 1;
+  if (seq < a.q_len || nb > a.bt_width) {
+    *bad = true;
+    return 0;
+  }
+  return nb;
+}
+// Whether some row of request r (rows at positions p_first .. p_first + q_len - 1) scores block b.
+__device__ __forceinline__ bool block_needed(const IndexParams &a, int64_t p_first, int b) {
+  for (int i = 0; i < a.q_len; ++i)
+    if (row_scores_block(p_first + i, b, a.init_blocks, a.local_blocks)) return true;
+  return false;
+}
+// Block id of (r, b) if it holds keys inside the cache, else -1.
+__device__ __forceinline__ int64_t key_block(const IndexParams &a, int r, int b) {
+  const int64_t blk = __ldg(a.block_table + (int64_t)r * a.bt_width + b);
+  return (blk < 0 || (blk + 1) * 128 > a.num_index_slots) ? -1 : blk;
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kIxPersistThreads) pa_index_scores_persist_kernel(
+    const __grid_constant__ CUtensorMap tmK, IndexParams a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  __shared__ __align__(8) uint64_t full[kIxStages], empty[kIxStages];
+  __shared__ int offs[kIxPersistMaxR + 1];  // items before request r
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  pdl_wait();  // the index_q rows (and new keys) come from the previous kernel
+  // each request's block count, then the prefix sum (warp 0: 16 requests a lane)
+  if (warp == 0) {
+    constexpr int kPer = (kIxPersistMaxR + 31) / 32;
+    int cnt[kPer], sum = 0;
+    bool bad = false;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int r = lane * kPer + k;
+      cnt[k] = r < a.R ? request_blocks(a, r, &bad) : 0;
+      sum += cnt[k];
+    }
+    if (blockIdx.x == 0 && __any_sync(0xffffffffu, bad) && lane == 0) set_status(a.status, kDevSlotRange);
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int r = lane * kPer + k;
+      if (r <= a.R) offs[r] = run;
+      run += cnt[k];
+    }
+    if (lane == 31 && 32 * kPer == a.R) offs[a.R] = incl;
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kIxStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kIxComputeWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int64_t total = offs[a.R];
+  const int64_t lo = total * blockIdx.x / gridDim.x, hi = total * (blockIdx.x + 1) / gridDim.x;
+  if (lo >= hi) return;
+  int r0 = 0;  // the request of item lo: the last r with offs[r] <= lo
+  for (int step = kIxPersistMaxR; step > 0; step >>= 1)
+    if (r0 + step < a.R && offs[r0 + step] <= lo) r0 += step;
+  // Items are resolved 32 at a time, one a lane (its request, block, whether
+  // its keys are loaded and from which block), so the block-table reads of a
+  // batch overlap instead of preceding each copy.
+  struct Item {
+    int r, b;
+    int64_t blk;  // >= 0: its keys are loaded from this block
+  };
+  auto resolve = [&](int64_t idx, int r_from) {
+    Item it{r_from, 0, -1};
+    if (idx >= hi) return it;
+    while (offs[it.r + 1] <= idx) ++it.r;
+    it.b = (int)(idx - offs[it.r]);
+    const int64_t pf = (int64_t)__ldg(a.seq_lens + it.r) - a.q_len;
+    if (block_needed(a, pf, it.b)) {
+      it.blk = key_block(a, it.r, it.b);
+      if (it.blk < 0) it.blk = -2;  // needed but outside the cache: flagged, not loaded
+    }
+    return it;
+  };
+  if (warp == kIxComputeWarps) {
+    // ------------------------------------------------------------ producer
+    int j = 0, r = r0;
+    bool ok = true;
+    for (int64_t base = lo; base < hi && ok; base += 32) {
+      const Item mine = resolve(base + lane, r);
+      r = __shfl_sync(0xffffffffu, mine.r, 31);  // items are in request order
+      for (int k = 0; k < 32 && base + k < hi; ++k) {
+        const int64_t blk = __shfl_sync(0xffffffffu, mine.blk, k);
+        if (blk == -2 && lane == 0) set_status(a.status, kDevSlotRange);
+        if (blk < 0) continue;
+        const int s = j % kIxStages;
+        if (lane == 0) {
+          if (!mbar_wait(&empty[s], ((uint32_t)(j / kIxStages) & 1) ^ 1, a.status)) ok = false;
+          else {
+            mbar_expect_tx(&full[s], kKeyBlockBytes);
+            tma_rows(smem_u32(smem + s * kKeyBlockBytes), &tmK, 0, (int)(blk * 128), &full[s]);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        ++j;
+      }
+    }
+    // the copies issued land before the CTA exits (they have, unless a wait ran out)
+    if (lane == 0)
+      for (int k = j - 1; k >= 0 && k >= j - kIxStages; --k)
+        mbar_wait(&full[k % kIxStages], (uint32_t)(k / kIxStages) & 1, a.status);
+    return;
+  }
+  // ------------------------------------------------------------ compute
+  int j = 0, cur = -1, r = r0;
+  uint2 qf[NT][8];
+  int64_t prow[NT][2];
+  for (int64_t base = lo; base < hi; base += 32) {
+    const Item mine = resolve(base + lane, r);
+    r = __shfl_sync(0xffffffffu, mine.r, 31);
+    bool stop = false;
+    for (int k = 0; k < 32 && base + k < hi; ++k) {
+      const int ri = __shfl_sync(0xffffffffu, mine.r, k);
+      const int b = __shfl_sync(0xffffffffu, mine.b, k);
+      const bool loaded = __shfl_sync(0xffffffffu, mine.blk, k) >= 0;
+      if (ri != cur) {  // the request's query fragments and row positions
+        cur = ri;
+        const int64_t p_first = (int64_t)__ldg(a.seq_lens + ri) - a.q_len;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int i = 8 * nt + g;
+          const __nv_bfloat16 *row = a.iq + ((int64_t)ri * a.q_len + i) * a.iq_stride + a.head * kHeadDim;
+#pragma unroll
+          for (int pc = 0; pc < 8; ++pc)
+            qf[nt][pc] = i < a.q_len ? *reinterpret_cast<const uint2 *>(row + 16 * pc + 4 * t) : make_uint2(0u, 0u);
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int ii = 8 * nt + 2 * t + e;
+            prow[nt][e] = ii < a.q_len ? p_first + ii : -1;
+          }
+        }
+      }
+      float c[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) c[nt][e] = 0.f;
+      if (loaded) {
+        const int s = j % kIxStages;
+        const bool got = mbar_wait(&full[s], (uint32_t)(j / kIxStages) & 1, a.status);
+        if (__any_sync(0xffffffffu, !got)) {  // the warp gives up together
+          stop = true;
+          break;
+        }
+        const uint32_t sbase = smem_u32(smem + s * kKeyBlockBytes);
+        const int key = 16 * warp + 8 * ((lane >> 3) & 1) + (lane & 7);
+        const uint32_t rowaddr = sbase + key * 128;
+#pragma unroll
+        for (int L = 0; L < 4; ++L) {
+          uint32_t m[4];
+          const int chunk = 2 * L + (lane >> 4);
+          ldmatrix_x4(rowaddr + ((chunk ^ (key & 7)) << 4), m);
+          const uint2 k0 = e4m3x4_to_bf16x4(m[0]), k1 = e4m3x4_to_bf16x4(m[1]);
+          const uint2 k2 = e4m3x4_to_bf16x4(m[2]), k3 = e4m3x4_to_bf16x4(m[3]);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            mma_bf16_16816(c[nt], k0.x, k1.x, k0.y, k1.y, qf[nt][2 * L].x, qf[nt][2 * L].y);
+            mma_bf16_16816(c[nt], k2.x, k3.x, k2.y, k3.y, qf[nt][2 * L + 1].x, qf[nt][2 * L + 1].y);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        ++j;
+      }
+      // scores of keys 128 b + 16 warp + g and + 8 for this thread's rows
+      const int64_t j0 = (int64_t)b * 128 + 16 * warp + g;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int64_t p = prow[nt][e];
+          if (!row_has_block(p, b)) continue;
+          const bool scored = row_scores_block(p, b, a.init_blocks, a.local_blocks);
+          if (scored && !loaded) continue;  // a key block outside the cache: left unwritten
+          float *out = a.scores + ((int64_t)ri * a.q_len + 8 * nt + 2 * t + e) * a.score_stride;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int64_t jj = j0 + 8 * h;
+            out[jj] = (scored && jj <= p) ? c[nt][2 * h + e] * a.index_scale : -INFINITY;
+          }
+        }
+    }
+    if (stop) break;
+  }
+}
+
+
 cudaError_t launch_index_scores(const IndexParams &a, cudaStream_t stream) {
   CUtensorMap tmK;
   if (!map_rows_sw128(&tmK, a.index_cache, (uint64_t)a.num_index_slots, kHeadDim, kHeadDim, 128))
     return cudaErrorInvalidValue;
-  auto kern = a.q_len <= 8 ? pa_index_scores_kernel<1> : pa_index_scores_kernel<2>;
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), kIdxSmem);
-  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  cfg.gridDim = dim3((a.bt_width + kIdxBlocksPerCta - 1) / kIdxBlocksPerCta, a.R);
-  cfg.blockDim = dim3(kIdxThreads);
-  cfg.dynamicSmemBytes = kIdxSmem;
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  const int sms = current_device_sms();
+  if (a.R <= kIxPersistMaxR && sms > 0) {
+    auto kern = a.q_len <= 8 ? pa_index_scores_persist_kernel<1> : pa_index_scores_persist_kernel<2>;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), kIxPersistSmem);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(3 * sms);
+    cfg.blockDim = dim3(kIxPersistThreads);
+    cfg.dynamicSmemBytes = kIxPersistSmem;
+    return cudaLaunchKernelEx(&cfg, kern, tmK, a);
+  }
+  auto kern = a.q_len <= 8 ? pa_index_scores_kernel<1> : pa_index_scores_kernel<2>;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), kIdxSmem);
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3((a.bt_width + kIdxBlocksPerCta - 1) / kIdxBlocksPerCta, a.R);
+  cfg.blockDim = dim3(kIdxThreads);
+  cfg.dynamicSmemBytes = kIdxSmem;
   return cudaLaunchKernelEx(&cfg, kern, tmK, a);
 }
 

@@ -31,6 +31,19 @@ inline cudaError_t ensure_smem_attr(const void *kern, int bytes) {
   return e;
 }
 
+// SM count of the current device (cached per device); -1 if the query fails.
+inline int current_device_sms() {
+  static int sms[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  if (sms[dev] <= 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    sms[dev] = n;
+  }
+  return sms[dev];
+}
+
 // Prologue over `grid` CTAs (M rows, plus padding rows of the MXFP8 scale grid).
 cudaError_t launch_prologue(const Params &p, int grid, bool pdl, cudaStream_t stream);
 // Prologue of the skinny path: one thread-block cluster per row (M <= 16).

@@ -167,3 +167,16 @@ def test_scores_follow_the_step_on_the_same_stream():
         compare_scores(iw, cmp, got, want, scale, extra_abs=dq)
     else:
         assert np.array_equal(np.isnan(got), np.isnan(want)) and np.array_equal(np.isneginf(got), np.isneginf(want))
+
+
+def test_many_requests_take_the_per_request_grid():
+    # more than 512 requests: the per-request grid, not the persistent kernel
+    iw = workloads.IndexWorkload("ixmany", R=600, q_len=2, seq_lo=2, seq_hi=700, bt_width=6, seed=17)
+    check(iw, 1, 1)
+
+
+def test_persistent_slices_cross_requests_and_empty_ones():
+    # requests of one row and very different lengths (some whose only block is
+    # pinned), so CTA slices start and end inside requests and skip empty ones
+    iw = workloads.IndexWorkload("ixmix", R=300, q_len=1, seq_lo=1, seq_hi=6000, bt_width=47, seed=19)
+    check(iw, 1, 2)
