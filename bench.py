@@ -938,8 +938,12 @@ def run_ours(args, wl, rank, world, local_rank):
     for name in [x for x in args.also.split(",") if x and x != "none" and x != args.workload]:
         if name in workloads.INDEX_CONFIGS:
             line[name] = index_secondary(args, name, dev, world, peaks)
+            if rank == 0 and world == 1 and not args.no_cpu_baseline:
+                line[name]["cpu_oracle"] = cpu_oracle_requests("index", name)
         elif name in workloads.DRAFTER_CONFIGS:
             line[name] = drafter_secondary(args, name, dev, world, peaks, peak_src)
+            if rank == 0 and world == 1 and not args.no_cpu_baseline:
+                line[name]["cpu_oracle"] = cpu_oracle_requests("drafter", name)
         else:
             line[name] = secondary(args, name, dev, world, peaks, peak_src)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -996,6 +1000,53 @@ def cpu_baseline(wl, st, budget_s: float = 15.0):
     return {"value": round(rows_done / dt, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"{rows_done} token rows of the {wl.name} step, one at a time, single-threaded on core "
                       f"{pin.core}, {dt:.1f} s", **cpu_info()}
+
+
+def cpu_oracle_requests(kind, name, budget_s: float = 4.0):
+    """The CPU oracle of a secondary workload (the indexer scores or the
+    drafter's attention), single-threaded on one pinned core, on whole
+    requests in order until the budget runs out; scaled to one call of all
+    its requests by their share of the call's work (window keys or scored
+    blocks)."""
+    import oracle
+
+    oracle.build()
+    if kind == "index":
+        iw = workloads.INDEX_CONFIGS[name]()
+        st = workloads.index_host_state(iw)
+        scale = float(np.float32(oracle.index_scale_log2e(iw.sm_scale)))
+        work = [max(1, (int(s) - 1) // 128 + 1) for s in st["seq_lens"]]
+
+        def one(r):
+            oracle.index_scores(st["iq"][:, iw.head * 128:(iw.head + 1) * 128], st["index_cache"],
+                                st["block_table"], st["seq_lens"], iw.q_len, iw.init_blocks, iw.local_blocks, scale,
+                                st["block_table"].shape[1] * 128, rows=[r * iw.q_len], threads=1)
+        R, unit = iw.R, "blocks"
+    else:
+        dw = workloads.DRAFTER_CONFIGS[name]()
+        st = workloads.drafter_host_state(dw)
+        cache = st["cache"].copy()
+        q8 = oracle.drafter_qkv(st["qkv"], st["qn"], st["kn"], dw.eps, st["cos_sin"], st["positions"],
+                                st["slot_mapping"], cache)
+        work = [hi - lo + 1 for lo, hi in drafter_windows(dw, st)]
+        part = 9
+
+        def one(r):
+            oracle.drafter_attention(q8, cache, st["block_table"], st["seq_lens"], st["positions"], dw.q_len,
+                                     dw.window, dw.max_blocks, part, dw.sm_scale, rows=[r * dw.q_len], threads=1)
+        R, unit = dw.R, "window keys"
+    done, share = 0, 0
+    with OneCore() as pin:
+        t0 = time.perf_counter()
+        while done < R and (done == 0 or time.perf_counter() - t0 < budget_s):
+            one(done)
+            share += work[done]
+            done += 1
+        dt = time.perf_counter() - t0
+    us_per_call = dt * 1e6 * sum(work) / share
+    return {"us_per_call": round(us_per_call, 1), "cores": 1, "kind": "oracle",
+            "sample": f"{done} of {R} requests ({share} of {sum(work)} {unit}), single-threaded on core {pin.core}, "
+                      f"{dt:.1f} s, scaled by {unit}"}
 
 
 def run_reference(args, wl):
