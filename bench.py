@@ -97,6 +97,7 @@ def step_flops(wl) -> int:
 
 # sources each kernel is compiled from (ties an ncu summary under profiles/ to them)
 KERNEL_SOURCES = {"skinny": ("pa_gemv.cu", "pa_device.cuh", "pa_tc.cuh", "pa_norm.cuh"),
+                  "skinny_persist": ("pa_gemv_persist.cu", "pa_device.cuh", "pa_tc.cuh", "pa_tma.h"),
                   "gemm": ("pa_gemm.cu", "pa_device.cuh", "pa_tc.cuh"),
                   "gemm_pair": ("pa_gemm2.cu", "pa_device.cuh", "pa_tc.cuh"),
                   "prologue": ("pa_prologue.cu", "pa_device.cuh", "pa_norm.cuh"),
@@ -300,11 +301,13 @@ class DeviceWorkload:
 
 
 def path_info(B, path):
-    name = {B.PA_PATH_GEMV: "skinny", B.PA_PATH_GEMV_FUSED: "skinny", B.PA_PATH_GEMM_SINGLE: "gemm",
-            B.PA_PATH_GEMM_PAIR: "gemm_pair"}[path]
+    name = {B.PA_PATH_GEMV: "skinny", B.PA_PATH_GEMV_FUSED: "skinny", B.PA_PATH_GEMV_PERSIST: "skinny_persist",
+            B.PA_PATH_GEMM_SINGLE: "gemm", B.PA_PATH_GEMM_PAIR: "gemm_pair"}[path]
     desc = {B.PA_PATH_GEMV: "pa_prologue_rows_kernel then pa_skinny_proj_kernel (tcgen05 GEMV, a cluster per head), "
                             "PDL-chained",
             B.PA_PATH_GEMV_FUSED: "pa_skinny_proj_kernel with the row normalisation inside (one launch)",
+            B.PA_PATH_GEMV_PERSIST: "pa_prologue_rows_kernel then pa_skinny_persist_kernel (tcgen05 GEMV, resident "
+                                    "clusters walking the heads, weights double-buffered), PDL-chained",
             B.PA_PATH_GEMM_SINGLE: "pa_prologue_kernel then pa_gemm_kernel (tcgen05, 128x128 tiles)",
             B.PA_PATH_GEMM_PAIR: "pa_prologue_kernel then pa_gemm_pair_kernel (tcgen05 cta_group::2, 256x256 tiles)"}[path]
     launches = 1 if path == B.PA_PATH_GEMV_FUSED else 2
@@ -905,6 +908,7 @@ def run_ours(args, wl, rank, world, local_rank):
     flags = {"auto": 0, "single": B.PA_FLAG_GEMM_SINGLE, "pair": B.PA_FLAG_GEMM_PAIR}[args.gemm]
     if args.fuse:
         flags |= B.PA_FLAG_FUSE
+    flags |= {"auto": 0, "regular": B.PA_FLAG_GEMV_REGULAR, "persist": B.PA_FLAG_GEMV_PERSIST}[args.gemv]
     K, W = args.steps, args.warmup
     m = measure(args, wl, dev, world, K, W, flags=flags)
     kname, desc, launches = path_info(B, m["path"])
@@ -1095,6 +1099,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--gemm", default="auto", choices=["auto", "single", "pair"],
                     help="tensor-core path tiling (auto: chosen per shape)")
+    ap.add_argument("--gemv", default="auto", choices=["auto", "regular", "persist"],
+                    help="skinny GEMV grid (auto: persistent when more heads than clusters fit at once)")
     ap.add_argument("--fuse", action="store_true",
                     help="skinny path in one kernel (row normalisation inside the GEMV) where the shape allows")
     args = ap.parse_args()

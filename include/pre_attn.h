@@ -113,6 +113,10 @@ enum pa_flags {
   PA_FLAG_EXACT_NORM = 1 << 7,      /* testing: the many-row prologue computes every activation code
                                        from the exact normalised value (the fast path's fallback);
                                        results are bitwise the same as without it */
+  PA_FLAG_GEMV_PERSIST = 1 << 9,    /* testing: the persistent skinny GEMV wherever it can run (H <= 6144),
+                                       also for head counts the one-cluster-a-head grid is chosen for */
+  PA_FLAG_GEMV_REGULAR = 1 << 10,   /* testing: the one-cluster-a-head skinny GEMV for any head count
+                                       (not with PA_FLAG_GEMV_PERSIST) */
   PA_FLAG_TEST_WAIT_TIMEOUT = 1 << 8 /* testing: every bounded device wait gives up after 200 us
                                        instead of about a second, and the main kernel's epilogue
                                        also waits on a barrier nothing arrives on, so the wait runs
@@ -462,7 +466,10 @@ enum {
   PA_PATH_GEMV = 0,         /* skinny path: prologue, then the FP8 GEMV on one cluster per head */
   PA_PATH_GEMM_SINGLE = 1,  /* tensor-core path, 128 x 128 tiles on single SMs */
   PA_PATH_GEMM_PAIR = 2,    /* tensor-core path, 256 x 256 tiles on SM pairs */
-  PA_PATH_GEMV_FUSED = 3    /* skinny path in one kernel (PA_FLAG_FUSE) */
+  PA_PATH_GEMV_FUSED = 3,   /* skinny path in one kernel (PA_FLAG_FUSE) */
+  PA_PATH_GEMV_PERSIST = 4  /* skinny path with more than four heads a resident 16-CTA cluster (H <= 6144):
+                               prologue, then a persistent GEMV whose resident clusters walk the heads
+                               through a 4-stage weight ring */
 };
 
 /* Which main kernel pre_attn_run(h, M, ...) launches on the current device

@@ -28,7 +28,8 @@ PA_CACHE_FP8, PA_CACHE_NVFP4 = 0, 1
 PA_FLAG_STATIC_KV_SCALE, PA_FLAG_FORCE_GEMV, PA_FLAG_FORCE_GEMM, PA_FLAG_NO_PDL = 1, 2, 4, 8
 PA_FLAG_GEMM_SINGLE, PA_FLAG_GEMM_PAIR, PA_FLAG_FUSE, PA_FLAG_EXACT_NORM = 16, 32, 64, 128
 PA_FLAG_TEST_WAIT_TIMEOUT = 256
-PA_PATH_GEMV, PA_PATH_GEMM_SINGLE, PA_PATH_GEMM_PAIR, PA_PATH_GEMV_FUSED = 0, 1, 2, 3
+PA_FLAG_GEMV_PERSIST, PA_FLAG_GEMV_REGULAR = 512, 1024
+PA_PATH_GEMV, PA_PATH_GEMM_SINGLE, PA_PATH_GEMM_PAIR, PA_PATH_GEMV_FUSED, PA_PATH_GEMV_PERSIST = 0, 1, 2, 3, 4
 
 _vp = ctypes.c_void_p
 

@@ -19,7 +19,7 @@ ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libpre_attn.so")
 STAMP = LIB + ".sha256"
 SOURCES = ["pa_api.cu", "pa_prologue.cu", "pa_gemv.cu", "pa_gemm.cu", "pa_gemm2.cu", "pa_noalloc.cu",
-           "pa_signal.cu", "pa_index.cu", "pa_drafter.cu"]
+           "pa_signal.cu", "pa_index.cu", "pa_drafter.cu", "pa_gemv_persist.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
               "-Xptxas", "-v", "--expt-relaxed-constexpr"]

@@ -87,9 +87,14 @@ cudaError_t query_sms(pa_handle *h) {
 // favours the finer tiles.
 int choose_path(const pa_handle *h, int M) {
   const pa_config &c = h->cfg;
-  if (uses_gemv(c, M))
-    return (c.flags & PA_FLAG_FUSE) && pa::gemv_fuses_prologue(c.hidden, c.weight_format) ? PA_PATH_GEMV_FUSED
-                                                                                         : PA_PATH_GEMV;
+  if (uses_gemv(c, M)) {
+    if ((c.flags & PA_FLAG_FUSE) && pa::gemv_fuses_prologue(c.hidden, c.weight_format)) return PA_PATH_GEMV_FUSED;
+    // more heads than clusters of the regular grid fit at once: the persistent GEMV
+    if (!(c.flags & PA_FLAG_GEMV_REGULAR) &&
+        pa::gemv_persist_clusters(h->N / 128, c.hidden, c.weight_format, (c.flags & PA_FLAG_GEMV_PERSIST) != 0) > 0)
+      return PA_PATH_GEMV_PERSIST;
+    return PA_PATH_GEMV;
+  }
   if (c.flags & PA_FLAG_GEMM_SINGLE) return PA_PATH_GEMM_SINGLE;
   if (c.flags & PA_FLAG_GEMM_PAIR) return PA_PATH_GEMM_PAIR;
   const int sms = h->num_sms > 1 ? h->num_sms : 2;
@@ -160,6 +165,7 @@ int pre_attn_init(const pa_config *cfg, pa_handle **out) {
   if (!(c.eps >= 0.0f) || c.max_tokens < 0 || c.gemm_grid < 0) return PA_ERR_CONFIG;
   if ((c.flags & PA_FLAG_FORCE_GEMV) && (c.flags & PA_FLAG_FORCE_GEMM)) return PA_ERR_CONFIG;
   if ((c.flags & PA_FLAG_GEMM_SINGLE) && (c.flags & PA_FLAG_GEMM_PAIR)) return PA_ERR_CONFIG;
+  if ((c.flags & PA_FLAG_GEMV_PERSIST) && (c.flags & PA_FLAG_GEMV_REGULAR)) return PA_ERR_CONFIG;
   pa_handle *h = new (std::nothrow) pa_handle;
   if (!h) return PA_ERR_CONFIG;
   h->cfg = c;
@@ -363,7 +369,11 @@ int pre_attn_run(pa_handle *h, int M, const pa_step_inputs *in, const pa_weights
     if (e != cudaSuccess) return cuda_fail(e);
   }
   if (h->prof_before && (e = cudaEventRecord(h->prof_before, s)) != cudaSuccess) return cuda_fail(e);
-  if (gemv) {
+  if (path == PA_PATH_GEMV_PERSIST) {
+    const int clusters = pa::gemv_persist_clusters(h->N / 128, c.hidden, c.weight_format,
+                                                   (c.flags & PA_FLAG_GEMV_PERSIST) != 0);
+    e = clusters > 0 ? pa::launch_gemv_persist(p, clusters, pdl, s) : cudaErrorNotSupported;
+  } else if (gemv) {
     e = pa::launch_gemv(p, fused, pdl, s);
   } else {
     e = path == PA_PATH_GEMM_PAIR ? pa::launch_gemm_pair(p, h->num_sms, h->l2_bytes, c.gemm_grid, pdl, s)

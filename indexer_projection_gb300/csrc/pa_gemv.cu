@@ -108,7 +108,7 @@ __host__ __device__ inline GvLayout gv_layout(int C, int kc, int mx) {
 }
 
 // Small per-CTA state (static shared memory).
-struct GvStatic {
+struct alignas(16) GvStatic {  // cs rows are 16-byte cp.async destinations
   float wsc[kHeadDim];           // per-channel weight scales of the head
   __nv_bfloat16 gam[kHeadDim];   // the head role's gamma
   __nv_bfloat16 cs[2][kRotDim];  // cos / sin rows of the tokens finished here
@@ -585,6 +585,30 @@ cudaError_t launch_t(const Params &p, bool fused, bool pdl, cudaStream_t stream)
 }  // namespace
 
 bool gemv_fuses_prologue(int H, int weight_fmt) { return weight_fmt == 0 ? fused_ok<0>(H) : fused_ok<1>(H); }
+
+int gemv_regular_clusters(int weight_fmt, int H) {
+  const int smem = gv_smem(16, gv_kc(H, 16), weight_fmt);
+  if ((weight_fmt == 0 ? pick_cluster<0>(smem) : pick_cluster<1>(smem)) != 16) return 0;
+  const void *k = weight_fmt == 0 ? reinterpret_cast<const void *>(pa_skinny_proj_kernel<0, 16, false, 0>)
+                                  : reinterpret_cast<const void *>(pa_skinny_proj_kernel<1, 16, false, 0>);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(16 * 64);
+  cfg.blockDim = dim3(kGvThreads);
+  cfg.dynamicSmemBytes = smem;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 16;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
 
 cudaError_t launch_gemv(const Params &p, bool fused, bool pdl, cudaStream_t stream) {
   if (p.cache_fmt == 0)

@@ -57,6 +57,14 @@ cudaError_t launch_pack_scales(const uint8_t *src, uint8_t *dst, int rows, int k
 // the prologue's work and no prologue is launched.
 bool gemv_fuses_prologue(int H, int weight_fmt);
 cudaError_t launch_gemv(const Params &p, bool fused, bool pdl, cudaStream_t stream);
+// Resident clusters of 16 of that kernel at hidden size H (0: clusters of 16
+// cannot be co-scheduled).
+int gemv_regular_clusters(int weight_fmt, int H);
+// The persistent variant for many heads (pa_gemv_persist.cu): the clusters
+// to launch, or 0 where it is not used (H > 6144, not launchable, or -
+// unless forced - the regular grid fits one wave).
+int gemv_persist_clusters(int n_heads, int H, int weight_fmt, bool force);
+cudaError_t launch_gemv_persist(const Params &p, int clusters, bool pdl, cudaStream_t stream);
 
 // Tensor-core path: persistent tcgen05 GEMM with the fused head epilogue,
 // on single CTAs (128 x 128 tiles) or on CTA pairs (cta_group::2, 256 x 256).

@@ -50,7 +50,8 @@ def _cfg(B, **kw):
                                  dict(n_kv_heads=3), dict(n_kv_heads=0), dict(weight_format=2),
                                  dict(cache_format=5), dict(block_size=8),
                                  dict(cache_format=1, block_size=6), dict(eps=-1.0),
-                                 dict(max_tokens=-1), dict(flags=2 | 4), dict(n_q_heads=-1)])
+                                 dict(max_tokens=-1), dict(flags=2 | 4), dict(flags=16 | 32),
+                                 dict(flags=512 | 1024), dict(n_q_heads=-1)])
 def test_init_rejects_bad_configs(B, bad):
     h = ctypes.c_void_p()
     st = B.load().pre_attn_init(ctypes.byref(_cfg(B, **bad)), ctypes.byref(h))

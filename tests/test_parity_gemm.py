@@ -111,9 +111,14 @@ def test_path_choice():
                     flags=flags)
         return B.pre_attn_path(r.handle, M)
 
-    skinny = (B.PA_PATH_GEMV, B.PA_PATH_GEMV_FUSED)
+    skinny = (B.PA_PATH_GEMV, B.PA_PATH_GEMV_FUSED, B.PA_PATH_GEMV_PERSIST)
     assert path(8) in skinny and path(16) in skinny
-    assert path(8) == B.PA_PATH_GEMV and path(8, B.PA_FLAG_FUSE) == B.PA_PATH_GEMV_FUSED
+    # 77 heads at nkv = 4: more than two waves of 16-CTA clusters on 152 SMs;
+    # 20 heads at nkv = 1 (the decode shape) stay on the one-cluster-a-head grid
+    assert path(8) == B.PA_PATH_GEMV_PERSIST and path(8, B.PA_FLAG_FUSE) == B.PA_PATH_GEMV_FUSED
+    assert path(8, nkv=1) == B.PA_PATH_GEMV
+    assert path(8, B.PA_FLAG_GEMV_REGULAR) == B.PA_PATH_GEMV
+    assert path(8, B.PA_FLAG_GEMV_PERSIST, nkv=1) == B.PA_PATH_GEMV_PERSIST
     assert path(8, B.PA_FLAG_FORCE_GEMM) in (B.PA_PATH_GEMM_SINGLE, B.PA_PATH_GEMM_PAIR)
     assert path(8192) == B.PA_PATH_GEMM_PAIR  # 1312 pair tiles vs 5184 single tiles
     assert path(8192, B.PA_FLAG_GEMM_SINGLE) == B.PA_PATH_GEMM_SINGLE

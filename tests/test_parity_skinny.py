@@ -111,6 +111,30 @@ def test_sweep_config_skinny_points(M):
     check(workloads.sweep(M), flags=0)
 
 
+@pytest.mark.parametrize("fmt", ["ptpc", "mx"])
+def test_persistent_gemv(fmt):
+    # the persistent GEMV: resident clusters walk the heads c, c + G, ...
+    # with weight buffers and tensor-memory accumulators double-buffered
+    from indexer_projection_gb300 import binding as B
+    flags = B.PA_FLAG_FORCE_GEMV | B.PA_FLAG_GEMV_PERSIST
+
+    def run(wl, runs=1):
+        g = check(wl, flags=flags, runs=runs)
+        assert B.pre_attn_path(g.runner.handle, wl.M) == B.PA_PATH_GEMV_PERSIST
+
+    # 77 heads: every cluster takes several, both buffers turn over many times;
+    # repeated calls reuse the barriers' fresh state each launch
+    run(workloads.sweep(16).replace(name=f"pg77_{fmt}", weight_fmt=fmt, M=16), runs=2)
+    run(workloads.sweep(1).replace(name=f"pg77m1_{fmt}", weight_fmt=fmt, cache_fmt="nvfp4", pool_pages=4096))
+    run(workloads.decode().replace(weight_fmt=fmt, q_fp8=True, iq_fp8=True))
+    # empty K ranges (512: 4 of 16 ranges hold a chunk), fewer heads than clusters
+    run(workloads.tiny().replace(M=5, weight_fmt=fmt, q_fp8=True, iq_fp8=True))
+    # ragged K: 4352 = 16 ranges of 384 with the last ones short or empty
+    run(workloads.Workload(f"pg_ragged_{fmt}", H=4352, nkv=2, M=9, weight_fmt=fmt, cache_fmt="nvfp4", seed=97,
+                           positions="uniform", max_pos=500, pool_pages=64, q_fp8=True, iq_fp8=True,
+                           outlier_frac=0.2, skip_rows=(3,)))
+
+
 @pytest.mark.parametrize("H", [128, 2048, 2176, 4352, 16384])
 @pytest.mark.parametrize("fmt", ["ptpc", "mx"])
 def test_k_ranges(H, fmt):

@@ -23,18 +23,19 @@ pytestmark = pytest.mark.gpu
 
 def _flags(path):
     from indexer_projection_gb300 import binding as B
-    return {"skinny": B.PA_FLAG_FORCE_GEMV, "single": B.PA_FLAG_FORCE_GEMM | B.PA_FLAG_GEMM_SINGLE,
+    return {"skinny": B.PA_FLAG_FORCE_GEMV, "persist": B.PA_FLAG_FORCE_GEMV | B.PA_FLAG_GEMV_PERSIST,
+            "single": B.PA_FLAG_FORCE_GEMM | B.PA_FLAG_GEMM_SINGLE,
             "pair": B.PA_FLAG_FORCE_GEMM | B.PA_FLAG_GEMM_PAIR}[path]
 
 
 def _wl(path):
-    if path == "skinny":
+    if path in ("skinny", "persist"):
         return workloads.tiny().replace(M=5, q_fp8=True, iq_fp8=True, skip_rows=(2,))
     return workloads.tiny().replace(name=f"sig_{path}", M=100, weight_fmt="mx", cache_fmt="nvfp4", pool_pages=64,
                                     q_fp8=True, iq_fp8=True, skip_rows=(7,))
 
 
-@pytest.mark.parametrize("path", ["skinny", "single", "pair"])
+@pytest.mark.parametrize("path", ["skinny", "persist", "single", "pair"])
 def test_done_words_carry_the_epoch_of_each_step(path):
     wl = _wl(path)
     st = workloads.host_state(wl)
@@ -51,7 +52,7 @@ def test_done_words_carry_the_epoch_of_each_step(path):
         assert g.runner.device_status() == 0
 
 
-@pytest.mark.parametrize("path", ["skinny", "pair"])
+@pytest.mark.parametrize("path", ["skinny", "persist", "pair"])
 def test_consumer_chained_behind_the_step_sees_every_word(path):
     from indexer_projection_gb300 import binding as B
 
@@ -92,7 +93,7 @@ def test_consumer_wait_runs_out_and_the_stream_stays_usable():
     assert B.pre_attn_wait_done(None, 3, 5, 100, status, check=False) == B.PA_ERR_NULL
 
 
-@pytest.mark.parametrize("path", ["skinny", "single", "pair"])
+@pytest.mark.parametrize("path", ["skinny", "persist", "single", "pair"])
 def test_a_device_wait_that_runs_out_is_reported_and_the_next_step_is_correct(path):
     # PA_FLAG_TEST_WAIT_TIMEOUT: the main kernel's epilogue waits on a barrier
     # nothing arrives on, with a 200 us limit; the wait runs out, the kernel
