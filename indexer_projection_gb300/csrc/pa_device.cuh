@@ -318,17 +318,26 @@ __device__ __forceinline__ void head_rope(float (&v)[E], int d0, const __nv_bflo
   if constexpr (E >= kRotDim) {
     // the thread holds dims [d0, d0 + E); d0 = 0 whenever it holds [0, 64)
     if (d0 == 0) {
+      // 16-byte pieces of the (16-byte aligned) cos / sin row: with a thread
+      // a row, every load instruction touches as many lines as the warp has
+      // rows, so fewer and wider loads
+      const uint4 *cs4 = reinterpret_cast<const uint4 *>(cs_row);
 #pragma unroll
-      for (int i = 0; i < kHalfRot; i += 2) {
-        const uint32_t cw = *reinterpret_cast<const uint32_t *>(cs_row + i);
-        const uint32_t sw = *reinterpret_cast<const uint32_t *>(cs_row + kHalfRot + i);
-        float c[2] = {bf16_to_f32(cw & 0xffff), bf16_to_f32(cw >> 16)};
-        float s[2] = {bf16_to_f32(sw & 0xffff), bf16_to_f32(sw >> 16)};
+      for (int q = 0; q < kHalfRot / 8; ++q) {
+        const uint4 cq = cs4[q], sq = cs4[kHalfRot / 8 + q];
+        const uint32_t cw4[4] = {cq.x, cq.y, cq.z, cq.w}, sw4[4] = {sq.x, sq.y, sq.z, sq.w};
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          float x = v[i + j], y = v[i + j + kHalfRot];
-          v[i + j] = x * c[j] - y * s[j];
-          v[i + j + kHalfRot] = y * c[j] + x * s[j];
+        for (int k = 0; k < 4; ++k) {
+          const int i = 8 * q + 2 * k;
+          const uint32_t cw = cw4[k], sw = sw4[k];
+          float c[2] = {bf16_to_f32(cw & 0xffff), bf16_to_f32(cw >> 16)};
+          float s[2] = {bf16_to_f32(sw & 0xffff), bf16_to_f32(sw >> 16)};
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            float x = v[i + j], y = v[i + j + kHalfRot];
+            v[i + j] = x * c[j] - y * s[j];
+            v[i + j + kHalfRot] = y * c[j] + x * s[j];
+          }
         }
       }
     }
@@ -352,6 +361,28 @@ __device__ __forceinline__ void head_rope(float (&v)[E], int d0, const __nv_bflo
       if (in_rope) v[j] = first ? (v[j] * c[j] - p * s[j]) : (v[j] * c[j] + p * s[j]);
     }
   }
+}
+
+// e4m3 codes of RN(x / s) (s > 0) for 4 values, from the product with
+// rs = RN(1 / s): x * rs is within 2^-22 (relative) of x / s and of its
+// rounding, so where the codes of x * rs scaled by 1 -+ 2^-20 agree, every
+// value in between (RN(x / s) included) has that code, rounding being
+// monotonic.  `ok` is cleared otherwise (a value within 2^-20 of a code
+// boundary, about one in 2^15), and the caller then takes the true quotient
+// (e4m3x4_div): the codes are those of the division bit for bit.  The check
+// and the rare division are kept apart so the common path stays straight-line
+// code (a fused select of the two measured 6x slower in a thread-per-row
+// epilogue).
+__device__ __forceinline__ uint32_t e4m3x4_prod_checked(float a, float b, float c, float d, float rs, bool &ok) {
+  const float qa = a * rs, qb = b * rs, qc = c * rs, qd = d * rs;
+  constexpr float lo = 1.0f - 0x1p-20f, hi = 1.0f + 0x1p-20f;
+  const uint32_t w = e4m3x4(qa, qb, qc, qd);
+  const uint32_t wl = e4m3x4(qa * lo, qb * lo, qc * lo, qd * lo), wh = e4m3x4(qa * hi, qb * hi, qc * hi, qd * hi);
+  ok = ok & (w == wl) & (w == wh);
+  return w;
+}
+static __device__ __noinline__ uint32_t e4m3x4_div(float a, float b, float c, float d, float s) {
+  return e4m3x4(__fdiv_rn(a, s), __fdiv_rn(b, s), __fdiv_rn(c, s), __fdiv_rn(d, s));
 }
 
 // [K1] page16_of: page-16 id of a slot under the K / V block page stride.
@@ -502,30 +533,48 @@ __device__ __forceinline__ void head_epilogue_stores(const Params &p, const Head
     for (int i = 0; i < E; ++i) amax = fmaxf(amax, fabsf(v[i]));
     amax = Row<E>::max(amax);
     const float s = p.static_kv ? 1.0f : (amax == 0.f ? 1.0f : __fdiv_rn(amax, kFp8Max));
+    const float rs = __frcp_rn(s);
     const int64_t page = (p16 * p.n_kv + kvh) * 2048;
     if (is_k) {
-      auto k4 = [&](int i) {
-        return e4m3x4(__fdiv_rn(bf16_round(v[i]), s), __fdiv_rn(bf16_round(v[i + 1]), s),
-                      __fdiv_rn(bf16_round(v[i + 2]), s), __fdiv_rn(bf16_round(v[i + 3]), s));
+      // codes of 4 K values (bf16 first), the true quotient only where the
+      // product's code is not certain
+      auto k4 = [&](int i, bool &ok) {
+        return e4m3x4_prod_checked(bf16_round(v[i]), bf16_round(v[i + 1]), bf16_round(v[i + 2]), bf16_round(v[i + 3]),
+                                   rs, ok);
+      };
+      auto k4_div = [&](int i) {
+        return e4m3x4_div(bf16_round(v[i]), bf16_round(v[i + 1]), bf16_round(v[i + 2]), bf16_round(v[i + 3]), s);
       };
       if constexpr (E >= 16) {  // 16 dims: one 16-byte row of the page's 16 x 16 block
 #pragma unroll
         for (int q = 0; q < E / 16; ++q) {
           const int d = d0 + 16 * q;
-          *reinterpret_cast<uint4 *>(p.k_cache + page + (d >> 4) * 256 + t * 16) =
-              make_uint4(k4(16 * q), k4(16 * q + 4), k4(16 * q + 8), k4(16 * q + 12));
+          bool ok = true;
+          uint4 w = make_uint4(k4(16 * q, ok), k4(16 * q + 4, ok), k4(16 * q + 8, ok), k4(16 * q + 12, ok));
+          if (__builtin_expect(!ok, 0))
+            w = make_uint4(k4_div(16 * q), k4_div(16 * q + 4), k4_div(16 * q + 8), k4_div(16 * q + 12));
+          *reinterpret_cast<uint4 *>(p.k_cache + page + (d >> 4) * 256 + t * 16) = w;
         }
       } else {
 #pragma unroll
         for (int q = 0; q < E / 4; ++q) {
           const int d = d0 + 4 * q;
-          *reinterpret_cast<uint32_t *>(p.k_cache + page + (d >> 4) * 256 + t * 16 + (d & 15)) = k4(4 * q);
+          bool ok = true;
+          uint32_t w = k4(4 * q, ok);
+          if (__builtin_expect(!ok, 0)) w = k4_div(4 * q);
+          *reinterpret_cast<uint32_t *>(p.k_cache + page + (d >> 4) * 256 + t * 16 + (d & 15)) = w;
         }
       }
       if (d0 == 0) p.k_scale[(p16 * p.n_kv + kvh) * 16 + t] = s;
     } else {
 #pragma unroll
-      for (int i = 0; i < E; ++i) p.v_cache[page + (d0 + i) * 16 + t] = e4m3(__fdiv_rn(v[i], s));
+      for (int i = 0; i < E; i += 4) {
+        bool ok = true;
+        uint32_t w = e4m3x4_prod_checked(v[i], v[i + 1], v[i + 2], v[i + 3], rs, ok);
+        if (__builtin_expect(!ok, 0)) w = e4m3x4_div(v[i], v[i + 1], v[i + 2], v[i + 3], s);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) p.v_cache[page + (d0 + i + j) * 16 + t] = (uint8_t)(w >> (8 * j));
+      }
       if (d0 == 0) p.v_scale[(p16 * p.n_kv + kvh) * 16 + t] = s;
     }
     return;
