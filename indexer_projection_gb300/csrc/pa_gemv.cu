@@ -132,16 +132,21 @@ __device__ __forceinline__ void st_async_b32(uint32_t caddr, float v, uint32_t c
 }
 
 // The fused variant's row normalisation for the CTA's K range [k0, k1) of
-// every token (16 threads a token: thread (m, sub) holds chunks sub + 16j of
-// 8 elements), written as the MMA's B operand.  Exchanges with the 16 CTAs
-// of the cluster; leaves the per-token scales in xs (per-channel format).
+// every token (G threads a token, G = 32 for up to 8 tokens, else 16: thread
+// (m, sub) holds chunks sub + G j of 8 elements), written as the MMA's B
+// operand.  Exchanges with the 16 CTAs of the cluster; leaves the per-token
+// scales in xs (per-channel format).  The codes come from the checked fast
+// path of the many-row prologue (pa_norm.cuh: a cheap n, kept where every
+// value within kSafe of it gives the same code or block exponent, else the
+// exact n), so they are the exact path's bit for bit.
 template <int WFMT>
 __device__ __forceinline__ void fused_norm_quant(const Params &p, int tid, int ks, int k0, int k1, int h,
                                                  uint8_t *x_s, uint8_t *sfb_s, float4 *ex1, const uint4 *gin_s,
                                                  float *xs, uint64_t *ex1_bar) {
-  constexpr int kJ = kFusedMaxKc / 8 / 16;  // chunks a thread
+  constexpr int kJ = kFusedMaxKc / 8 / 16;  // chunks a thread at most (G = 16)
   const int M = p.M, K = p.H;
-  const int m = tid >> 4, sub = tid & 15;
+  const int G = M <= 8 ? 32 : 16;
+  const int m = tid / G, sub = tid % G;
   const int cpt = (k1 - k0) / 8;  // chunks of 8 elements a token in the range
   const bool active = m < M;
   float acc[kJ][8];
@@ -150,20 +155,28 @@ __device__ __forceinline__ void fused_norm_quant(const Params &p, int tid, int k
     const uint4 *ar = reinterpret_cast<const uint4 *>(p.ar + (int64_t)m * K + k0);
     const uint4 *res = reinterpret_cast<const uint4 *>(p.res + (int64_t)m * K + k0);
     uint4 *rout = (h == 0 && p.residual) ? reinterpret_cast<uint4 *>(p.residual + (int64_t)m * K + k0) : nullptr;
+    uint4 av[kJ], rv[kJ];  // every load in flight before the first use
 #pragma unroll
     for (int j = 0; j < kJ; ++j) {
-      const int c = sub + 16 * j;
+      const int c = sub + G * j;
+      if (c < cpt) {
+        av[j] = __ldcs(ar + c);
+        rv[j] = __ldcs(res + c);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kJ; ++j) {
+      const int c = sub + G * j;
       if (c < cpt) {
         uint4 rb;
-        acc8(__ldcs(ar + c), __ldcs(res + c), acc[j], rb, sh, sl);
+        acc8(av[j], rv[j], acc[j], rb, sh, sl);
         if (rout) __stcs(rout + c, rb);
         if (WFMT == 0) absprod_max8(acc[j], gin_s[c], mh, ml);
       }
     }
   }
-  // the token's partials over this K range, in all 16 lanes of the group
-#pragma unroll
-  for (int o = 8; o > 0; o >>= 1) {
+  // the token's partials over this K range, in all G lanes of the group
+  for (int o = G / 2; o > 0; o >>= 1) {
     const float oh = __shfl_xor_sync(0xffffffffu, sh, o), ol = __shfl_xor_sync(0xffffffffu, sl, o);
     dd_add(sh, sl, oh, ol);
     if (WFMT == 0) {
@@ -172,8 +185,8 @@ __device__ __forceinline__ void fused_norm_quant(const Params &p, int tid, int k
     }
   }
   cluster_wait();  // every CTA of the cluster has initialised its barriers
-  // lane sub of token m's group sends this range's partials to cluster CTA sub
-  if (active) {
+  // lane sub < 16 of token m's group sends this range's partials to cluster CTA sub
+  if (active && sub < 16) {
     float4 *dst = ex1 + ks * kMaxTok + m;
     if (WFMT == 0)
       st_async_v4(mapa(smem_u32(dst), sub), make_float4(sh, sl, mh, ml), mapa(smem_u32(ex1_bar), sub));
@@ -190,12 +203,8 @@ __device__ __forceinline__ void fused_norm_quant(const Params &p, int tid, int k
 #pragma unroll
     for (int q = 1; q < 16; ++q) dd_add(th, tl, ex1[q * kMaxTok + m].x, ex1[q * kMaxTok + m].y);
     rstd_from_dd(th, tl, K, p.eps, rh, rl);
-#pragma unroll
-    for (int j = 0; j < kJ; ++j) {
-      const int c = sub + 16 * j;
-      if (c < cpt) norm8(acc[j], gin_s[c], rh, rl);
-    }
   }
+  const float f = __fadd_rn(rh, rl);
   // quantise into the B operand: chunk c of token m is K bytes 8c .. 8c + 7 of
   // the range: 128-byte chunk c / 16, 16-byte piece (c % 16) / 2, half c % 2
   auto put = [&](int c, uint2 w) {
@@ -208,10 +217,20 @@ __device__ __forceinline__ void fused_norm_quant(const Params &p, int tid, int k
       for (int q = 1; q < 16; ++q) pair_max(qh, ql, ex1[q * kMaxTok + m].z, ex1[q * kMaxTok + m].w);
       const float tmax = amax_from_pair(qh, ql, rh, rl);
       const float s = tmax == 0.f ? 1.0f : __fdiv_rn(tmax, kFp8Max);
+      const float rs = __frcp_rn(s);
 #pragma unroll
       for (int j = 0; j < kJ; ++j) {
-        const int c = sub + 16 * j;
-        if (c < cpt) put(c, quant8_ptpc(acc[j], s));
+        const int c = sub + G * j;
+        if (c < cpt) {
+          float t[8];
+          napprox8(acc[j], gin_s[c], f, t);
+          uint2 w;
+          if (!codes8_checked(t, rs, w)) {  // near a code boundary: the exact n and a true divide
+            norm8(acc[j], gin_s[c], rh, rl);
+            w = quant8_ptpc(acc[j], s);
+          }
+          put(c, w);
+        }
       }
       if (sub == 0) xs[m] = s;
     }
@@ -219,13 +238,37 @@ __device__ __forceinline__ void fused_norm_quant(const Params &p, int tid, int k
     // a 32-element block is 4 consecutive chunks: lanes sub .. sub + 3 of the group
 #pragma unroll
     for (int j = 0; j < kJ; ++j) {
-      const int c = sub + 16 * j;
-      float bm = (active && ok1 && c < cpt) ? amax8(acc[j]) : 0.f;
+      const int c = sub + G * j;
+      const bool mine = active && ok1 && c < cpt;
+      float t[8];
+      float bm = 0.f;
+      if (mine) {
+        napprox8(acc[j], gin_s[c], f, t);
+        bm = amax8(t);
+      }
       bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
       bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
-      if (active && ok1 && c < cpt) {
+      // the exponent is exact where every amax within kSafe gives it
+      const bool e_ok = mx_exponent(bm * (1.0f - kSafe)) == mx_exponent(bm * (1.0f + kSafe));
+      const bool exact = __any_sync(0xffffffffu, !e_ok);  // warp-uniform
+      if (exact) {  // rare: this warp's blocks from the exact n (acc[j] becomes n)
+        if (mine) {
+          norm8(acc[j], gin_s[c], rh, rl);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) t[i] = acc[j][i];
+        }
+        bm = mine ? amax8(t) : 0.f;
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+      }
+      if (mine) {
         const int e = mx_exponent(bm);
-        put(c, quant8_mx(acc[j], pow2_neg(e)));
+        uint2 w;
+        if (!codes8_checked(t, pow2_neg(e), w)) {  // near a code boundary: from the exact n
+          if (!exact) norm8(acc[j], gin_s[c], rh, rl);
+          w = quant8_mx(acc[j], pow2_neg(e));
+        }
+        put(c, w);
         // F8_128x4 atom of 128-byte chunk c / 16: row m, K-block (c / 4) % 4
         if ((c & 3) == 0) sfb_s[(c >> 4) * kSfAtom + m * 16 + ((c >> 2) & 3)] = (uint8_t)(e + 127);
       }
