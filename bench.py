@@ -1092,7 +1092,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference", "ours"])
     ap.add_argument("--workload", default="decode")
-    ap.add_argument("--also", default="prefill,spec_decode,index_spec_decode,drafter_spec_decode",
+    ap.add_argument("--also", default="prefill,spec_decode,sweep_m8,index_spec_decode,drafter_spec_decode",
                     help="comma-separated workloads also timed in the same run, each reported under its name "
                          "(the step's configurations, or an indexer-score configuration); none: skip")
     ap.add_argument("--no-cpu-baseline", action="store_true")
