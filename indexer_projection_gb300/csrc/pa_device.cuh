@@ -220,6 +220,14 @@ __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.w
 __device__ __forceinline__ void arrive_remote(uint32_t caddr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
 }
+// The same without release semantics, for an arrival that orders nothing in
+// memory the waiter reads (a tensor-memory accumulator freed after
+// tcgen05.wait::ld and tcgen05.fence::before_thread_sync): a release there
+// waits until every earlier store of the thread is performed at cluster
+// scope, which behind an epilogue's global stores takes microseconds.
+__device__ __forceinline__ void arrive_remote_relaxed(uint32_t caddr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
 __device__ __forceinline__ void st_cluster_v4(uint32_t caddr, float4 v) {
   asm volatile("st.shared::cluster.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(caddr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
                : "memory");
