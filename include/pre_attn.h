@@ -358,6 +358,10 @@ typedef struct pa_index_args {
   uint32_t *status;           /* device status word: PA_DEV_SLOT_RANGE (a block id outside the cache, or a
                                  request shorter than q_len or longer than its block table: skipped),
                                  PA_DEV_WAIT_TIMEOUT */
+  uint32_t flags;             /* 0, or PA_FLAG_TEST_WAIT_TIMEOUT (testing: every wait gives up after 200 us
+                                 and the score warps also wait on a barrier nothing arrives on, so the
+                                 wait runs out: the CTAs stop, their scores are not written and
+                                 PA_DEV_WAIT_TIMEOUT is raised, as a real timeout would) */
 } pa_index_args;
 
 /* index_scale_log2e(sm_scale) (build_pre_attn_kernel; body not printed):
@@ -368,8 +372,8 @@ float pre_attn_index_scale_log2e(float sm_scale);
  * pre_attn_run on the same stream: it reads the rows and keys after that
  * step's kernels complete (programmatic dependent launch).  Allocates
  * nothing, never synchronises.  Errors (nothing launched): PA_ERR_NULL,
- * PA_ERR_SHAPE, PA_ERR_CONFIG (negative block counts, NaN scale),
- * PA_ERR_ALIGN; PA_ERR_CUDA if the launch fails. */
+ * PA_ERR_SHAPE, PA_ERR_CONFIG (negative block counts, NaN scale, unknown
+ * flags), PA_ERR_ALIGN; PA_ERR_CUDA if the launch fails. */
 int pre_attn_index_scores(const pa_index_args *args, void *stream);
 
 /* ------------------------------------------------ the drafter's attention

@@ -71,7 +71,7 @@ class pa_index_args(ctypes.Structure):
                 ("num_index_slots", ctypes.c_int64), ("block_table", _vp), ("seq_lens", _vp), ("R", ctypes.c_int),
                 ("q_len", ctypes.c_int), ("bt_width", ctypes.c_int), ("init_blocks", ctypes.c_int),
                 ("local_blocks", ctypes.c_int), ("index_scale", ctypes.c_float), ("scores", _vp),
-                ("score_stride", ctypes.c_int64), ("status", _vp)]
+                ("score_stride", ctypes.c_int64), ("status", _vp), ("flags", ctypes.c_uint32)]
 
 
 class pa_drafter_args(ctypes.Structure):

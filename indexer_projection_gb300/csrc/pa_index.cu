@@ -59,6 +59,8 @@ struct IndexParams {
   float *scores;
   int64_t score_stride;
   uint32_t *status;
+  uint64_t lim;      // bound of every wait (ns)
+  int test_timeout;  // testing: the score warps also wait on a barrier nothing arrives on
 };
 
 __device__ __forceinline__ void tma_rows(uint32_t dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
@@ -115,6 +117,7 @@ __global__ void __launch_bounds__(kIdxThreads) pa_index_scores_kernel(const __gr
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   __shared__ __align__(8) uint64_t full[kIdxBlocksPerCta];
+  __shared__ __align__(8) uint64_t never;  // testing: nothing arrives on it
   __shared__ int blk_s[kIdxBlocksPerCta];  // block id, -1: not loaded
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -131,6 +134,7 @@ __global__ void __launch_bounds__(kIdxThreads) pa_index_scores_kernel(const __gr
       mbar_init(&full[k], 1);
       blk_s[k] = -1;
     }
+    mbar_init(&never, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -185,7 +189,8 @@ __global__ void __launch_bounds__(kIdxThreads) pa_index_scores_kernel(const __gr
       for (int e = 0; e < 4; ++e) c[nt][e] = 0.f;
     bool ok = true;
     if (loaded) {
-      ok = mbar_wait(&full[k], 0, a.status);
+      ok = mbar_wait(&full[k], 0, a.status, a.lim);
+      if (ok && a.test_timeout) ok = mbar_wait(&never, 0, a.status, a.lim);
       if (ok) {
         const uint32_t base = smem_u32(smem + k * kKeyBlockBytes);
         // ldmatrix: thread l gives row (l & 7) of tile (l >> 3): key 16 warp +
@@ -272,6 +277,7 @@ __global__ void __launch_bounds__(kIxPersistThreads) pa_index_scores_persist_ker
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   __shared__ __align__(8) uint64_t full[kIxStages], empty[kIxStages];
+  __shared__ __align__(8) uint64_t never;  // testing: nothing arrives on it
   __shared__ int offs[kIxPersistMaxR + 1];  // items before request r
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -308,6 +314,7 @@ __global__ void __launch_bounds__(kIxPersistThreads) pa_index_scores_persist_ker
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kIxComputeWarps);
     }
+    mbar_init(&never, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -349,7 +356,7 @@ __global__ void __launch_bounds__(kIxPersistThreads) pa_index_scores_persist_ker
         if (blk < 0) continue;
         const int s = j % kIxStages;
         if (lane == 0) {
-          if (!mbar_wait(&empty[s], ((uint32_t)(j / kIxStages) & 1) ^ 1, a.status)) ok = false;
+          if (!mbar_wait(&empty[s], ((uint32_t)(j / kIxStages) & 1) ^ 1, a.status, a.lim)) ok = false;
           else {
             mbar_expect_tx(&full[s], kKeyBlockBytes);
             tma_rows(smem_u32(smem + s * kKeyBlockBytes), &tmK, 0, (int)(blk * 128), &full[s]);
@@ -363,7 +370,7 @@ __global__ void __launch_bounds__(kIxPersistThreads) pa_index_scores_persist_ker
     // the copies issued land before the CTA exits (they have, unless a wait ran out)
     if (lane == 0)
       for (int k = j - 1; k >= 0 && k >= j - kIxStages; --k)
-        mbar_wait(&full[k % kIxStages], (uint32_t)(k / kIxStages) & 1, a.status);
+        mbar_wait(&full[k % kIxStages], (uint32_t)(k / kIxStages) & 1, a.status, a.lim);
     return;
   }
   // ------------------------------------------------------------ compute
@@ -402,7 +409,8 @@ __global__ void __launch_bounds__(kIxPersistThreads) pa_index_scores_persist_ker
         for (int e = 0; e < 4; ++e) c[nt][e] = 0.f;
       if (loaded) {
         const int s = j % kIxStages;
-        const bool got = mbar_wait(&full[s], (uint32_t)(j / kIxStages) & 1, a.status);
+        bool got = mbar_wait(&full[s], (uint32_t)(j / kIxStages) & 1, a.status, a.lim);
+        if (got && a.test_timeout) got = mbar_wait(&never, 0, a.status, a.lim);
         if (__any_sync(0xffffffffu, !got)) {  // the warp gives up together
           stop = true;
           break;
@@ -493,6 +501,7 @@ extern "C" int pre_attn_index_scores(const pa_index_args *in, void *stream) {
   if (x.R < 0 || x.R > 65535 || x.q_len < 1 || x.q_len > pa::kIdxMaxRows || x.bt_width < 1 || x.head < 0)
     return PA_ERR_SHAPE;
   if (x.init_blocks < 0 || x.local_blocks < 0 || !(x.index_scale == x.index_scale)) return PA_ERR_CONFIG;
+  if (x.flags & ~(uint32_t)PA_FLAG_TEST_WAIT_TIMEOUT) return PA_ERR_CONFIG;
   if (x.num_index_slots < 128 || x.num_index_slots % 128) return PA_ERR_SHAPE;
   if (x.iq_stride < (int64_t)(x.head + 1) * pa::kHeadDim || x.score_stride < (int64_t)x.bt_width * 128)
     return PA_ERR_SHAPE;
@@ -520,6 +529,8 @@ extern "C" int pre_attn_index_scores(const pa_index_args *in, void *stream) {
   a.scores = x.scores;
   a.score_stride = x.score_stride;
   a.status = x.status;
+  a.test_timeout = (x.flags & PA_FLAG_TEST_WAIT_TIMEOUT) ? 1 : 0;
+  a.lim = a.test_timeout ? pa::kTestWaitNs : pa::kWaitNs;
   const cudaError_t e = pa::launch_index_scores(a, (cudaStream_t)stream);
   return e == cudaSuccess ? PA_OK : pa::record_cuda_error(e);
 }

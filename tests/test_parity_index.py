@@ -21,7 +21,7 @@ def _bf16(a):
     return (np.asarray(a, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def run_gpu(iw, st, init, local, scale, score_cols, iq=None, cache=None):
+def run_gpu(iw, st, init, local, scale, score_cols, iq=None, cache=None, flags=0):
     import torch
 
     from indexer_projection_gb300 import binding as B
@@ -35,7 +35,7 @@ def run_gpu(iw, st, init, local, scale, score_cols, iq=None, cache=None):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     a = B.pa_index_args(B.ptr(d_iq), d_iq.shape[1], iw.head, B.ptr(d_cache), d_cache.numel() // 128,
                         B.ptr(d_bt), B.ptr(d_sl), iw.R, iw.q_len, st["block_table"].shape[1], init, local,
-                        scale, B.ptr(scores), score_cols, B.ptr(status))
+                        scale, B.ptr(scores), score_cols, B.ptr(status), flags)
     B.pre_attn_index_scores(a, torch.cuda.current_stream())
     torch.cuda.synchronize()
     return scores.cpu().numpy(), int(status.item())
@@ -180,3 +180,24 @@ def test_persistent_slices_cross_requests_and_empty_ones():
     # pinned), so CTA slices start and end inside requests and skip empty ones
     iw = workloads.IndexWorkload("ixmix", R=300, q_len=1, seq_lo=1, seq_hi=6000, bt_width=47, seed=19)
     check(iw, 1, 2)
+
+
+@pytest.mark.parametrize("R", [5, 600])
+def test_a_wait_that_runs_out_is_reported_and_the_next_call_is_correct(R):
+    # PA_FLAG_TEST_WAIT_TIMEOUT: the score warps also wait on a barrier
+    # nothing arrives on (200 us limit); every CTA stops, no scored key is
+    # written, PA_DEV_WAIT_TIMEOUT comes back, and a normal call after it (the
+    # persistent kernel at R = 5, the per-request grid at R = 600) is exact
+    from indexer_projection_gb300 import binding as B
+
+    iw = workloads.IndexWorkload(f"ixto{R}", R=R, q_len=2, seq_lo=200, seq_hi=1500, bt_width=12, seed=70 + R)
+    st = workloads.index_host_state(iw)
+    scale = float(np.float32(oracle.index_scale_log2e(iw.sm_scale)))
+    cols = st["block_table"].shape[1] * 128
+    got, status = run_gpu(iw, st, 1, 1, scale, cols, flags=B.PA_FLAG_TEST_WAIT_TIMEOUT)
+    assert status & B.PA_DEV_WAIT_TIMEOUT
+    want = oracle.index_scores(st["iq"][:, iw.head * 128:(iw.head + 1) * 128], st["index_cache"],
+                               st["block_table"], st["seq_lens"], iw.q_len, 1, 1, scale, cols)
+    scored = np.isfinite(want)
+    assert not np.any(np.isfinite(got) & scored)  # no scored key was written
+    check(iw, 1, 1)
