@@ -62,7 +62,9 @@ constexpr int kDaStages = 2;              // K + V stages
 constexpr int kDaThreads = 192;           // warp 0 TMA, warp 1 MMA + TMEM, warps 2..5 softmax
 constexpr uint32_t kDaTmemCols = 256;     // S at column 0, O at column 128
 constexpr int kDaOCol = 128;
-constexpr int64_t kDaPartBytes = 2 * 128 * 4 + 128 * 128 * 4;  // m[128], l[128], o[128][128] f32
+// a partition's (m, l, o): m[128], l[128] f32, then o as [32 dim quads][128 rows] float4 (a row's
+// quad q at float4 index 128 q + row: the threads of a row each store 16 contiguous bytes a quad)
+constexpr int64_t kDaPartBytes = 2 * 128 * 4 + 128 * 128 * 4;
 constexpr int kDaQkvThreads = 256;
 
 // shared memory (from a 1024-byte aligned base)
@@ -454,10 +456,10 @@ __global__ void __launch_bounds__(kDaThreads, 2)
       float o[64];
       tc_ld64(trow + kDaOCol + 64 * hf, o);
       tc_wait_ld();
-      if (live) {
-        float4 *dst = reinterpret_cast<float4 *>(pp + 1024 + row * 512 + hf * 256);
+      if (live) {  // quad-major: a warp's 32 rows of a quad are 512 contiguous bytes
+        float4 *dst = reinterpret_cast<float4 *>(pp + 1024) + (16 * hf) * 128 + row;
 #pragma unroll
-        for (int q = 0; q < 16; ++q) dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+        for (int q = 0; q < 16; ++q) dst[q * 128] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
       }
     }
     if (live) {
@@ -517,9 +519,9 @@ __global__ void __launch_bounds__(kDaMergeThreads) pa_drafter_merge_kernel(AttnP
       const uint8_t *pi = pr + (int64_t)(in ? i0 + u : 0) * kDaPartBytes;
       mi[u] = in ? __ldcg(reinterpret_cast<const float *>(pi) + row) : -INFINITY;
       li[u] = in ? __ldcg(reinterpret_cast<const float *>(pi + 512) + row) : 0.f;
-      const float4 *o = reinterpret_cast<const float4 *>(pi + 1024 + row * 512 + piece * 64);
+      const float4 *o = reinterpret_cast<const float4 *>(pi + 1024) + (4 * piece) * 128 + row;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) oi[u][q] = in ? __ldcg(o + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int q = 0; q < 4; ++q) oi[u][q] = in ? __ldcg(o + q * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int u = 0; u < kDaMergeBatch; ++u) {  // in partition order
