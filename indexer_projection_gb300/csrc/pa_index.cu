@@ -102,6 +102,61 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint3
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// The f16 variant.  Every E4M3 code is an f16 value, so a key converts in one
+// instruction a pair (cvt.rn.f16x2.e4m3x2) instead of four through f32 and
+// bf16; a bf16 query value is an f16 value when it is 0 or 2^-17 <= |x| <
+// 2^15 (its 8 significant bits then sit on the f16 grid), so where every
+// query value of a warp's fragments is, the products and the f32 sums are
+// those of the bf16 MMA.  Otherwise (a value outside that range) the warp
+// keeps the bf16 path for the request.
+__device__ __forceinline__ void mma_f16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint2 e4m3x4_to_f16x4(uint32_t w) {
+  uint32_t h[2];
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h[0]) : "h"((uint16_t)(w & 0xffffu)));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h[1]) : "h"((uint16_t)(w >> 16)));
+  return make_uint2(h[0], h[1]);
+}
+__device__ __forceinline__ bool bf16_on_f16_grid(uint32_t b) {  // b: 16 bf16 bits
+  const uint32_t e = (b >> 7) & 0xffu;
+  return (b & 0x7fffu) == 0 || (e >= 127 - 17 && e < 127 + 15);
+}
+// The query fragments of a thread as f16 pairs, in place, when every value
+// of the warp's fragments is on the f16 grid; returns whether they are.
+template <int NT>
+__device__ __forceinline__ bool q_to_f16(uint2 (&qf)[NT][8]) {
+  bool ok = true;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int pc = 0; pc < 8; ++pc) {
+      const uint32_t w[2] = {qf[nt][pc].x, qf[nt][pc].y};
+#pragma unroll
+      for (int u = 0; u < 2; ++u) ok &= bf16_on_f16_grid(w[u] & 0xffffu) & bf16_on_f16_grid(w[u] >> 16);
+    }
+  ok = __all_sync(0xffffffffu, ok);
+  if (ok) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int pc = 0; pc < 8; ++pc) {
+        uint32_t w[2] = {qf[nt][pc].x, qf[nt][pc].y};
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const float lo = bf16_to_f32(w[u] & 0xffffu), hi = bf16_to_f32(w[u] >> 16);
+          asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(w[u]) : "f"(hi), "f"(lo));
+        }
+        qf[nt][pc] = make_uint2(w[0], w[1]);
+      }
+  }
+  return ok;
+}
+
 // Whether row (position p, nb = p / 128 + 1) takes a score in block b, and
 // whether block b is one of its blocks at all.
 __device__ __forceinline__ bool row_has_block(int64_t p, int b) { return p >= 0 && b <= p / 128; }
@@ -168,6 +223,7 @@ __global__ void __launch_bounds__(kIdxThreads) pa_index_scores_kernel(const __gr
     for (int pc = 0; pc < 8; ++pc)
       qf[nt][pc] = i < a.q_len ? *reinterpret_cast<const uint2 *>(row + 16 * pc + 4 * t) : make_uint2(0u, 0u);
   }
+  const bool qh = q_to_f16<NT>(qf);
   // rows of this thread's accumulator columns: 2t, 2t + 1 of each n8 tile
   int64_t prow[NT][2];
 #pragma unroll
@@ -202,12 +258,22 @@ __global__ void __launch_bounds__(kIdxThreads) pa_index_scores_kernel(const __gr
           uint32_t m[4];
           const int chunk = 2 * L + (lane >> 4);
           ldmatrix_x4(rowaddr + ((chunk ^ (key & 7)) << 4), m);
-          const uint2 k0 = e4m3x4_to_bf16x4(m[0]), k1 = e4m3x4_to_bf16x4(m[1]);  // keys g, g + 8: half 0
-          const uint2 k2 = e4m3x4_to_bf16x4(m[2]), k3 = e4m3x4_to_bf16x4(m[3]);  // half 1
+          if (qh) {
+            const uint2 k0 = e4m3x4_to_f16x4(m[0]), k1 = e4m3x4_to_f16x4(m[1]);  // keys g, g + 8: half 0
+            const uint2 k2 = e4m3x4_to_f16x4(m[2]), k3 = e4m3x4_to_f16x4(m[3]);  // half 1
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            mma_bf16_16816(c[nt], k0.x, k1.x, k0.y, k1.y, qf[nt][2 * L].x, qf[nt][2 * L].y);
-            mma_bf16_16816(c[nt], k2.x, k3.x, k2.y, k3.y, qf[nt][2 * L + 1].x, qf[nt][2 * L + 1].y);
+            for (int nt = 0; nt < NT; ++nt) {
+              mma_f16_16816(c[nt], k0.x, k1.x, k0.y, k1.y, qf[nt][2 * L].x, qf[nt][2 * L].y);
+              mma_f16_16816(c[nt], k2.x, k3.x, k2.y, k3.y, qf[nt][2 * L + 1].x, qf[nt][2 * L + 1].y);
+            }
+          } else {
+            const uint2 k0 = e4m3x4_to_bf16x4(m[0]), k1 = e4m3x4_to_bf16x4(m[1]);
+            const uint2 k2 = e4m3x4_to_bf16x4(m[2]), k3 = e4m3x4_to_bf16x4(m[3]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              mma_bf16_16816(c[nt], k0.x, k1.x, k0.y, k1.y, qf[nt][2 * L].x, qf[nt][2 * L].y);
+              mma_bf16_16816(c[nt], k2.x, k3.x, k2.y, k3.y, qf[nt][2 * L + 1].x, qf[nt][2 * L + 1].y);
+            }
           }
         }
       }
@@ -377,6 +443,7 @@ __global__ void __launch_bounds__(kIxPersistThreads) pa_index_scores_persist_ker
   int j = 0, cur = -1, r = r0;
   uint2 qf[NT][8];
   int64_t prow[NT][2];
+  bool qh = false;  // the fragments hold f16 values
   for (int64_t base = lo; base < hi; base += 32) {
     const Item mine = resolve(base + lane, r);
     r = __shfl_sync(0xffffffffu, mine.r, 31);
@@ -401,6 +468,7 @@ __global__ void __launch_bounds__(kIxPersistThreads) pa_index_scores_persist_ker
             prow[nt][e] = ii < a.q_len ? p_first + ii : -1;
           }
         }
+        qh = q_to_f16<NT>(qf);
       }
       float c[NT][4];
 #pragma unroll
@@ -423,12 +491,22 @@ __global__ void __launch_bounds__(kIxPersistThreads) pa_index_scores_persist_ker
           uint32_t m[4];
           const int chunk = 2 * L + (lane >> 4);
           ldmatrix_x4(rowaddr + ((chunk ^ (key & 7)) << 4), m);
-          const uint2 k0 = e4m3x4_to_bf16x4(m[0]), k1 = e4m3x4_to_bf16x4(m[1]);
-          const uint2 k2 = e4m3x4_to_bf16x4(m[2]), k3 = e4m3x4_to_bf16x4(m[3]);
+          if (qh) {
+            const uint2 k0 = e4m3x4_to_f16x4(m[0]), k1 = e4m3x4_to_f16x4(m[1]);
+            const uint2 k2 = e4m3x4_to_f16x4(m[2]), k3 = e4m3x4_to_f16x4(m[3]);
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            mma_bf16_16816(c[nt], k0.x, k1.x, k0.y, k1.y, qf[nt][2 * L].x, qf[nt][2 * L].y);
-            mma_bf16_16816(c[nt], k2.x, k3.x, k2.y, k3.y, qf[nt][2 * L + 1].x, qf[nt][2 * L + 1].y);
+            for (int nt = 0; nt < NT; ++nt) {
+              mma_f16_16816(c[nt], k0.x, k1.x, k0.y, k1.y, qf[nt][2 * L].x, qf[nt][2 * L].y);
+              mma_f16_16816(c[nt], k2.x, k3.x, k2.y, k3.y, qf[nt][2 * L + 1].x, qf[nt][2 * L + 1].y);
+            }
+          } else {
+            const uint2 k0 = e4m3x4_to_bf16x4(m[0]), k1 = e4m3x4_to_bf16x4(m[1]);
+            const uint2 k2 = e4m3x4_to_bf16x4(m[2]), k3 = e4m3x4_to_bf16x4(m[3]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              mma_bf16_16816(c[nt], k0.x, k1.x, k0.y, k1.y, qf[nt][2 * L].x, qf[nt][2 * L].y);
+              mma_bf16_16816(c[nt], k2.x, k3.x, k2.y, k3.y, qf[nt][2 * L + 1].x, qf[nt][2 * L + 1].y);
+            }
           }
         }
         __syncwarp();

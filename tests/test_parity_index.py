@@ -201,3 +201,26 @@ def test_a_wait_that_runs_out_is_reported_and_the_next_call_is_correct(R):
     scored = np.isfinite(want)
     assert not np.any(np.isfinite(got) & scored)  # no scored key was written
     check(iw, 1, 1)
+
+
+@pytest.mark.parametrize("R", [5, 600])
+def test_query_values_off_the_f16_grid_take_the_bf16_path(R):
+    # a warp's fragments go to f16 MMAs only when every query value is an
+    # f16 value (0, or 2^-17 <= |x| < 2^15); here request 1 has one value of
+    # 40000 and request 3 one of 1e-7 (their warps keep the bf16 path), the
+    # others stay on the f16 path: all scores follow the oracle
+    iw = workloads.IndexWorkload(f"ixgrid{R}", R=R, q_len=3, seq_lo=300, seq_hi=2000, bt_width=16, seed=77)
+    st = workloads.index_host_state(iw)
+    iq = st["iq"].copy()  # bf16 bits
+    big = np.array([40000.0], np.float32).view(np.uint32) >> 16
+    tiny = np.array([1e-7], np.float32).view(np.uint32) >> 16
+    iq[1 * iw.q_len + 1, iw.head * 128 + 5] = np.uint16(big[0])
+    iq[3 * iw.q_len + 0, iw.head * 128 + 77] = np.uint16(tiny[0])
+    st["iq"] = iq
+    scale = float(np.float32(oracle.index_scale_log2e(iw.sm_scale)))
+    cols = st["block_table"].shape[1] * 128
+    got, status = run_gpu(iw, st, 1, 2, scale, cols)
+    assert status == 0
+    want = oracle.index_scores(iq[:, iw.head * 128:(iw.head + 1) * 128], st["index_cache"], st["block_table"],
+                               st["seq_lens"], iw.q_len, 1, 2, scale, cols)
+    assert compare_scores(iw, st, got, want, scale, iq_bits=iq) > 0
