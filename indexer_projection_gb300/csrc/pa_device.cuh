@@ -681,4 +681,66 @@ __device__ __forceinline__ void head_epilogue(const Params &p, const HeadCtx &hc
   publish_done<E>(p, hc, d0);
 }
 
+// The FP8 V rows of a whole warp, a thread a row (the tensor-core epilogues).
+// Every lane of the warp calls it (the warp's head is a V head; `live`:
+// the lane holds a token row).  Each lane takes its row's scale and codes
+// exactly as head_epilogue_stores does; the cache bytes then leave 8 rows x
+// 4 dims an instruction: lane l stores dim 4k + l % 4 of row 8b + l / 4,
+// fetched with one shuffle of the row's code word k.  A V page keeps a dim's
+// 16 tokens together ([128 dims][16 tokens] bytes), so those 32 bytes fall in
+// one 128-byte line of each page the 8 rows touch, where a store of one dim
+// for 32 rows touched a line per page of all 32.  Done words (signal mode)
+// follow every lane's stores.
+__device__ __forceinline__ void v_rows_fp8_warp(const Params &p, const HeadCtx &hc, float (&v)[kHeadDim], bool live) {
+  const int lane = threadIdx.x & 31;
+  const int kvh = hc.head - p.v0;
+  int64_t off = -1;  // byte offset of the row's (page, token) in the V cache; -1: nothing to store
+  float s = 1.0f;
+  if (live && hc.slot >= 0) {
+    const int64_t p16 = page16_of(hc.slot, p.kps);
+    if (p16 >= p.num_pages16) {
+      set_status(p.status, kDevSlotRange);
+    } else {
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < kHeadDim; ++i) amax = fmaxf(amax, fabsf(v[i]));
+      s = p.static_kv ? 1.0f : (amax == 0.f ? 1.0f : __fdiv_rn(amax, kFp8Max));
+      off = (p16 * p.n_kv + kvh) * 2048 + (hc.slot & 15);
+    }
+  }
+  const float rs = __frcp_rn(s);
+  int64_t o[4];  // offsets of the rows this lane stores for: 8b + lane / 4
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const int src = 8 * b + (lane >> 2);
+    o[b] = (int64_t)(((uint64_t)__shfl_sync(0xffffffffu, (uint32_t)((uint64_t)off >> 32), src) << 32) |
+                     __shfl_sync(0xffffffffu, (uint32_t)(uint64_t)off, src));
+  }
+  uint8_t *dst = p.v_cache + 16 * (lane & 3);
+  const int sh = 8 * (lane & 3);
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {  // the row's codes of dims 4k .. 4k + 3, made just before they go out
+    uint32_t w = 0u;
+    if (off >= 0) {
+      bool ok = true;
+      w = e4m3x4_prod_checked(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3], rs, ok);
+      if (__builtin_expect(!ok, 0)) w = e4m3x4_div(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3], s);
+    }
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t x = __shfl_sync(0xffffffffu, w, 8 * b + (lane >> 2));
+      if (o[b] >= 0) dst[o[b] + 64 * k] = (uint8_t)(x >> sh);
+    }
+  }
+  if (off >= 0) p.v_scale[(off >> 11) * 16 + (off & 15)] = s;
+  if (p.done) {
+    __threadfence();
+    __syncwarp();
+    if (live)
+      asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.done + (int64_t)hc.m * p.n_heads + hc.head),
+                   "r"(p.done_epoch)
+                   : "memory");
+  }
+}
+
 }  // namespace pa

@@ -266,8 +266,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         abuf = 0;
         aphase ^= 1;
       }
-      if (!live) continue;
-      if (WFMT == 0) {
+      if (WFMT == 0 && live) {
         const float *wsb = ws_s + (it & 1) * kBN;
 #pragma unroll
         for (int i = 0; i < kBN; ++i) v[i] = v[i] * xs * wsb[i];
@@ -282,6 +281,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       hc.g_k = p.g_k;
       hc.g_iq = p.g_iq;
       hc.g_ik = p.g_ik;
+      if (p.cache_fmt == 0 && nt >= p.v0 && nt < p.iq0) {  // a V head
+        v_rows_fp8_warp(p, hc, v, live);                   // every lane of the warp
+        continue;
+      }
+      if (!live) continue;
       head_epilogue<kBN>(p, hc, v, 0);
     }
   }

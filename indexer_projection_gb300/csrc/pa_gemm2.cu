@@ -349,8 +349,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       named_bar_sync(2 + wg, 128);
       if ((warp & 3) == 0 && lane == 0) arrive_remote_relaxed(tempty0);
       aphase ^= 1;
-      if (!live) continue;
-      if (WFMT == 0) {
+      if (WFMT == 0 && live) {
         const float *wsb = ws_s + ((it & 1) * 2 + wg) * 128;
 #pragma unroll
         for (int i = 0; i < 128; ++i) v[i] = v[i] * xs * wsb[i];
@@ -365,6 +364,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       hc.g_k = p.g_k;
       hc.g_iq = p.g_iq;
       hc.g_ik = p.g_ik;
+      if (p.cache_fmt == 0 && head >= p.v0 && head < p.iq0) {  // the warpgroup's head is a V head
+        v_rows_fp8_warp(p, hc, v, live);                       // every lane of the warp
+        continue;
+      }
+      if (!live) continue;
       head_epilogue<128>(p, hc, v, 0);
     }
   }
