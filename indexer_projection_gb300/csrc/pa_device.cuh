@@ -68,10 +68,24 @@ struct Params {
 // ------------------------------------------------------------ small utils
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+// f32 -> bf16 bits (round to nearest even), one value a conversion.
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
-__device__ __forceinline__ float bf16_round(float f) { return bf16_to_f32(f32_to_bf16_bits(f)); }
+// Two f32 -> two bf16 (round to nearest even), lo in the low half, in one
+// packed conversion (on sm_103a it converts about four times as many values
+// a cycle as the single-value conversion).
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// bf16_round of a pair, through one packed conversion.
+__device__ __forceinline__ void bf16_round2(float a, float b, float &ra, float &rb) {
+  const uint32_t w = bf16x2_bits(a, b);
+  ra = __uint_as_float(w << 16);
+  rb = __uint_as_float(w & 0xffff0000u);
+}
 
 // Two f32 -> two E4M3 (round to nearest even, saturate to +-448); lo in the low byte.
 __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
@@ -475,8 +489,15 @@ __device__ __forceinline__ void head_epilogue_stores(const Params &p, const Head
     // quarter of the store transactions of 4-byte pieces); a warp holding a
     // row (E = 4) already writes it contiguously
     if (ob) {
+      // A thread holding a whole row (the tensor-core epilogues, which run
+      // beside the next tile's K loop) converts one value at a time: with the
+      // packed conversion that epilogue was faster but the prefill GEMM 4%
+      // slower (measured on the same GPU; the cause was not pinned down)
       auto bf2 = [&](int i) {
-        return (uint32_t)f32_to_bf16_bits(v[i]) | ((uint32_t)f32_to_bf16_bits(v[i + 1]) << 16);
+        if constexpr (E >= 8)
+          return (uint32_t)f32_to_bf16_bits(v[i]) | ((uint32_t)f32_to_bf16_bits(v[i + 1]) << 16);
+        else
+          return bf16x2_bits(v[i], v[i + 1]);
       };
       if constexpr (E >= 8) {
 #pragma unroll
@@ -517,7 +538,10 @@ __device__ __forceinline__ void head_epilogue_stores(const Params &p, const Head
       }
       uint8_t *dst = p.index_cache + slot * kHeadDim + d0;
       auto ik4 = [&](int i) {
-        return e4m3x4(bf16_round(v[i]), bf16_round(v[i + 1]), bf16_round(v[i + 2]), bf16_round(v[i + 3]));
+        float a, b, c, d;
+        bf16_round2(v[i], v[i + 1], a, b);
+        bf16_round2(v[i + 2], v[i + 3], c, d);
+        return e4m3x4(a, b, c, d);
       };
       if constexpr (E >= 16) {
 #pragma unroll
@@ -547,11 +571,16 @@ __device__ __forceinline__ void head_epilogue_stores(const Params &p, const Head
       // codes of 4 K values (bf16 first), the true quotient only where the
       // product's code is not certain
       auto k4 = [&](int i, bool &ok) {
-        return e4m3x4_prod_checked(bf16_round(v[i]), bf16_round(v[i + 1]), bf16_round(v[i + 2]), bf16_round(v[i + 3]),
-                                   rs, ok);
+        float a, b, c, d;
+        bf16_round2(v[i], v[i + 1], a, b);
+        bf16_round2(v[i + 2], v[i + 3], c, d);
+        return e4m3x4_prod_checked(a, b, c, d, rs, ok);
       };
       auto k4_div = [&](int i) {
-        return e4m3x4_div(bf16_round(v[i]), bf16_round(v[i + 1]), bf16_round(v[i + 2]), bf16_round(v[i + 3]), s);
+        float a, b, c, d;
+        bf16_round2(v[i], v[i + 1], a, b);
+        bf16_round2(v[i + 2], v[i + 3], c, d);
+        return e4m3x4_div(a, b, c, d, s);
       };
       if constexpr (E >= 16) {  // 16 dims: one 16-byte row of the page's 16 x 16 block
 #pragma unroll

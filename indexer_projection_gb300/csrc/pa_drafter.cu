@@ -543,11 +543,11 @@ __global__ void __launch_bounds__(kDaMergeThreads) pa_drafter_merge_kernel(AttnP
 #pragma unroll
   for (int e = 0; e < 16; e += 2) {
     const float x0 = L > 0.f ? acc[e] / L : 0.f, x1 = L > 0.f ? acc[e + 1] / L : 0.f;
-    const uint16_t h0 = f32_to_bf16_bits(x0), h1 = f32_to_bf16_bits(x1);
-    acc[e] = bf16_to_f32(h0);
-    acc[e + 1] = bf16_to_f32(h1);
+    const uint32_t h = bf16x2_bits(x0, x1);
+    acc[e] = __uint_as_float(h << 16);
+    acc[e + 1] = __uint_as_float(h & 0xffff0000u);
     amax = fmaxf(amax, fmaxf(fabsf(acc[e]), fabsf(acc[e + 1])));
-    bw[e >> 1] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+    bw[e >> 1] = h;
   }
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
   const int e = mx_exponent(amax);

@@ -123,7 +123,7 @@ __device__ __forceinline__ void acc8(uint4 a, uint4 r, float (&acc)[8], uint4 &r
     float hi = bf16_to_f32(aw[i] >> 16) + bf16_to_f32(rw[i] >> 16);
     acc[2 * i] = lo;
     acc[2 * i + 1] = hi;
-    ow[i] = (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
+    ow[i] = bf16x2_bits(lo, hi);
     float q, ql;
     two_prod(lo, lo, q, ql);
     dd_add(ss, ss_lo, q, ql);
