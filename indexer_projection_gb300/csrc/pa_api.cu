@@ -365,7 +365,7 @@ int pre_attn_run(pa_handle *h, int M, const pa_step_inputs *in, const pa_weights
     e = pa::launch_prologue_rows(p, pdl, s);
     if (e != cudaSuccess) return cuda_fail(e);
   } else if (!gemv) {
-    e = pa::launch_prologue(p, c.weight_format == PA_WEIGHT_MXFP8 ? L.m_pad : M, pdl, s);
+    e = pa::launch_prologue(p, c.weight_format == PA_WEIGHT_MXFP8 ? L.m_pad : M, pdl, h->num_sms, s);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   if (h->prof_before && (e = cudaEventRecord(h->prof_before, s)) != cudaSuccess) return cuda_fail(e);

@@ -45,7 +45,7 @@ inline int current_device_sms() {
 }
 
 // Prologue over `grid` CTAs (M rows, plus padding rows of the MXFP8 scale grid).
-cudaError_t launch_prologue(const Params &p, int grid, bool pdl, cudaStream_t stream);
+cudaError_t launch_prologue(const Params &p, int grid, bool pdl, int num_sms, cudaStream_t stream);
 // Prologue of the skinny path: one thread-block cluster per row (M <= 16).
 cudaError_t launch_prologue_rows(const Params &p, bool pdl, cudaStream_t stream);
 // Row-major [rows, ksf] E8M0 -> F8_128x4 layout.

@@ -25,13 +25,19 @@ namespace pa {
 // the row is done sooner.
 // The tensor-core kernel that follows is launched when every CTA of this
 // grid has passed its trigger, and it takes a whole SM's registers and
-// shared memory for its CTA: the trigger comes after the row's work, so its
-// CTAs do not take SMs this grid's remaining rows still need (a trigger at
-// the start let them do that and stretched a 448-row prologue fourfold).
+// shared memory for its CTA.  A grid of more than one wave triggers after
+// the row's work (use_pdl 1), so the GEMM's CTAs do not take SMs this grid's
+// later rows still need (a trigger at the start let them do that and
+// stretched a two-wave 448-row prologue fourfold).  A grid resident all at
+// once with at most two CTAs an SM triggers at its start (use_pdl 2): the
+// GEMM's CTAs then take each SM as its rows finish and set up while the rest
+// run (measured: 256 rows 35.6 -> 34.3 us a step; at 448 rows, three CTAs on
+// most SMs, the early trigger was slower, 33.2 against 32.7 us).
 template <int WFMT, int NTHR, int MAXC>
 __global__ void __launch_bounds__(NTHR) pa_prologue_kernel(Params p, int use_pdl) {
   __shared__ float2 red2[NTHR / 32];
   if (use_pdl) pdl_wait();
+  if (use_pdl == 2) pdl_trigger();
   const int m = blockIdx.x;
   const int ksf = p.H >> 5;
   if (m >= p.M) {  // MXFP8 padding rows of the tensor-core path: scale 1, codes unused
@@ -40,7 +46,7 @@ __global__ void __launch_bounds__(NTHR) pa_prologue_kernel(Params p, int use_pdl
   } else {
     norm_quant_row<WFMT, NTHR, MAXC>(p, m, red2);
   }
-  if (use_pdl) pdl_trigger();
+  if (use_pdl == 1) pdl_trigger();
 }
 
 // One cluster of C CTAs per token row (blockIdx.x / C); CTA r takes the
@@ -183,26 +189,37 @@ __global__ void pa_pack_scales_kernel(const uint8_t *src, uint8_t *dst, int rows
 }
 
 namespace {
-// H <= 16384: 1024 threads need at most 2 chunks, 256 threads at most 8
-cudaError_t launch_1024(const Params &p, cudaLaunchConfig_t &cfg, bool pdl) {
-  cfg.blockDim = dim3(1024);
-  const bool mx = p.weight_fmt == 1;
-  if (mx) return cudaLaunchKernelEx(&cfg, pa_prologue_kernel<1, 1024, 2>, p, (int)pdl);  // (one chunk spills)
-  if (p.H <= 8 * 1024) return cudaLaunchKernelEx(&cfg, pa_prologue_kernel<0, 1024, 1>, p, (int)pdl);
-  return cudaLaunchKernelEx(&cfg, pa_prologue_kernel<0, 1024, 2>, p, (int)pdl);
+using ProKernel = void (*)(Params, int);
+// use_pdl for the launch: 0 without PDL; 2 where the whole grid is resident
+// at once with at most two CTAs an SM, else 1.
+int trigger_mode(ProKernel kern, const cudaLaunchConfig_t &cfg, bool pdl, int num_sms) {
+  if (!pdl) return 0;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, (int)cfg.blockDim.x, 0) != cudaSuccess) {
+    cudaGetLastError();  // not resolved: the safe choice
+    return 1;
+  }
+  return (int64_t)(per_sm < 2 ? per_sm : 2) * num_sms >= (int64_t)cfg.gridDim.x ? 2 : 1;
 }
-cudaError_t launch_256(const Params &p, cudaLaunchConfig_t &cfg, bool pdl) {
-  cfg.blockDim = dim3(256);
+cudaError_t launch_k(ProKernel kern, const Params &p, cudaLaunchConfig_t &cfg, bool pdl, int num_sms) {
+  return cudaLaunchKernelEx(&cfg, kern, p, trigger_mode(kern, cfg, pdl, num_sms));
+}
+// H <= 16384: 1024 threads need at most 2 chunks, 256 threads at most 8
+ProKernel kernel_1024(const Params &p) {
+  if (p.weight_fmt == 1) return pa_prologue_kernel<1, 1024, 2>;  // (one chunk spills)
+  return p.H <= 8 * 1024 ? pa_prologue_kernel<0, 1024, 1> : pa_prologue_kernel<0, 1024, 2>;
+}
+ProKernel kernel_256(const Params &p) {
   const int maxc = (p.H + 8 * 256 - 1) / (8 * 256);
   const bool mx = p.weight_fmt == 1;
-  if (maxc <= 2) return cudaLaunchKernelEx(&cfg, mx ? pa_prologue_kernel<1, 256, 2> : pa_prologue_kernel<0, 256, 2>, p, (int)pdl);
-  if (maxc <= 3) return cudaLaunchKernelEx(&cfg, mx ? pa_prologue_kernel<1, 256, 3> : pa_prologue_kernel<0, 256, 3>, p, (int)pdl);
-  if (maxc <= 4) return cudaLaunchKernelEx(&cfg, mx ? pa_prologue_kernel<1, 256, 4> : pa_prologue_kernel<0, 256, 4>, p, (int)pdl);
-  return cudaLaunchKernelEx(&cfg, mx ? pa_prologue_kernel<1, 256, 8> : pa_prologue_kernel<0, 256, 8>, p, (int)pdl);
+  if (maxc <= 2) return mx ? pa_prologue_kernel<1, 256, 2> : pa_prologue_kernel<0, 256, 2>;
+  if (maxc <= 3) return mx ? pa_prologue_kernel<1, 256, 3> : pa_prologue_kernel<0, 256, 3>;
+  if (maxc <= 4) return mx ? pa_prologue_kernel<1, 256, 4> : pa_prologue_kernel<0, 256, 4>;
+  return mx ? pa_prologue_kernel<1, 256, 8> : pa_prologue_kernel<0, 256, 8>;
 }
 }  // namespace
 
-cudaError_t launch_prologue(const Params &p, int grid, bool pdl, cudaStream_t stream) {
+cudaError_t launch_prologue(const Params &p, int grid, bool pdl, int num_sms, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3(grid);
@@ -213,7 +230,9 @@ cudaError_t launch_prologue(const Params &p, int grid, bool pdl, cudaStream_t st
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   // fewer rows than a fraction of the SMs: the row latency is the step's
-  return grid <= 64 ? launch_1024(p, cfg, pdl) : launch_256(p, cfg, pdl);
+  const bool wide = grid <= 64;
+  cfg.blockDim = dim3(wide ? 1024 : 256);
+  return launch_k(wide ? kernel_1024(p) : kernel_256(p), p, cfg, pdl, num_sms);
 }
 
 namespace {
