@@ -78,6 +78,46 @@ def test_long_k_and_outliers(tiles):
           flags=_flags(tiles=tiles))
 
 
+@pytest.mark.parametrize("tiles", TILES)
+def test_skipped_slots_static_scale_separate_index_slots(tiles):
+    # skipped rows scattered over several warps (the V rows leave a warp at a
+    # time, so a warp mixes rows with and without a slot), K / V scales fixed
+    # at 1, index_k rows in their own slots
+    check(small(f"g_skip_{tiles}", 200, "ptpc", "fp8", nkv=2, seed=31, skip_rows=(0, 5, 6, 37, 64, 130, 199),
+                static_kv_scale=True, separate_index_slots=True), flags=_flags(tiles=tiles))
+
+
+@pytest.mark.parametrize("tiles", TILES)
+def test_kv_page_stride_16(tiles):
+    wl = small(f"g_kps16_{tiles}", 150, "mx", "fp8", nkv=2, seed=32, kv_page_stride=16, pool_pages16=256)
+    st = workloads.host_state(wl)
+    # distinct slots below 128 * 16, so page16 ids stay below 256
+    st["slot_mapping"] = np.random.default_rng(32).permutation(128 * 16)[:wl.M].astype(np.int64)
+    g = harness.GpuRun(wl, st, flags=_flags(tiles=tiles))
+    g.run()
+    ref = harness.oracle_run(wl, st, range(wl.M))
+    harness.compare(wl, g.results(), ref, range(wl.M))
+    assert g.runner.device_status() == 0
+
+
+@pytest.mark.parametrize("tiles", TILES)
+def test_out_of_range_slots_are_flagged_not_written(tiles):
+    from indexer_projection_gb300 import binding as B
+    wl = small(f"g_oor_{tiles}", 140, "ptpc", "fp8", nkv=2, seed=33)
+    st = workloads.host_state(wl)
+    bad = (1, 40, 139)
+    for m in bad:
+        st["slot_mapping"][m] = wl.num_pages16 * 16 + 5 + m  # beyond the cache
+        st["index_slot_mapping"][m] = wl.num_index_slots + 9 + m
+    g = harness.GpuRun(wl, st, flags=_flags(tiles=tiles))
+    g.run()
+    got = g.results()
+    assert g.runner.device_status() == B.PA_DEV_SLOT_RANGE
+    ok_rows = [m for m in range(wl.M) if m not in bad]
+    ref = harness.oracle_run(wl, st, ok_rows)
+    harness.compare(wl, got, ref, ok_rows, all_rows=ok_rows)
+
+
 def test_spec_decode_config():
     check(workloads.spec_decode(), flags=0)
 
