@@ -18,6 +18,8 @@ struct pa_handle {
   int device;   // device of the cached SM count (-1: not queried yet)
   int num_sms;
   int64_t l2_bytes;
+  int early_max[2];  // many-row prologue (256 / 1024 threads a CTA): the largest grid resident
+                     // at once with at most two CTAs an SM (it then triggers the GEMM early)
   cudaEvent_t prof_before, prof_after;  // optional events around the main kernel
 };
 
@@ -75,6 +77,12 @@ cudaError_t query_sms(pa_handle *h) {
     if (e != cudaSuccess) return e;
     h->num_sms = sms;
     h->l2_bytes = l2;
+    for (int wide = 0; wide < 2; ++wide) {
+      int per_sm = 0;
+      e = pa::prologue_ctas_per_sm(h->cfg.hidden, h->cfg.weight_format == PA_WEIGHT_MXFP8 ? 1 : 0, wide != 0, &per_sm);
+      if (e != cudaSuccess) return e;
+      h->early_max[wide] = (per_sm < 2 ? per_sm : 2) * sms;
+    }
     h->device = dev;
   }
   return cudaSuccess;
@@ -178,6 +186,7 @@ int pre_attn_init(const pa_config *cfg, pa_handle **out) {
   h->device = -1;
   h->num_sms = 0;
   h->l2_bytes = 0;
+  h->early_max[0] = h->early_max[1] = 0;
   h->prof_before = h->prof_after = nullptr;
   *out = h;
   return PA_OK;
@@ -365,7 +374,8 @@ int pre_attn_run(pa_handle *h, int M, const pa_step_inputs *in, const pa_weights
     e = pa::launch_prologue_rows(p, pdl, s);
     if (e != cudaSuccess) return cuda_fail(e);
   } else if (!gemv) {
-    e = pa::launch_prologue(p, c.weight_format == PA_WEIGHT_MXFP8 ? L.m_pad : M, pdl, h->num_sms, s);
+    const int grid = c.weight_format == PA_WEIGHT_MXFP8 ? L.m_pad : M;
+    e = pa::launch_prologue(p, grid, pdl, h->early_max[grid <= 64 ? 1 : 0], s);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   if (h->prof_before && (e = cudaEventRecord(h->prof_before, s)) != cudaSuccess) return cuda_fail(e);

@@ -45,7 +45,12 @@ inline int current_device_sms() {
 }
 
 // Prologue over `grid` CTAs (M rows, plus padding rows of the MXFP8 scale grid).
-cudaError_t launch_prologue(const Params &p, int grid, bool pdl, int num_sms, cudaStream_t stream);
+// A grid of at most early_max CTAs triggers the next kernel's launch at its
+// start, a larger one after its rows' work.
+cudaError_t launch_prologue(const Params &p, int grid, bool pdl, int early_max, cudaStream_t stream);
+// CTAs an SM holds of the prologue kernel launch_prologue picks for H, the
+// weight format and the grid width (wide: grid <= 64, 1024 threads a CTA).
+cudaError_t prologue_ctas_per_sm(int H, int weight_fmt, bool wide, int *per_sm);
 // Prologue of the skinny path: one thread-block cluster per row (M <= 16).
 cudaError_t launch_prologue_rows(const Params &p, bool pdl, cudaStream_t stream);
 // Row-major [rows, ksf] E8M0 -> F8_128x4 layout.

@@ -190,20 +190,6 @@ __global__ void pa_pack_scales_kernel(const uint8_t *src, uint8_t *dst, int rows
 
 namespace {
 using ProKernel = void (*)(Params, int);
-// use_pdl for the launch: 0 without PDL; 2 where the whole grid is resident
-// at once with at most two CTAs an SM, else 1.
-int trigger_mode(ProKernel kern, const cudaLaunchConfig_t &cfg, bool pdl, int num_sms) {
-  if (!pdl) return 0;
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, (int)cfg.blockDim.x, 0) != cudaSuccess) {
-    cudaGetLastError();  // not resolved: the safe choice
-    return 1;
-  }
-  return (int64_t)(per_sm < 2 ? per_sm : 2) * num_sms >= (int64_t)cfg.gridDim.x ? 2 : 1;
-}
-cudaError_t launch_k(ProKernel kern, const Params &p, cudaLaunchConfig_t &cfg, bool pdl, int num_sms) {
-  return cudaLaunchKernelEx(&cfg, kern, p, trigger_mode(kern, cfg, pdl, num_sms));
-}
 // H <= 16384: 1024 threads need at most 2 chunks, 256 threads at most 8
 ProKernel kernel_1024(const Params &p) {
   if (p.weight_fmt == 1) return pa_prologue_kernel<1, 1024, 2>;  // (one chunk spills)
@@ -219,7 +205,16 @@ ProKernel kernel_256(const Params &p) {
 }
 }  // namespace
 
-cudaError_t launch_prologue(const Params &p, int grid, bool pdl, int num_sms, cudaStream_t stream) {
+// CTAs an SM holds of the kernel launch_prologue picks for these sizes.
+cudaError_t prologue_ctas_per_sm(int H, int weight_fmt, bool wide, int *per_sm) {
+  Params p{};
+  p.H = H;
+  p.weight_fmt = weight_fmt;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, wide ? kernel_1024(p) : kernel_256(p), wide ? 1024 : 256,
+                                                       0);
+}
+
+cudaError_t launch_prologue(const Params &p, int grid, bool pdl, int early_max, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3(grid);
@@ -232,7 +227,8 @@ cudaError_t launch_prologue(const Params &p, int grid, bool pdl, int num_sms, cu
   // fewer rows than a fraction of the SMs: the row latency is the step's
   const bool wide = grid <= 64;
   cfg.blockDim = dim3(wide ? 1024 : 256);
-  return launch_k(wide ? kernel_1024(p) : kernel_256(p), p, cfg, pdl, num_sms);
+  const int mode = !pdl ? 0 : grid <= early_max ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, wide ? kernel_1024(p) : kernel_256(p), p, mode);
 }
 
 namespace {
