@@ -314,23 +314,34 @@ def path_info(B, path):
     return name, desc, launches
 
 
-def build_graphs(torch, dw, n_steps, stream, events=None):
-    """CUDA graphs holding exactly n_steps steps (chunks of at most 4096).
-    With `events` (a start / end pair, n_steps <= 4096): recorded as the first
-    and last nodes of the one graph, so they bracket exactly the steps'
-    device execution and not the graph's launch."""
+def build_graphs(torch, dw, n_steps, stream, events=None, lead=0):
+    """CUDA graphs holding exactly n_steps timed steps (chunks of at most
+    4096).  With `events` (a start / end pair, n_steps <= 4096) the one graph
+    holds `lead` untimed warm-up steps, then the start event, the n_steps
+    steps and the end event, so the events bracket exactly the steps' device
+    execution and not the graph's launch.  The start event is recorded on a
+    branch that waits for the last warm-up step: the main chain keeps its
+    programmatic (PDL) edge into the first timed step, which therefore runs as
+    every later one does, and the region is the span from the end of the
+    last warm-up step to the end of the last timed one (n_steps step
+    periods)."""
     G = min(n_steps, 4096)
     full, rest = divmod(n_steps, G)
     graphs = []
+    side = torch.cuda.Stream(stream.device) if events else None
     for n in [G] * min(full, 1) + ([rest] if rest else []):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             if events:
-                events[0].record(stream)
+                for i in range(lead):
+                    dw.step(i, stream)
+                side.wait_stream(stream)
+                events[0].record(side)
             for i in range(n):
-                dw.step(i, stream)
+                dw.step(lead + i if events else i, stream)
             if events:
                 events[1].record(stream)
+                stream.wait_stream(side)
         graphs.append(g)
     order = [graphs[0]] * full + ([graphs[-1]] if rest else [])
     return graphs, order
@@ -394,7 +405,7 @@ def measure(args, wl, dev, world, K, W, min_seconds=0.0, flags=0):
     inside = K <= 4096 and min_seconds <= 0
     ev_in = ((torch.cuda.Event(enable_timing=True, external=True),
               torch.cuda.Event(enable_timing=True, external=True)) if inside else None)
-    graphs, order = build_graphs(torch, dw, K, stream, events=ev_in)
+    graphs, order = build_graphs(torch, dw, K, stream, events=ev_in, lead=max(W, 3) if inside else 0)
     with torch.cuda.stream(stream):
         for g in graphs:  # untimed replay: instantiation / first-launch costs
             g.replay()
@@ -924,8 +935,10 @@ def run_ours(args, wl, rank, world, local_rank):
         "path": desc,
         "l2": f"inputs larger than L2: {m['copies']} rotating weight+input copies "
               f"({m['copies'] * m['per_copy'] / 1e6:.0f} MB > 2x L2), no flush",
-        "timing": ("CUDA events recorded as the first and last nodes of one CUDA graph of exactly K steps "
-                   "(PDL chained), replayed once between synchronizes" if m["events_inside"] else
+        "timing": ("one CUDA graph replayed once between synchronizes: max(W, 3) untimed warm-up steps, "
+                   "then exactly K timed steps (PDL chained) between two CUDA event nodes; the start event "
+                   "waits, on a side branch, for the last warm-up step, so the region is K step periods "
+                   "from the end of that step to the end of the last timed one" if m["events_inside"] else
                    "CUDA events around CUDA graphs of exactly K steps in all (PDL chained)"),
         "roofline": roofline(B, wl, kname, m, peaks, peak_src, args.workload),
         "step_hbm_frac": round(nb["step"] / (ms_step * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
