@@ -632,7 +632,7 @@ def secondary(args, name, dev, world, peaks, peak_src):
     from indexer_projection_gb300 import binding as B
 
     wl = get_workload(name)
-    K2 = max(20, min(args.steps, 200))
+    K2 = 200  # a graph of this many steps, replayed for at least a second (few graph boundaries)
     m = measure(args, wl, dev, world, K2, max(3, args.warmup), min_seconds=1.0)
     kname, desc, _ = path_info(B, m["path"])
     ms = m["ms"]
