@@ -923,7 +923,7 @@ def run_ours(args, wl, rank, world, local_rank):
     K, W = args.steps, args.warmup
     m = measure(args, wl, dev, world, K, W, flags=flags)
     kname, desc, launches = path_info(B, m["path"])
-    e2e = end_to_end(torch, wl, m["st"], m["dw"], m["stream"], min(K, 2000), world, dev)
+    e2e = end_to_end(torch, wl, m["st"], m["dw"], m["stream"], min(max(K, 200), 2000), world, dev)
     ms_step = m["ms"]
     nb = step_bytes(wl)
     line = {
