@@ -111,10 +111,6 @@ __device__ __forceinline__ uint8_t e2m1x2(float lo, float hi) {
 }
 // f32 product rounded toward zero ([EPI] _nvfp4_quant32).
 __device__ __forceinline__ float mul_rz(float a, float b) { return __fmul_rz(a, b); }
-// E8M0 code -> f32 power of two (code 0 -> 2^-127, a subnormal).
-__device__ __forceinline__ float e8m0_to_f32(uint32_t c) {
-  return c == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(c << 23);
-}
 
 __device__ __forceinline__ void set_status(uint32_t *st, uint32_t bit) { atomicOr(st, bit); }
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
@@ -126,9 +122,6 @@ __device__ __forceinline__ int64_t ld_i64(const int64_t *p) { return __ldg(p); }
 // It orders nothing and changes no value a later load returns, so it may be
 // issued for an input before the wait on the kernel that produces it.
 __device__ __forceinline__ void prefetch_l2(const void *p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
-__device__ __forceinline__ void st_release(int *p, int v) {
-  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 
 // Offset of (row r, K-block kb) in the F8_128x4 scale layout ([EPI]
 // prepare_SF): [R/128, Ksf/4, 32, 4, 4].
@@ -230,21 +223,14 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
-// Arrive (release at cluster scope) on an mbarrier given by its cluster address.
-__device__ __forceinline__ void arrive_remote(uint32_t caddr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
-}
-// The same without release semantics, for an arrival that orders nothing in
-// memory the waiter reads (a tensor-memory accumulator freed after
-// tcgen05.wait::ld and tcgen05.fence::before_thread_sync): a release there
-// waits until every earlier store of the thread is performed at cluster
-// scope, which behind an epilogue's global stores takes microseconds.
+// Arrive on an mbarrier given by its cluster address, without release
+// semantics: for an arrival that orders nothing in memory the waiter reads
+// (a tensor-memory accumulator freed after tcgen05.wait::ld and
+// tcgen05.fence::before_thread_sync).  A release there would wait until every
+// earlier store of the thread is performed at cluster scope, which behind an
+// epilogue's global stores takes microseconds.
 __device__ __forceinline__ void arrive_remote_relaxed(uint32_t caddr) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
-}
-__device__ __forceinline__ void st_cluster_v4(uint32_t caddr, float4 v) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(caddr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
-               : "memory");
 }
 // Asynchronous store of 16 bytes into the shared memory of a CTA of the
 // cluster; its completion counts 16 bytes on that CTA's mbarrier `cbar`
